@@ -1,0 +1,185 @@
+"""Float64 CPU oracle for the routed NVFP4 MoE FFN -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+package never imports it and has no CPU fallback.  The arithmetic lives in
+``moe_oracle.c`` (plain C, float64, single thread); this module only compiles it
+with gcc and marshals numpy arrays through ctypes.
+
+Each function names the passage it follows in ``moe_oracle.c``.  Parity pins
+(tests under ``tests/test_oracle_*.py``) tie it to things other than itself:
+the pages' byte count per expert, library decodes of e4m3/bf16, the e2m1 value
+set, brute-force routing, closed-form experts, invariants and an independent
+float64 torch composition.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_ARG, ERR_NAN_SCALE, ERR_BAD_ID = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into a shared library (gcc, -O2, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC",
+                           "-shared", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64 = ctypes.c_int, ctypes.c_int64
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_value.restype = ctypes.c_double
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_value.restype = ctypes.c_double
+            lib.oracle_expert_bytes.argtypes = [i64, i64]
+            lib.oracle_expert_bytes.restype = ctypes.c_uint64
+            lib.oracle_dequant.argtypes = [P, P, ctypes.c_float, i64, i64, P]
+            lib.oracle_dequant.restype = i32
+            lib.oracle_router_logits.argtypes = [i32, i32, i32, P, P, P, P]
+            lib.oracle_router_logits.restype = i32
+            lib.oracle_route.argtypes = [i32, i32, i32, P, P, P, P]
+            lib.oracle_route.restype = i32
+            lib.oracle_expert_ffn.argtypes = [i32, i32] + [P, P, ctypes.c_float] * 3 + [P, P]
+            lib.oracle_expert_ffn.restype = i32
+            lib.oracle_moe_forward.argtypes = [i32] * 5 + [P, P, P] * 3 + [P, P, P, P]
+            lib.oracle_moe_forward.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def e2m1_value(nibble: int) -> float:
+    return _load().oracle_e2m1_value(nibble)
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().oracle_e4m3_value(byte)
+
+
+def bf16_value(bits: int) -> float:
+    return _load().oracle_bf16_value(bits)
+
+
+def expert_bytes(hidden: int, inter: int) -> int:
+    return int(_load().oracle_expert_bytes(hidden, inter))
+
+
+def dequant(codes, scales, g, rows, K):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    out = np.empty((rows, K), np.float64)
+    rc = _load().oracle_dequant(_ptr(codes), _ptr(scales), float(g), rows, K, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_dequant failed ({rc})")
+    return out
+
+
+def router_logits(Wr, x_bf16, bias=None):
+    """Wr float32 [E][H], x_bf16 uint16 [C][H] -> float64 logits [C][E]."""
+    Wr = _c(Wr, np.float32)
+    x = _c(x_bf16, np.uint16)
+    E, H = Wr.shape
+    C = x.shape[0]
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((C, E), np.float64)
+    rc = _load().oracle_router_logits(C, E, H, _ptr(Wr), _ptr(x), _ptr(b), _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_router_logits failed ({rc})")
+    return out
+
+
+def route(logits, k):
+    """float64 logits [C][E] -> (ids int32 [C][k] ascending, weights float64 [C][k], gap [C])."""
+    logits = _c(logits, np.float64)
+    C, E = logits.shape
+    ids = np.empty((C, k), np.int32)
+    w = np.empty((C, k), np.float64)
+    gap = np.empty((C,), np.float64)
+    rc = _load().oracle_route(C, E, k, _ptr(logits), _ptr(ids), _ptr(w), _ptr(gap))
+    if rc != OK:
+        raise ValueError(f"oracle_route failed ({rc})")
+    return ids, w, gap
+
+
+def expert_ffn(H, I, gate, up, down, x):
+    """gate/up/down = (codes, scales, g) of one expert; x float64 [H] -> y float64 [H]."""
+    x = _c(x, np.float64)
+    y = np.empty((H,), np.float64)
+    mats = []
+    args = []
+    for m in (gate, up, down):
+        c, s = _c(m[0], np.uint8), _c(m[1], np.uint8)
+        mats.append((c, s))
+        args += [_ptr(c), _ptr(s), float(m[2])]
+    rc = _load().oracle_expert_ffn(H, I, *args, _ptr(x), _ptr(y))
+    if rc != OK:
+        raise ValueError(f"oracle_expert_ffn failed ({rc})")
+    return y
+
+
+def moe_forward(weights, x_bf16, ids, w):
+    """Routed MoE output.
+
+    weights: dict with 'gate', 'up', 'down', each a dict of 'codes' [E][rows][K/2],
+    'scales' [E][rows][K/16], 'g' [E] (canonical NVFP4).  x_bf16 uint16 [C][H],
+    ids int32 [C][k], w float64 [C][k] -> y float64 [C][H].
+    """
+    gate, up, down = weights["gate"], weights["up"], weights["down"]
+    E, I, Hh = gate["codes"].shape
+    H = Hh * 2
+    x = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    C, k = ids.shape
+    keep = []
+    args = []
+    for m in (gate, up, down):
+        c, s, g = _c(m["codes"], np.uint8), _c(m["scales"], np.uint8), _c(m["g"], np.float32)
+        keep.append((c, s, g))
+        args += [_ptr(c), _ptr(s), _ptr(g)]
+    y = np.empty((C, H), np.float64)
+    rc = _load().oracle_moe_forward(C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
+    if rc != OK:
+        raise ValueError(f"oracle_moe_forward failed ({rc})")
+    return y
+
+
+def full_layer(weights, Wr, x_bf16, k, bias=None):
+    """Router + top-k + routed FFN for C tokens: returns (ids, w, gap, y)."""
+    logits = router_logits(Wr, x_bf16, bias)
+    ids, w, gap = route(logits, k)
+    y = moe_forward(weights, x_bf16, ids, w)
+    return ids, w, gap, y

@@ -1,0 +1,317 @@
+/*
+ * moe_oracle.c -- plain, slow, float64 CPU oracle for the routed NVFP4 MoE FFN.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check of the
+ * package entry module and the CPU-baseline leg of the benchmark may load this
+ * file.  The product library never links it, calls it or falls back to it, and
+ * this file shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes (one MoE layer of a Kimi-K3-class model at decode, the
+ * "MUL_MAT_ID" step):
+ *   1. router logits  l[t][e] = sum_j Wr[e][j] * x[t][j]  (+ bias[e])
+ *   2. softmax over all E experts, the k largest logits kept (equal logits:
+ *      lower expert index first), the kept probabilities renormalised to sum 1
+ *   3. for every kept expert: g = G x, u = U x, a = silu(g) * u, y_e = D a,
+ *      with G, U, D decoded exactly from NVFP4
+ *   4. y[t] = sum_i w[t][i] * y_{e_i}
+ * Sources: "SparkInfer-K3" README, sections "How the TP module works" (every
+ * rank runs the same router and agrees on the same top-16; the partial expert
+ * sums add up to the full 3584-wide output) and "The model" (896 routed
+ * experts, top-16, experts in a 3584-wide latent space, expert FFN 3072);
+ * "Kimi-K3 on 2x A40 - measured findings", section "Why the placement
+ * experiments all looked the same" (MUL_MAT_ID over the selected experts'
+ * 3584->3072 matrices); "Kimi-K3 on the same pod, two engines", section "Same
+ * hardware, same weights" (NVFP4 checkpoint, 18,579,480 bytes per routed
+ * expert).
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes):
+ *   - router scoring is a softmax, renormalised over the top-k, with no extra
+ *     routed scaling factor;
+ *   - the expert activation is SwiGLU, silu(g) * u (the K3 page names a
+ *     different activation, "situ", without a formula);
+ *   - NVFP4 bytes per matrix [rows][K]: one e2m1 code per element, two per
+ *     byte, the LOW nibble holding the even element; one e4m3 scale byte per
+ *     16 consecutive elements along K; one fp32 tensor (global) scale that
+ *     multiplies every element; one fp32 input scale that this path carries
+ *     but does not use.  That reading is the only one that reproduces the
+ *     page's 18,579,480 bytes for three 3072x3584 matrices exactly:
+ *     3 * (3072*3584/2 + 3072*3584/16 + 2*4).
+ *
+ * Precision: every product and sum is float64.  A decoded weight
+ * e2m1 * e4m3 * fp32 has at most 2 + 4 + 24 significant bits, so it is exact
+ * in float64.  Build with -ffp-contract=off so the result does not depend on
+ * whether the host compiler fuses multiply-adds.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG 1
+#define ORACLE_ERR_NAN_SCALE 2
+#define ORACLE_ERR_BAD_ID 3
+
+/* ---------------------------------------------------------------- decode */
+
+/* e2m1 (FP4): bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.
+ * Exponent field 0 is subnormal: value = mantissa * 0.5.
+ * Otherwise value = 2^(exp-1) * (1 + mantissa/2). */
+double oracle_e2m1_value(uint8_t nibble) {
+  int sign = (nibble >> 3) & 1;
+  int exp_field = (nibble >> 1) & 3;
+  int mant = nibble & 1;
+  double mag;
+  if (exp_field == 0)
+    mag = 0.5 * (double)mant;
+  else
+    mag = ldexp(1.0 + 0.5 * (double)mant, exp_field - 1);
+  return sign ? -mag : mag;
+}
+
+/* e4m3 ("fn" variant): bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ * mantissa.  Exponent field 0 is subnormal: value = mantissa/8 * 2^-6.
+ * Exponent 15 with mantissa 7 (bytes 0x7F, 0xFF) is NaN; there are no
+ * infinities, so the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int exp_field = (byte >> 3) & 15;
+  int mant = byte & 7;
+  double mag;
+  if (exp_field == 15 && mant == 7) return NAN;
+  if (exp_field == 0)
+    mag = ldexp((double)mant / 8.0, -6);
+  else
+    mag = ldexp(1.0 + (double)mant / 8.0, exp_field - 7);
+  return sign ? -mag : mag;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Bytes of one canonical NVFP4 expert (gate [I][H], up [I][H], down [H][I]):
+ * codes + scale bytes + two fp32 per matrix.  The K3 shape (H 3584, I 3072)
+ * must give the 18,579,480 bytes per routed expert printed in "Kimi-K3 on the
+ * same pod, two engines", section "Same hardware, same weights". */
+uint64_t oracle_expert_bytes(int64_t hidden, int64_t inter) {
+  uint64_t per_matrix_elems = (uint64_t)hidden * (uint64_t)inter;
+  uint64_t one = per_matrix_elems / 2 + per_matrix_elems / 16 + 2 * 4;
+  return 3 * one;
+}
+
+/* Weight (r, k) of one NVFP4 matrix [rows][K]:
+ *   code  = nibble k%2 (low nibble for even k) of codes[r*K/2 + k/2]
+ *   scale = scales[r*K/16 + k/16]
+ *   w     = e2m1(code) * e4m3(scale) * g                                      */
+static double nvfp4_weight(const uint8_t *codes, const uint8_t *scales, float g,
+                           int64_t K, int64_t r, int64_t k) {
+  uint8_t byte = codes[r * (K / 2) + k / 2];
+  uint8_t nibble = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+  uint8_t sbyte = scales[r * (K / 16) + k / 16];
+  return oracle_e2m1_value(nibble) * oracle_e4m3_value(sbyte) * (double)g;
+}
+
+/* Dense float64 copy of one NVFP4 matrix: out[rows][K].  Returns
+ * ORACLE_ERR_NAN_SCALE if any scale byte is NaN. */
+int oracle_dequant(const uint8_t *codes, const uint8_t *scales, float g,
+                   int64_t rows, int64_t K, double *out) {
+  if (!codes || !scales || !out || rows < 0 || K <= 0 || K % 16 != 0)
+    return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < rows * (K / 16); i++)
+    if (isnan(oracle_e4m3_value(scales[i]))) return ORACLE_ERR_NAN_SCALE;
+  for (int64_t r = 0; r < rows; r++)
+    for (int64_t k = 0; k < K; k++)
+      out[r * K + k] = nvfp4_weight(codes, scales, g, K, r, k);
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- router */
+
+/* Router logits l[t][e] = sum_j Wr[e][j] * x[t][j] (+ bias[e]); Wr is fp32
+ * [E][H], x is bf16 [C][H], bias is fp32 [E] or NULL.  The router is
+ * replicated and identical on every rank ("SparkInfer-K3", "How the TP module
+ * works"). */
+int oracle_router_logits(int C, int E, int H, const float *Wr,
+                         const uint16_t *x, const float *bias,
+                         double *logits) {
+  if (C < 0 || E <= 0 || H <= 0 || !Wr || !x || !logits) return ORACLE_ERR_ARG;
+  for (int t = 0; t < C; t++)
+    for (int e = 0; e < E; e++) {
+      double s = 0.0;
+      for (int j = 0; j < H; j++)
+        s += (double)Wr[(int64_t)e * H + j] *
+             oracle_bf16_value(x[(int64_t)t * H + j]);
+      if (bias) s += (double)bias[e];
+      logits[(int64_t)t * E + e] = s;
+    }
+  return ORACLE_OK;
+}
+
+/* Top-k routing of one token's logits l[0..E-1]:
+ *   p = softmax(l) over all E experts (computed as exp(l - max l) / sum);
+ *   the k experts with the largest logits are kept, equal logits ranked by
+ *   lower expert index first;
+ *   w_i = p_i / sum over the kept experts of p_j.
+ * Output: ids in ascending expert order with their weights, and the boundary
+ * gap l_(k) - l_(k+1) between the k-th and (k+1)-th ranked logits (+inf when
+ * k == E).  The kept set is plain selection: k passes, each taking the best
+ * remaining expert by (logit descending, index ascending). */
+int oracle_route(int C, int E, int k, const double *logits, int32_t *ids,
+                 double *weights, double *gap) {
+  if (C < 0 || E <= 0 || k <= 0 || k > E || !logits || !ids || !weights)
+    return ORACLE_ERR_ARG;
+  unsigned char *taken = (unsigned char *)malloc((size_t)E);
+  double *p = (double *)malloc(sizeof(double) * (size_t)E);
+  if (!taken || !p) {
+    free(taken);
+    free(p);
+    return ORACLE_ERR_ARG;
+  }
+  for (int t = 0; t < C; t++) {
+    const double *l = logits + (int64_t)t * E;
+    double lmax = l[0];
+    for (int e = 1; e < E; e++)
+      if (l[e] > lmax) lmax = l[e];
+    double z = 0.0;
+    for (int e = 0; e < E; e++) {
+      p[e] = exp(l[e] - lmax);
+      z += p[e];
+    }
+    for (int e = 0; e < E; e++) p[e] /= z;
+
+    memset(taken, 0, (size_t)E);
+    double kth = 0.0;
+    for (int r = 0; r < k; r++) {
+      int best = -1;
+      for (int e = 0; e < E; e++) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e; /* strict '>' keeps the lower index on ties */
+      }
+      taken[best] = 1;
+      kth = l[best];
+    }
+    if (gap) {
+      if (k == E) {
+        gap[t] = INFINITY;
+      } else {
+        int next = -1;
+        for (int e = 0; e < E; e++) {
+          if (taken[e]) continue;
+          if (next < 0 || l[e] > l[next]) next = e;
+        }
+        gap[t] = kth - l[next];
+      }
+    }
+    double psel = 0.0;
+    for (int e = 0; e < E; e++)
+      if (taken[e]) psel += p[e];
+    int n = 0;
+    for (int e = 0; e < E; e++) /* ascending expert id */
+      if (taken[e]) {
+        ids[(int64_t)t * k + n] = e;
+        weights[(int64_t)t * k + n] = p[e] / psel;
+        n++;
+      }
+  }
+  free(taken);
+  free(p);
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------ expert FFN */
+
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* One expert's SwiGLU FFN on a float64 input vector x[H]:
+ *   g = G x, u = U x         (G, U: NVFP4 [I][H])
+ *   a = silu(g) * u
+ *   y = D a                  (D: NVFP4 [H][I])
+ * Shapes from "SparkInfer-K3", "The model": the expert reads and writes the
+ * 3584-wide latent space and is 3072 wide inside. */
+int oracle_expert_ffn(int H, int I,
+                      const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
+                      const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
+                      const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
+                      const double *x, double *y) {
+  if (H <= 0 || I <= 0 || H % 16 || I % 16 || !x || !y) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < (int64_t)I * (H / 16); i++)
+    if (isnan(oracle_e4m3_value(gate_scales[i])) || isnan(oracle_e4m3_value(up_scales[i])))
+      return ORACLE_ERR_NAN_SCALE;
+  for (int64_t i = 0; i < (int64_t)H * (I / 16); i++)
+    if (isnan(oracle_e4m3_value(down_scales[i]))) return ORACLE_ERR_NAN_SCALE;
+  double *a = (double *)malloc(sizeof(double) * (size_t)I);
+  if (!a) return ORACLE_ERR_ARG;
+  for (int r = 0; r < I; r++) {
+    double g = 0.0, u = 0.0;
+    for (int k = 0; k < H; k++) {
+      g += nvfp4_weight(gate_codes, gate_scales, gate_g, H, r, k) * x[k];
+      u += nvfp4_weight(up_codes, up_scales, up_g, H, r, k) * x[k];
+    }
+    a[r] = silu(g) * u;
+  }
+  for (int r = 0; r < H; r++) {
+    double s = 0.0;
+    for (int k = 0; k < I; k++)
+      s += nvfp4_weight(down_codes, down_scales, down_g, I, r, k) * a[k];
+    y[r] = s;
+  }
+  free(a);
+  return ORACLE_OK;
+}
+
+/* The routed MoE output of C tokens given their selections:
+ *   y[t] = sum_i w[t][i] * FFN_{ids[t][i]}(x[t])
+ * Canonical weights are arrays over E experts:
+ *   *_codes  [E][rows][K/2], *_scales [E][rows][K/16], *_g [E]
+ * (gate/up: rows I, K H; down: rows H, K I).  The sum over i runs in the
+ * order the ids are given.  An id outside [0, E) is an error.  The partial
+ * sums over disjoint subsets of the selected experts add up to this result
+ * ("SparkInfer-K3", "How the TP module works"). */
+int oracle_moe_forward(int C, int E, int k, int H, int I,
+                       const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                       const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                       const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                       const uint16_t *x, const int32_t *ids, const double *w,
+                       double *y) {
+  if (C < 0 || E <= 0 || k <= 0 || H <= 0 || I <= 0 || H % 16 || I % 16 || !x ||
+      !ids || !w || !y)
+    return ORACLE_ERR_ARG;
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+  double *ye = (double *)malloc(sizeof(double) * (size_t)H);
+  if (!xt || !ye) {
+    free(xt);
+    free(ye);
+    return ORACLE_ERR_ARG;
+  }
+  int rc = ORACLE_OK;
+  for (int t = 0; t < C && rc == ORACLE_OK; t++) {
+    for (int j = 0; j < H; j++) xt[j] = oracle_bf16_value(x[(int64_t)t * H + j]);
+    for (int j = 0; j < H; j++) y[(int64_t)t * H + j] = 0.0;
+    for (int i = 0; i < k; i++) {
+      int e = ids[(int64_t)t * k + i];
+      if (e < 0 || e >= E) {
+        rc = ORACLE_ERR_BAD_ID;
+        break;
+      }
+      rc = oracle_expert_ffn(H, I,
+                             gate_codes + e * gu_codes, gate_scales + e * gu_scales, gate_g[e],
+                             up_codes + e * gu_codes, up_scales + e * gu_scales, up_g[e],
+                             down_codes + e * dn_codes, down_scales + e * dn_scales, down_g[e],
+                             xt, ye);
+      if (rc != ORACLE_OK) break;
+      double wi = w[(int64_t)t * k + i];
+      for (int j = 0; j < H; j++) y[(int64_t)t * H + j] += wi * ye[j];
+    }
+  }
+  free(xt);
+  free(ye);
+  return rc;
+}
