@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed NVFP4 MoE layer at decode (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: router GEMV + top-k
+(moe_route) and the routed expert FFN with its combine (moe_forward), on
+inputs already resident in HBM.  Default workload: the K3-shape layer (896
+experts, top-16, hidden 3584, FFN 3072, NVFP4, ~16.6 GB resident) at decode
+batch 1.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Timed region: K steps replayed from CUDA graphs (16 rotating token sets, so
+the routed experts change every step; the 297 MB of expert bytes a step reads
+exceed the 129 MB L2), bracketed by barrier + synchronize, timed with CUDA
+events, max over ranks.  Under torchrun each rank runs its own replica of the
+layer on its own tokens (weak scaling, no collective on the data path).
+
+The JSON line also carries: the gate/up kernel's roofline (algorithmic bytes /
+CUDA-event duration, from a second loop with per-stage events), an end-to-end
+number through the C ABI with host buffers (H2D of x and D2H of y inside the
+timed region), SM clocks sampled during the timed region, and the float64
+oracle timed on the host cores on a bounded sample (cpu_baseline).
+``--impl reference`` times only that oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tok/s (896 experts, top-16, NVFP4); expert-weight HBM GB/s"
+EXPERT_BYTES_K3 = 18_579_480
+
+CONFIGS = {
+    # name: experts, top_k, hidden, inter, tokens per step, layers, zipf router
+    "k3b1": dict(E=896, k=16, H=3584, I=3072, C=1, layers=1, zipf=False,
+                 workload="K3-shape MoE layer, decode batch 1, top-16 of 896, NVFP4, uniform routing"),
+    "k3c7k16": dict(E=896, k=16, H=3584, I=3072, C=7, layers=1, zipf=False,
+                    workload="K3-shape MoE layer, decode batch 7, top-16 of 896, NVFP4, uniform routing"),
+    "k3c7k8": dict(E=896, k=8, H=3584, I=3072, C=7, layers=1, zipf=False,
+                   workload="K3-shape MoE layer, decode batch 7, top-8 of 896, NVFP4, uniform routing"),
+    "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
+                 workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
+}
+ROTATE = 16          # distinct token sets cycled through the timed steps
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--config", default="k3b1", choices=sorted(CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=20.0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- utilities
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id is not None:
+                cmd += ["-i", str(self.gpu_id)]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [q.strip() for q in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel_file, tag):
+    """DRAM bytes per unit from a committed ncu summary, if the kernel source
+    is unchanged since the capture (sha256 recorded in the summary)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"{tag}.md")
+    if not os.path.exists(prof):
+        return None
+    txt = open(prof).read()
+    m = re.search(r"dram_bytes_per_expert:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    src = open(os.path.join(ROOT, "quantized_moe_expert_router_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != h.group(1):
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- oracle legs
+
+def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits):
+    """Time the float64 oracle (single thread) on whole tokens of the workload
+    until ``budget_s`` is used (at least one token).  Returns tokens/s."""
+    import oracle
+    done, t_total = 0, 0.0
+    for t in range(x_bits.shape[0]):
+        xb = x_bits[t:t + 1]
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(Wr, xb, bias)
+        ids, w, _ = oracle.route(logits, cfg["k"])
+        sel = sorted(set(int(e) for e in ids.ravel()))
+        t_prep0 = time.perf_counter()
+        weights = weights_for(sel)                       # input staging, not timed
+        t_prep = time.perf_counter() - t_prep0
+        remap = {e: i for i, e in enumerate(sel)}
+        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w)
+        t_total += time.perf_counter() - t0 - t_prep
+        done += 1
+        if t_total >= budget_s:
+            break
+    return done, t_total
+
+
+def run_reference(args, cfg, rank):
+    """Reference arm: the float64 oracle on the host cores, on this config."""
+    from quantized_moe_expert_router_gb300 import synth
+    import oracle
+    oracle.build()
+    if rank != 0:
+        return
+    E, k, H, I, C = cfg["E"], cfg["k"], cfg["H"], cfg["I"], cfg["C"]
+    Wr = synth.router_weights(args.seed, 0, E, H, synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0)
+    bias = synth.zipf_bias(args.seed, 0, E) if cfg["zipf"] else None
+    cache = {}
+
+    def weights_for(sel):
+        need = [e for e in sel if e not in cache]
+        if need:
+            part = synth.canonical_layer(args.seed, 0, E, H, I, experts=need)
+            for j, e in enumerate(need):
+                cache[e] = {n: {f: m[f][j] for f in ("codes", "scales", "g", "a")} for n, m in part.items()}
+        return {n: {f: np.stack([cache[e][n][f] for e in sel]) for f in ("codes", "scales", "g", "a")}
+                for n in ("gate", "up", "down")}
+
+    # one step = one token of the workload; the step count is capped so the
+    # whole run stays within a few minutes
+    x_all = synth.tokens(args.seed, 0, max(1, args.steps + args.warmup), H) if args.steps + args.warmup <= 64 \
+        else synth.tokens(args.seed, 0, 64, H)
+    per_token = None
+    warm = min(args.warmup, 1)
+    for t in range(warm):
+        oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, x_all[t:t + 1])
+    steps_done, elapsed = 0, 0.0
+    budget = 150.0
+    for s in range(args.steps):
+        xb = x_all[(warm + s) % x_all.shape[0]: (warm + s) % x_all.shape[0] + 1]
+        n, dt = oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, xb)
+        steps_done += 1
+        elapsed += dt
+        if elapsed >= budget:
+            break
+    tok_s = steps_done / elapsed
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": steps_done, "warmup": warm, "ms_per_step": 1e3 * elapsed / steps_done,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg["workload"], "tokens_per_step": 1},
+        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{steps_done} whole token(s) of the workload (router, top-k, "
+                                   f"{k} experts), single-threaded float64 C"},
+        "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": ("step count capped by a 150 s budget" if steps_done < args.steps else ""),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    args = parse()
+    cfg = CONFIGS[args.config]
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    from quantized_moe_expert_router_gb300 import build as pkg_build
+    if rank == 0:
+        pkg_build.build()
+    if world > 1:
+        dist.barrier()
+    from quantized_moe_expert_router_gb300 import moe, synth
+    from quantized_moe_expert_router_gb300.synth import device as synth_dev
+
+    E, k, H, I, C = cfg["E"], cfg["k"], cfg["H"], cfg["I"], cfg["C"]
+    free, total = torch.cuda.mem_get_info(dev)
+    need = cfg["layers"] * E * EXPERT_BYTES_K3 * (H * I) / (3584 * 3072) * 2.2
+    if need > free:
+        print(json.dumps({"metric": METRIC, "error": f"needs {need / 1e9:.1f} GB free HBM, {free / 1e9:.1f} GB free"}))
+        sys.exit(1)
+
+    layer = moe.Layer(E, k, H, I, C, device=local)
+    canon = synth_dev.canonical_layer_device(args.seed, 0, E, H, I, dev)
+    packed = moe.alloc_packed(layer, dev)
+    moe.moe_pack_weights(layer, canon, packed)
+    router_std = synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0
+    Wr = synth.router_weights(args.seed, 0, E, H, router_std)
+    bias = synth.zipf_bias(args.seed, 0, E) if cfg["zipf"] else None
+    Wr_d = torch.from_numpy(Wr).to(dev)
+    bias_d = None if bias is None else torch.from_numpy(bias).to(dev)
+
+    # rotating token sets, distinct per rank
+    x_host = [synth.tokens(args.seed + 1000 * rank, r, C, H) for r in range(ROTATE)]
+    xs = [torch.from_numpy(xh.view(np.int16)).to(dev) for xh in x_host]
+    ids = [torch.empty((C, k), dtype=torch.int32, device=dev) for _ in range(ROTATE)]
+    wts = [torch.empty((C, k), dtype=torch.float32, device=dev) for _ in range(ROTATE)]
+    ys = [torch.empty((C, H), dtype=torch.float32, device=dev) for _ in range(ROTATE)]
+    ws = moe.alloc_workspace(layer, C, dev)
+
+    # the oracle's sample needs the canonical bytes of the experts it selects
+    cpu_sample = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sample_x = np.concatenate(x_host[:4], axis=0)[:8]
+        host_cache = {}
+
+        def weights_for(sel):
+            need_e = [e for e in sel if e not in host_cache]
+            if need_e:
+                part = synth_dev.gather_to_host(canon, need_e)
+                for j, e in enumerate(need_e):
+                    host_cache[e] = {n: {f: m[f][j] for f in ("codes", "scales", "g", "a")} for n, m in part.items()}
+            return {n: {f: np.stack([host_cache[e][n][f] for e in sel]) for f in ("codes", "scales", "g", "a")}
+                    for n in ("gate", "up", "down")}
+        cpu_sample = (sample_x, weights_for)
+        done, secs = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s, Wr, bias, sample_x)
+        cpu_baseline = {"value": done / secs, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{done} whole token(s) of this workload (router + top-{k} + {k} expert FFNs "
+                                  f"+ combine), single-threaded float64 C oracle, {secs:.1f} s"}
+    del canon
+    torch.cuda.empty_cache()
+
+    stream = torch.cuda.Stream(dev)
+
+    def step(r, s):
+        moe.moe_route(layer, xs[r], C, Wr_d, bias_d, ids[r], wts[r], ws, s)
+        moe.moe_forward(layer, xs[r], C, ids[r], wts[r], packed, ys[r], ws, s)
+
+    # distinct experts each rotating input selects (bytes a step streams)
+    with torch.cuda.stream(stream):
+        for r in range(ROTATE):
+            step(r, stream)
+    stream.synchronize()
+    distinct = [len(set(ids[r].cpu().numpy().ravel().tolist())) for r in range(ROTATE)]
+    flags = moe.moe_get_device_status(layer, ws, stream)
+    if flags:
+        raise RuntimeError(f"device flags {flags:#x} after the first pass")
+
+    def capture(nsteps, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                step((offset + i) % ROTATE, stream)
+        return g
+
+    g_full = capture(ROTATE, 0)
+    rem = args.steps % ROTATE
+    g_rem = capture(rem, 0) if rem else None
+    wrem = args.warmup % ROTATE
+    g_wrem = capture(wrem, 0) if wrem else None
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup // ROTATE):
+            g_full.replay()
+        if g_wrem is not None:
+            g_wrem.replay()
+    stream.synchronize()
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.perf_counter()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps // ROTATE):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    ev1.record(stream)
+    stream.synchronize()
+    t_host = time.perf_counter() - t_host0
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    tokens = C * args.steps * world
+    tok_s = tokens / (ms / 1e3)
+    avg_distinct = sum(distinct[(i % ROTATE)] for i in range(args.steps)) / args.steps
+    expert_bytes = E and (EXPERT_BYTES_K3 if (H, I) == (3584, 3072) else 3 * (I * H // 2 + I * H // 16 + 8))
+    hbm_gbs = avg_distinct * expert_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (gate/up), per-stage CUDA events
+    n_prof = 256 if C == 1 else 128
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
+    for trio in evs:
+        for e_ in trio:
+            e_.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            r = i % ROTATE
+            moe.moe_route(layer, xs[r], C, Wr_d, bias_d, ids[r], wts[r], ws, stream)
+            moe.moe_set_stage_events(layer, evs[i])
+            moe.moe_forward(layer, xs[r], C, ids[r], wts[r], packed, ys[r], ws, stream)
+    moe.moe_set_stage_events(layer, None)
+    stream.synchronize()
+    gu_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof)]
+    dn_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_prof)]
+    gu_bytes_per_expert = 2 * (I * H // 2 + I * H // 16)
+    gu_units = sum(distinct[i % ROTATE] for i in range(n_prof)) / n_prof
+    gu_avg = float(np.mean(gu_ms))
+    dn_avg = float(np.mean(dn_ms))
+    hbm_peak, peak_src = measured_peaks()
+    achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
+    traffic_per_expert = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
+    roofline = {"kernel": "expert_gemv_kernel<0,NT> (gate/up + SwiGLU)", "bound": "hbm",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_source": peak_src,
+                "traffic": None if traffic_per_expert is None else traffic_per_expert * gu_units,
+                "algorithmic_bytes_per_launch": gu_units * gu_bytes_per_expert,
+                "avg_launch_us": gu_avg * 1e3,
+                "down_kernel": {"avg_launch_us": dn_avg * 1e3,
+                                "achieved_gbs": gu_units * (gu_bytes_per_expert / 2) / (dn_avg * 1e-3) / 1e9}}
+
+    # ---- end to end through the C ABI with host buffers
+    n_e2e = min(args.steps, 2000)
+    x_pin = [torch.from_numpy(xh.view(np.int16)).pin_memory() for xh in x_host]
+    y_pin = torch.empty((C, H), dtype=torch.float32).pin_memory()
+    x_stage = torch.empty((C, H), dtype=torch.int16, device=dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            r = i % ROTATE
+            x_stage.copy_(x_pin[r], non_blocking=True)
+            moe.moe_route(layer, x_stage, C, Wr_d, bias_d, ids[r], wts[r], ws, stream)
+            moe.moe_forward(layer, x_stage, C, ids[r], wts[r], packed, ys[r], ws, stream)
+            y_pin.copy_(ys[r], non_blocking=True)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e = {"value": C * n_e2e * world / e2e_s, "unit": "tok/s", "steps": n_e2e,
+           "h2d_bytes_per_step": C * H * 2, "d2h_bytes_per_step": C * H * 4,
+           "path": "pinned host x -> H2D -> moe_route -> moe_forward -> D2H y, per step, host-timed"}
+
+    flags = moe.moe_get_device_status(layer, ws, stream)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": cfg["workload"], "experts": E, "top_k": k, "hidden": H,
+                       "intermediate": I, "tokens_per_step": C, "layers": cfg["layers"],
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"{ROTATE} rotating token sets; each step streams ~{avg_distinct * expert_bytes / 1e6:.0f} MB "
+                             "of expert weights (> 129 MB L2)" if H == 3584 else "L2-resident (tiny)",
+                       "timing": "CUDA graphs of route+forward, CUDA events on the launching stream"},
+            "us_per_layer": 1e3 * ms_per_step,
+            "expert_hbm_gbs": hbm_gbs, "expert_hbm_frac": hbm_gbs / world / hbm_peak,
+            "distinct_experts_per_step": avg_distinct,
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps * (C + 7) // 8 if C > 8 else 3 * args.steps,
+            "clocks": clocks,
+            "host_s": t_host,
+            "device_flags": flags,
+        }
+        if cpu_sample is not None:
+            line["cpu_baseline"] = cpu_baseline
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed NVFP4 MoE FFN library.
+ *
+ * One MoE layer of a Kimi-K3-class model at decode ("MUL_MAT_ID"): router
+ * scores, top-k of the routed experts with softmax weights renormalised over
+ * the top-k, an NVFP4 SwiGLU FFN per selected expert, and the weighted sum of
+ * the expert outputs.  Shapes and byte counts follow "SparkInfer-K3"
+ * (sections "The model" and "How the TP module works") and "Kimi-K3 on the
+ * same pod, two engines" (section "Same hardware, same weights": 896 routed
+ * experts, top-16, 18,579,480 bytes per NVFP4 expert).
+ *
+ * Conventions for every entry point
+ *   - All pointers named "device" are CUDA device pointers on the layer's
+ *     device, owned by the caller, 16-byte aligned, and must stay valid until
+ *     the work queued on `stream` has finished.  The library allocates no
+ *     device memory and keeps no pointer after a call returns.
+ *   - Argument and shape errors are returned synchronously before anything is
+ *     queued.  A failed launch returns MOE_ERR_CUDA.  Errors found in the data
+ *     on the device (an expert id out of range or repeated within a token) set
+ *     bits in a flag word inside the workspace: read them with
+ *     moe_get_device_status.  No kernel traps or asserts.
+ *   - moe_route and moe_forward allocate nothing and never synchronise the
+ *     host, so a sequence of them can be captured into a CUDA graph.
+ *   - The handle is immutable after creation; concurrent calls on different
+ *     streams need different workspaces and output buffers.
+ *
+ * Canonical NVFP4 matrix [rows][K] (the checkpoint's byte layout as read
+ * here; it reproduces the 18,579,480 bytes per expert exactly):
+ *   codes   uint8 [rows][K/2]  e2m1 codes, low nibble = element 2j, high = 2j+1
+ *   scales  uint8 [rows][K/16] e4m3 scale of elements 16b .. 16b+15 of the row
+ *   global_scale float         multiplies every element of the matrix
+ *   input_scale  float         carried, not used (activations stay bf16/fp32)
+ *   weight(r, k) = e2m1(code) * e4m3(scale) * global_scale
+ * Expert e's FFN:  g = G x, u = U x (G, U: [I][H]);  a = silu(g) * u;
+ *                  y_e = D a (D: [H][I]).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad count */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported range */
+  MOE_ERR_INVALID_VALUE = 3,      /* a NaN e4m3 scale byte in the weights */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  MOE_ERR_OUT_OF_MEMORY = 5,
+  MOE_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 7,     /* reserved: a bounded device wait ran out */
+  MOE_ERR_BAD_EXPERT_ID = 8       /* device flag: an id out of [0,E) or repeated */
+} moe_status;
+
+/* Device flag bits reported by moe_get_device_status. */
+#define MOE_FLAG_BAD_EXPERT_ID 0x1   /* an id outside [0, num_experts): slot skipped */
+#define MOE_FLAG_DUPLICATE_ID 0x2    /* an expert repeated within one token: one copy dropped */
+#define MOE_FLAG_TIMEOUT 0x4         /* reserved for bounded waits */
+
+typedef struct {
+  int32_t num_experts;   /* E, 1 .. 1024 */
+  int32_t top_k;         /* k, 1 .. min(32, E) */
+  int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 16384 */
+  int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 16384 */
+  int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
+  uint32_t flags;        /* must be 0 */
+} moe_config;
+
+typedef struct {
+  const uint8_t *codes;        /* device, [E][rows][K/2] */
+  const uint8_t *scales;       /* device, [E][rows][K/16] */
+  const float *global_scale;   /* device, [E] */
+  const float *input_scale;    /* device, [E] (copied into the packed buffer, unused) */
+} moe_fp4_tensor;
+
+typedef struct {
+  moe_fp4_tensor gate;  /* rows I, K H */
+  moe_fp4_tensor up;    /* rows I, K H */
+  moe_fp4_tensor down;  /* rows H, K I */
+} moe_canonical_weights;
+
+typedef struct moe_layer *moe_layer_t;
+
+/* Validate `cfg` and create a host-side handle for `device` (queries its SM
+ * count; allocates no device memory).  *out is set only on MOE_OK. */
+moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out);
+
+/* Free the handle (host memory only).  NULL is accepted. */
+moe_status moe_layer_destroy(moe_layer_t layer);
+
+/* Bytes of the packed weight buffer moe_pack_weights writes.  For H and I
+ * multiples of 512 it equals E * (bytes of one canonical expert) + 16: the
+ * packer reorders bytes and adds nothing but a 16-byte status trailer.
+ * Smaller shapes are padded along K to a multiple of 512 with zero codes. */
+moe_status moe_packed_bytes(moe_layer_t layer, size_t *bytes);
+
+/* Bytes of workspace route/forward need for up to `num_tokens` tokens.  The
+ * workspace is caller-owned device memory that must be ZERO-FILLED once
+ * before its first use; route and forward leave it in a reusable state. */
+moe_status moe_workspace_bytes(moe_layer_t layer, int num_tokens, size_t *bytes);
+
+/* Reorder canonical NVFP4 weights (all E experts) into the packed layout the
+ * kernels stream: per expert, I "gate/up pair rows" (gate row r and up row r
+ * interleaved per 16-element block) then H/2 "down pair rows" (down rows 2p
+ * and 2p+1 interleaved), each pair row holding its codes and then its scale
+ * bytes; the 6 fp32 scalars of all experts follow.  Offline, once per layer:
+ * this call synchronises `stream` and returns MOE_ERR_INVALID_VALUE if any
+ * scale byte is an e4m3 NaN (0x7F or 0xFF).  `packed` (device,
+ * moe_packed_bytes long) must not overlap the canonical buffers. */
+moe_status moe_pack_weights(moe_layer_t layer, const moe_canonical_weights *canon,
+                            void *packed, cudaStream_t stream);
+
+/* Router and top-k for C tokens ("SparkInfer-K3", "How the TP module works":
+ * one replicated router, all ranks agree on the same top-k):
+ *   logits l[t][e] = sum_j w_router[e][j] * x[t][j] (+ bias[e]), fp32
+ *   ids[t][0..k)     the k largest logits, equal logits -> lower index first,
+ *                    written in ascending expert id order
+ *   weights[t][i]    softmax over all experts renormalised over the k kept
+ *                    = exp(l_i - l_max) / sum over kept of exp(l_j - l_max)
+ * x: device bf16 bits [C][H]; w_router: device fp32 [E][H]; bias: device fp32
+ * [E] or NULL; ids: device int32 [C][k]; weights: device fp32 [C][k];
+ * ws: workspace of at least moe_workspace_bytes(C).  1 <= C <= max_tokens. */
+moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
+                     const float *w_router, const float *bias, int32_t *ids,
+                     float *weights, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Routed expert FFN and combine for C tokens:
+ *   y[t] = sum_i weights[t][i] * D_e (silu(G_e x[t]) * (U_e x[t])),  e = ids[t][i]
+ * x: device bf16 bits [C][H]; ids: device int32 [C][k] (any order; each
+ * token's ids must be distinct and in [0,E) -- offending slots are skipped
+ * and flagged); weights: device fp32 [C][k]; packed: the buffer written by
+ * moe_pack_weights; y: device fp32 [C][H] (overwritten).  Each selected
+ * expert's packed bytes are read once per call whatever number of tokens
+ * chose it.  The sum over a token's experts runs in ascending expert id
+ * order, so results are bitwise reproducible. */
+moe_status moe_forward(moe_layer_t layer, const uint16_t *x, int num_tokens,
+                       const int32_t *ids, const float *weights, const void *packed,
+                       float *y, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronise `stream`, return the device flag bits accumulated in `ws` since
+ * the last call (MOE_FLAG_*), and clear them. */
+moe_status moe_get_device_status(moe_layer_t layer, void *ws, cudaStream_t stream,
+                                 int32_t *flags);
+
+/* Optional timing hook: when `events` is non-NULL, moe_forward records
+ * events[0] on its stream before its first kernel, events[1] after the
+ * gate/up kernel and events[2] after the down/combine kernel (n_events must
+ * be 3).  Pass NULL to switch it off.  Not thread-safe with respect to
+ * concurrent moe_forward calls on the same handle. */
+moe_status moe_set_stage_events(moe_layer_t layer, cudaEvent_t *events, int n_events);
+
+/* Static, NUL-terminated description of a status code. */
+const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

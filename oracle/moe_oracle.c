@@ -105,6 +105,20 @@ uint64_t oracle_expert_bytes(int64_t hidden, int64_t inter) {
   return 3 * one;
 }
 
+/* Value tables filled from the two decode functions above (16 and 256
+ * entries), so the matrix loops below look values up instead of calling
+ * ldexp per element.  Same numbers, exactly. */
+static double e2m1_table[16];
+static double e4m3_table[256];
+static int tables_ready = 0;
+
+static void init_tables(void) {
+  if (tables_ready) return;
+  for (int i = 0; i < 16; i++) e2m1_table[i] = oracle_e2m1_value((uint8_t)i);
+  for (int i = 0; i < 256; i++) e4m3_table[i] = oracle_e4m3_value((uint8_t)i);
+  tables_ready = 1;
+}
+
 /* Weight (r, k) of one NVFP4 matrix [rows][K]:
  *   code  = nibble k%2 (low nibble for even k) of codes[r*K/2 + k/2]
  *   scale = scales[r*K/16 + k/16]
@@ -114,7 +128,7 @@ static double nvfp4_weight(const uint8_t *codes, const uint8_t *scales, float g,
   uint8_t byte = codes[r * (K / 2) + k / 2];
   uint8_t nibble = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
   uint8_t sbyte = scales[r * (K / 16) + k / 16];
-  return oracle_e2m1_value(nibble) * oracle_e4m3_value(sbyte) * (double)g;
+  return e2m1_table[nibble] * e4m3_table[sbyte] * (double)g;
 }
 
 /* Dense float64 copy of one NVFP4 matrix: out[rows][K].  Returns
@@ -123,6 +137,7 @@ int oracle_dequant(const uint8_t *codes, const uint8_t *scales, float g,
                    int64_t rows, int64_t K, double *out) {
   if (!codes || !scales || !out || rows < 0 || K <= 0 || K % 16 != 0)
     return ORACLE_ERR_ARG;
+  init_tables();
   for (int64_t i = 0; i < rows * (K / 16); i++)
     if (isnan(oracle_e4m3_value(scales[i]))) return ORACLE_ERR_NAN_SCALE;
   for (int64_t r = 0; r < rows; r++)
@@ -240,6 +255,7 @@ int oracle_expert_ffn(int H, int I,
                       const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
                       const double *x, double *y) {
   if (H <= 0 || I <= 0 || H % 16 || I % 16 || !x || !y) return ORACLE_ERR_ARG;
+  init_tables();
   for (int64_t i = 0; i < (int64_t)I * (H / 16); i++)
     if (isnan(oracle_e4m3_value(gate_scales[i])) || isnan(oracle_e4m3_value(up_scales[i])))
       return ORACLE_ERR_NAN_SCALE;

@@ -1,0 +1,272 @@
+// moe_api.cu -- the extern "C" entry points declared in include/moe.h.
+//
+// Host-side only: argument validation, packed/workspace layout arithmetic and
+// the launch sequence.  Every step of the computation runs in the kernels of
+// pack.cu, route.cu and expert_gemv.cu; there is no host or CPU fallback.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "kernels.h"
+#include "moe_internal.cuh"
+
+using moe::align_up;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    if (ok && prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int nt_index(int nt) { return nt <= 1 ? 0 : nt <= 2 ? 1 : nt <= 4 ? 2 : 3; }
+
+int gemv_grid(const moe_layer &L, int mode, int nt, long long max_rows) {
+  const int occ = L.gemv_occ[mode][nt_index(nt)];
+  long long g = (long long)L.num_sms * occ;
+  // at least two rows per CTA so that the CTA count never exceeds the work
+  const long long cap = (max_rows + 1) / 2;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+int pow2_tokens(int c) { return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8; }
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_INVALID_VALUE: return "invalid value (NaN e4m3 scale)";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_OUT_OF_MEMORY: return "out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BAD_EXPERT_ID: return "bad expert id";
+  }
+  return "unknown status";
+}
+
+moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out) {
+  if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+  const moe_config c = *cfg;
+  if (c.flags != 0 || c.max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c.top_k < 1 || c.top_k > moe::kMaxTopK || c.top_k > c.num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c.hidden < 64 || c.hidden % 64 || c.hidden > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c.intermediate < 64 || c.intermediate % 64 || c.intermediate > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe_layer *L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OUT_OF_MEMORY;
+  L->cfg = c;
+  L->device = device;
+  L->num_sms = sms;
+  L->Hp = (int)align_up(c.hidden, moe::kKAlign);
+  L->Ip = (int)align_up(c.intermediate, moe::kKAlign);
+  L->tpr_gu = L->Hp / 16;
+  L->tpr_dn = L->Ip / 16;
+  L->gu_pair_bytes = (size_t)L->tpr_gu * 18;
+  L->dn_pair_bytes = (size_t)L->tpr_dn * 18;
+  L->dn_region_off = (size_t)c.intermediate * L->gu_pair_bytes;
+  L->expert_bytes = L->dn_region_off + (size_t)(c.hidden / 2) * L->dn_pair_bytes;
+  L->scalars_off = (size_t)c.num_experts * L->expert_bytes;
+  L->trailer_off = align_up(L->scalars_off + (size_t)c.num_experts * 6 * sizeof(float), 16);
+  L->packed_bytes = L->trailer_off + 16;
+  L->n_chunks = (c.hidden / 2 + moe::kChunkPairRows - 1) / moe::kChunkPairRows;
+  L->stage_events_on = 0;
+  for (int j = 0; j < 4; j++) {
+    L->gemv_occ[0][j] = moe::gemv_occupancy(0, 1 << j, L->tpr_gu);
+    L->gemv_occ[1][j] = moe::gemv_occupancy(1, 1 << j, L->tpr_dn);
+  }
+  if (moe::route_setup(c.hidden) != cudaSuccess) {
+    delete L;
+    return MOE_ERR_CUDA;
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status moe_layer_destroy(moe_layer_t L) {
+  delete L;
+  return MOE_OK;
+}
+
+moe_status moe_packed_bytes(moe_layer_t L, size_t *bytes) {
+  if (!L || !bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = L->packed_bytes;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_bytes(moe_layer_t L, int num_tokens, size_t *bytes) {
+  if (!L || !bytes || num_tokens < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::ws_layout(*L, num_tokens).total;
+  return MOE_OK;
+}
+
+moe_status moe_pack_weights(moe_layer_t L, const moe_canonical_weights *cw, void *packed,
+                            cudaStream_t stream) {
+  if (!L || !cw || !packed) return MOE_ERR_INVALID_ARG;
+  const moe_fp4_tensor *ts[3] = {&cw->gate, &cw->up, &cw->down};
+  for (const moe_fp4_tensor *t : ts) {
+    if (!t->codes || !t->scales || !t->global_scale || !t->input_scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(t->codes)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(packed)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  uint8_t *pk = static_cast<uint8_t *>(packed);
+  int32_t *status = reinterpret_cast<int32_t *>(pk + L->trailer_off);
+  cudaError_t err = cudaMemsetAsync(pk + L->trailer_off, 0, 16, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  moe::PackArgs a;
+  a.gate_codes = cw->gate.codes; a.gate_scales = cw->gate.scales;
+  a.up_codes = cw->up.codes; a.up_scales = cw->up.scales;
+  a.down_codes = cw->down.codes; a.down_scales = cw->down.scales;
+  a.gate_g = cw->gate.global_scale; a.gate_a = cw->gate.input_scale;
+  a.up_g = cw->up.global_scale; a.up_a = cw->up.input_scale;
+  a.down_g = cw->down.global_scale; a.down_a = cw->down.input_scale;
+  a.packed = pk;
+  a.status = status;
+  a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.I = L->cfg.intermediate;
+  a.tpr_gu = L->tpr_gu; a.tpr_dn = L->tpr_dn;
+  a.gu_pair_bytes = L->gu_pair_bytes; a.dn_pair_bytes = L->dn_pair_bytes;
+  a.dn_region_off = L->dn_region_off; a.expert_bytes = L->expert_bytes;
+  a.scalars_off = L->scalars_off;
+  err = moe::launch_pack(a, L->num_sms, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t host_status = 0;
+  err = cudaMemcpyAsync(&host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  return host_status ? MOE_ERR_INVALID_VALUE : MOE_OK;
+}
+
+moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_router,
+                     const float *bias, int32_t *ids, float *weights, void *ws,
+                     size_t ws_bytes, cudaStream_t stream) {
+  if (!L || !x || !w_router || !ids || !weights || !ws) return MOE_ERR_INVALID_ARG;
+  if (C < 1 || C > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const moe::WsLayout wl = moe::ws_layout(*L, C);
+  if (ws_bytes < wl.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceGuard guard(L->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  moe::RouteArgs a;
+  a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
+  a.logits = reinterpret_cast<float *>(w + wl.logits);
+  a.ticket = &reinterpret_cast<moe::WsControl *>(w)->route_ticket;
+  a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
+  cudaError_t err;
+  if (C <= moe::kRouteFusedTokens) {
+    const int grid = (a.E + 7) / 8 < L->num_sms ? (a.E + 7) / 8 : L->num_sms;
+    err = moe::launch_route_fused(a, grid, stream);
+  } else {
+    err = moe::launch_route_batched(a, stream);
+  }
+  return cuda_status(err);
+}
+
+moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *ids,
+                       const float *weights, const void *packed, float *y, void *ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (!L || !x || !ids || !weights || !packed || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (C < 1 || C > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const moe::WsLayout wl = moe::ws_layout(*L, C);
+  if (ws_bytes < wl.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceGuard guard(L->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  const uint8_t *pk = static_cast<const uint8_t *>(packed);
+  const int H = L->cfg.hidden, I = L->cfg.intermediate, k = L->cfg.top_k;
+
+  moe::GemvArgs a;
+  a.packed = pk;
+  a.scalars = reinterpret_cast<const float *>(pk + L->scalars_off);
+  a.hbuf = reinterpret_cast<float *>(w + wl.hbuf);
+  a.ypair = reinterpret_cast<float *>(w + wl.ypair);
+  a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
+  a.chunk_cnt = reinterpret_cast<uint32_t *>(w + wl.chunk_cnt);
+  a.k = k; a.E = L->cfg.num_experts; a.H = H; a.I = I;
+  a.expert_bytes = L->expert_bytes;
+
+  cudaError_t err = cudaSuccess;
+  if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
+  for (int t0 = 0; t0 < C && err == cudaSuccess; t0 += moe::kGemvTokens) {
+    const int Cg = (C - t0) < moe::kGemvTokens ? (C - t0) : moe::kGemvTokens;
+    const int nt = pow2_tokens(Cg);
+    a.C = Cg;
+    a.x = x + (size_t)t0 * H;
+    a.ids = ids + (size_t)t0 * k;
+    a.weights = weights + (size_t)t0 * k;
+    a.y = y + (size_t)t0 * H;
+    const long long max_pairs = (long long)Cg * k;
+    // gate/up + SwiGLU
+    a.region_off = 0;
+    a.pair_bytes = (int)L->gu_pair_bytes;
+    a.rows = I;
+    err = moe::launch_expert_gemv(0, nt, a, L->tpr_gu,
+                                  gemv_grid(*L, 0, nt, max_pairs * I), true, stream);
+    if (err != cudaSuccess) break;
+    if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
+    if (err != cudaSuccess) break;
+    // down + combine
+    a.region_off = L->dn_region_off;
+    a.pair_bytes = (int)L->dn_pair_bytes;
+    a.rows = H / 2;
+    err = moe::launch_expert_gemv(1, nt, a, L->tpr_dn,
+                                  gemv_grid(*L, 1, nt, max_pairs * (H / 2)), true, stream);
+  }
+  if (err == cudaSuccess && L->stage_events_on) err = cudaEventRecord(L->stage_events[2], stream);
+  return cuda_status(err);
+}
+
+moe_status moe_get_device_status(moe_layer_t L, void *ws, cudaStream_t stream, int32_t *flags) {
+  if (!L || !ws || !flags) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  int32_t *f = &static_cast<moe::WsControl *>(ws)->flags;
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err == cudaSuccess) err = cudaMemcpy(flags, f, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess) err = cudaMemsetAsync(f, 0, sizeof(int32_t), stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  return cuda_status(err);
+}
+
+moe_status moe_set_stage_events(moe_layer_t L, cudaEvent_t *events, int n_events) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (!events) {
+    L->stage_events_on = 0;
+    return MOE_OK;
+  }
+  if (n_events != 3) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; i++) L->stage_events[i] = events[i];
+  L->stage_events_on = 1;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+// moe_internal.cuh -- layer handle, packed-layout arithmetic and PTX helpers
+// shared by the kernels of the routed NVFP4 MoE library (sm_103a only).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "this library is written for Blackwell (sm_103a); build with -gencode arch=compute_103a,code=sm_103a"
+#endif
+
+namespace moe {
+
+// ----------------------------------------------------------------- limits
+constexpr int kMaxExperts = 1024;        // dispatch bitmap: 32 words of 32 bits
+constexpr int kMaxTopK = 32;             // one top-k slot per lane
+constexpr int kGemvTokens = 8;           // tokens per GEMV group (token mask bits)
+constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
+constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
+constexpr int kChunkPairRows = 32;       // down/combine row chunk: 64 output rows
+constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
+
+// Workspace control block (first 256 bytes of the workspace).
+struct WsControl {
+  int32_t flags;          // MOE_FLAG_* bits, cleared by moe_get_device_status
+  uint32_t route_ticket;  // CTAs of the router that finished their logits
+  uint32_t pad[62];
+};
+static_assert(sizeof(WsControl) == 256, "control block is 256 bytes");
+
+// Byte offsets of the workspace regions for a group of up to kGemvTokens
+// tokens (GEMV path) and C tokens of router logits.
+struct WsLayout {
+  size_t chunk_cnt;   // uint32 [n_chunks]
+  size_t logits;      // float  [C][E]
+  size_t hbuf;        // float  [kGemvTokens * k][I]  w * silu(g) * u per (token, slot)
+  size_t ypair;       // float  [kGemvTokens * k][H]  D_e h per (token, slot)
+  size_t total;
+};
+
+}  // namespace moe
+
+// The handle.  Immutable after moe_layer_create except for the optional
+// stage-event hook.
+struct moe_layer {
+  moe_config cfg;
+  int device;
+  int num_sms;
+  int Hp, Ip;                 // K of gate/up and of down, padded to kKAlign
+  int tpr_gu, tpr_dn;         // threads of one pair row = Kp / 16
+  size_t gu_pair_bytes;       // tpr_gu * 18
+  size_t dn_pair_bytes;       // tpr_dn * 18
+  size_t dn_region_off;       // offset of the down pair rows inside an expert
+  size_t expert_bytes;        // packed bytes of one expert (without scalars)
+  size_t scalars_off;         // float [E][6] : g_gate a_gate g_up a_up g_down a_down
+  size_t trailer_off;         // 16-byte status trailer written by the packer
+  size_t packed_bytes;
+  int n_chunks;               // ceil((H/2) / kChunkPairRows)
+  int gemv_occ[2][4];         // CTAs per SM of the gemv kernels [mode][log2 NT]
+  cudaEvent_t stage_events[3];
+  int stage_events_on;
+};
+
+namespace moe {
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline WsLayout ws_layout(const moe_layer &L, int C) {
+  WsLayout w;
+  size_t off = sizeof(WsControl);
+  w.chunk_cnt = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)L.n_chunks, 256);
+  w.logits = off;
+  off = align_up(off + sizeof(float) * (size_t)C * L.cfg.num_experts, 256);
+  const size_t pairs = (size_t)kGemvTokens * L.cfg.top_k;
+  w.hbuf = off;
+  off = align_up(off + sizeof(float) * pairs * L.cfg.intermediate, 256);
+  w.ypair = off;
+  off = align_up(off + sizeof(float) * pairs * L.cfg.hidden, 256);
+  w.total = off;
+  return w;
+}
+
+// ------------------------------------------------------------ PTX helpers
+#ifdef __CUDACC__
+
+// Streaming 16-byte load: no L1 allocation, L2 evict-first (the weights are
+// read once per call; keep L2 for the activations and partial sums).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void *ptr, uint64_t pol) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;"
+               : "=h"(v)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
+// Four e2m1 pairs (one 32-bit word = 8 codes, low nibble first) -> four
+// f16x2 words; word i holds elements 2i (low half) and 2i+1 (high half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Two e4m3 bytes (low byte first) -> two fp32 values.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(two_bytes));
+  __half2 hh = *reinterpret_cast<__half2 *>(&h2);
+  return __half22float2(hh);
+}
+
+// acc += a.lo * b.lo + a.hi * b.hi with f16 inputs and fp32 accumulation
+// (mixed-precision fma, sm_100+): each product of two f16 values is exact in
+// fp32 and is rounded once when added.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
+
+// Packed fp32x2 fma: (d.x, d.y) = (a.x*b.x + c.x, a.y*b.y + c.y).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra = *reinterpret_cast<uint64_t *>(&a), rb = *reinterpret_cast<uint64_t *>(&b),
+           rc = *reinterpret_cast<uint64_t *>(&c), rd;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2 *>(&rd);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

@@ -1,0 +1,76 @@
+"""Device-side synthetic NVFP4 layers (the CUDA twin of the host generator).
+
+Full K3-shape layers (16.6 GB of canonical NVFP4 each) are generated on the
+GPU by ``synth.cu``; they are bit-identical to ``canonical_layer`` in this
+package's ``__init__`` (a GPU test checks a sample).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+from . import (MAT_DOWN, MAT_GATE, MAT_UP, W_COEF, global_scales, weight_key)
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                         "_lib", "libmoe_synth.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is missing: run the package build first")
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.synth_generate_matrices.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.synth_generate_matrices.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def canonical_layer_device(seed: int, layer: int, E: int, H: int, I: int, device="cuda:0",
+                           stream=None):
+    """Canonical NVFP4 layer on the device: dict gate/up/down -> {'codes',
+    'scales', 'g', 'a'} torch tensors ([E][rows][K/2] uint8, [E][rows][K/16]
+    uint8, [E] float32, [E] float32)."""
+    lib = _load()
+    g, a = global_scales(seed, layer, E)
+    stream = stream or torch.cuda.current_stream(device)
+    out = {}
+    for mat, name, rows, K in ((MAT_GATE, "gate", I, H), (MAT_UP, "up", I, H), (MAT_DOWN, "down", H, I)):
+        keys = np.array([weight_key(seed, layer, e, mat) for e in range(E)], dtype=np.uint64)
+        keys_d = torch.from_numpy(keys.view(np.int64)).to(device)
+        g_d = torch.from_numpy(g[mat].copy()).to(device)
+        a_d = torch.from_numpy(a[mat].copy()).to(device)
+        codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty((E, rows, K // 16), dtype=torch.uint8, device=device)
+        rc = lib.synth_generate_matrices(keys_d.data_ptr(), g_d.data_ptr(), E, rows, K, W_COEF,
+                                         codes.data_ptr(), scales.data_ptr(),
+                                         ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"synth_generate_matrices failed with cudaError {rc}")
+        out[name] = {"codes": codes, "scales": scales, "g": g_d, "a": a_d, "_keys": keys_d}
+    return out
+
+
+def gather_to_host(canon_dev: dict, experts) -> dict:
+    """Copy the listed experts' canonical NVFP4 matrices to host numpy arrays
+    (the oracle's input for full-size layers)."""
+    idx = torch.as_tensor(list(experts), dtype=torch.long, device=canon_dev["gate"]["codes"].device)
+    out = {}
+    for name, m in canon_dev.items():
+        out[name] = {f: m[f].index_select(0, idx).cpu().numpy() for f in ("codes", "scales", "g", "a")}
+    return out
+
+
+def free(canon_dev: dict) -> None:
+    for m in canon_dev.values():
+        m.clear()

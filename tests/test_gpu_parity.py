@@ -1,0 +1,281 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs.  Selected ids must match bit for bit (the generator
+keeps a >= 1e-3 logit gap at the k-th boundary); outputs must meet the
+acceptance tolerance in ``helpers``."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import MIN_GAP, assert_close, gapped_tokens
+from quantized_moe_expert_router_gb300 import moe, synth
+from quantized_moe_expert_router_gb300.synth import device as synth_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from quantized_moe_expert_router_gb300 import build
+    build.build()
+    moe.load_library()
+
+
+def to_device(canon_h):
+    return {n: {f: torch.from_numpy(np.ascontiguousarray(m[f])).to(DEV) for f in ("codes", "scales", "g", "a")}
+            for n, m in canon_h.items()}
+
+
+class GpuLayer:
+    def __init__(self, E, k, H, I, max_tokens, seed=0, layer=0, device_gen=False, router_std=1.0,
+                 zipf=False):
+        self.E, self.k, self.H, self.I = E, k, H, I
+        self.seed, self.layer_id = seed, layer
+        self.h = moe.Layer(E, k, H, I, max_tokens)
+        if device_gen:
+            self.canon = synth_dev.canonical_layer_device(seed, layer, E, H, I, DEV)
+        else:
+            self.canon_h = synth.canonical_layer(seed, layer, E, H, I)
+            self.canon = to_device(self.canon_h)
+        self.packed = moe.alloc_packed(self.h)
+        moe.moe_pack_weights(self.h, self.canon, self.packed)
+        self.Wr = synth.router_weights(seed, layer, E, H, router_std)
+        self.bias = synth.zipf_bias(seed, layer, E) if zipf else None
+        self.Wr_d = torch.from_numpy(self.Wr).to(DEV)
+        self.bias_d = None if self.bias is None else torch.from_numpy(self.bias).to(DEV)
+        self.ws = moe.alloc_workspace(self.h, max_tokens)
+
+    def host_weights(self, experts):
+        if hasattr(self, "canon_h"):
+            return {n: {f: m[f][list(experts)] for f in ("codes", "scales", "g", "a")}
+                    for n, m in self.canon_h.items()}
+        return synth_dev.gather_to_host(self.canon, experts)
+
+    def run(self, x_bits):
+        C = x_bits.shape[0]
+        x = torch.from_numpy(x_bits.view(np.int16)).to(DEV)
+        ids = torch.empty((C, self.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((C, self.k), dtype=torch.float32, device=DEV)
+        y = torch.empty((C, self.H), dtype=torch.float32, device=DEV)
+        moe.moe_route(self.h, x, C, self.Wr_d, self.bias_d, ids, w, self.ws)
+        moe.moe_forward(self.h, x, C, ids, w, self.packed, y, self.ws)
+        torch.cuda.synchronize()
+        return ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+
+    def oracle(self, x_bits):
+        """Oracle routing + forward on the selected experts only."""
+        logits = oracle.router_logits(self.Wr, x_bits, self.bias)
+        ids, w, gap = oracle.route(logits, self.k)
+        sel = sorted(set(int(e) for e in ids.ravel()))
+        remap = {e: i for i, e in enumerate(sel)}
+        y = oracle.moe_forward(self.host_weights(sel), x_bits, np.vectorize(remap.get)(ids).astype(np.int32), w)
+        return ids, w, gap, y
+
+
+def check_layer(L, x_bits, label):
+    ids, w, y = L.run(x_bits)
+    oids, ow, gap, oy = L.oracle(x_bits)
+    assert (gap >= MIN_GAP).all()
+    assert (ids == oids).all(), f"{label}: ids differ\n{ids}\n{oids}"
+    np.testing.assert_allclose(w, ow, rtol=2e-5, atol=1e-7)
+    assert abs(w.sum(1) - 1).max() < 1e-5
+    flags = moe.moe_get_device_status(L.h, L.ws)
+    assert flags == 0, f"{label}: device flags {flags:#x}"
+    return assert_close(y, oy, label)
+
+
+# ------------------------------------------------------------------ generator
+
+def test_device_generator_matches_host():
+    E, H, I = 5, 256, 192
+    d = synth_dev.canonical_layer_device(0, 3, E, H, I, DEV)
+    h = synth.canonical_layer(0, 3, E, H, I)
+    for n in ("gate", "up", "down"):
+        for f in ("codes", "scales", "g", "a"):
+            assert (d[n][f].cpu().numpy() == h[n][f]).all(), (n, f)
+
+
+def test_device_generator_matches_host_k3_expert():
+    E, H, I = 2, 3584, 3072
+    d = synth_dev.canonical_layer_device(7, 1, E, H, I, DEV)
+    h = synth.canonical_layer(7, 1, E, H, I, experts=[1])
+    for n in ("gate", "up", "down"):
+        assert (d[n]["codes"][1].cpu().numpy() == h[n]["codes"][0]).all(), n
+        assert (d[n]["scales"][1].cpu().numpy() == h[n]["scales"][0]).all(), n
+
+
+# ------------------------------------------------------------------ packer
+
+def unpack_host(packed, E, H, I):
+    """Reverse the packed layout on the host (byte moves only)."""
+    Hp, Ip = -(-H // 512) * 512, -(-I // 512) * 512
+    tg, td = Hp // 16, Ip // 16
+    gpb, dpb = tg * 18, td * 18
+    ebytes = I * gpb + (H // 2) * dpb
+    out = {n: {"codes": np.zeros((E, r, K // 2), np.uint8), "scales": np.zeros((E, r, K // 16), np.uint8)}
+           for n, r, K in (("gate", I, H), ("up", I, H), ("down", H, I))}
+    for e in range(E):
+        base = e * ebytes
+        gu = packed[base: base + I * gpb].reshape(I, gpb)
+        codes = gu[:, :tg * 16].reshape(I, tg, 16)[:, :H // 16]
+        sc = gu[:, tg * 16:].reshape(I, tg, 2)[:, :H // 16]
+        out["gate"]["codes"][e] = codes[:, :, :8].reshape(I, H // 2)
+        out["up"]["codes"][e] = codes[:, :, 8:].reshape(I, H // 2)
+        out["gate"]["scales"][e] = sc[:, :, 0]
+        out["up"]["scales"][e] = sc[:, :, 1]
+        dn = packed[base + I * gpb: base + ebytes].reshape(H // 2, dpb)
+        codes = dn[:, :td * 16].reshape(H // 2, td, 16)[:, :I // 16]
+        sc = dn[:, td * 16:].reshape(H // 2, td, 2)[:, :I // 16]
+        out["down"]["codes"][e][0::2] = codes[:, :, :8].reshape(H // 2, I // 2)
+        out["down"]["codes"][e][1::2] = codes[:, :, 8:].reshape(H // 2, I // 2)
+        out["down"]["scales"][e][0::2] = sc[:, :, 0]
+        out["down"]["scales"][e][1::2] = sc[:, :, 1]
+    scal = packed[E * ebytes: E * ebytes + E * 24].view(np.float32).reshape(E, 6)
+    return out, scal
+
+
+@pytest.mark.parametrize("E,H,I", [(32, 256, 192), (3, 1024, 512)])
+def test_pack_layout_roundtrip(E, H, I):
+    L = GpuLayer(E, 2, H, I, 1)
+    packed = L.packed.cpu().numpy()
+    assert packed.size == moe.moe_packed_bytes(L.h)
+    un, scal = unpack_host(packed, E, H, I)
+    for n in ("gate", "up", "down"):
+        assert (un[n]["codes"] == L.canon_h[n]["codes"]).all(), n
+        assert (un[n]["scales"] == L.canon_h[n]["scales"]).all(), n
+    for j, (n, f) in enumerate([("gate", "g"), ("gate", "a"), ("up", "g"), ("up", "a"), ("down", "g"), ("down", "a")]):
+        assert (scal[:, j] == L.canon_h[n][f]).all()
+
+
+def test_packed_bytes_equal_canonical_for_k3_shape():
+    h = moe.Layer(896, 16, 3584, 3072, 1)
+    assert moe.moe_packed_bytes(h) == 896 * oracle.expert_bytes(3584, 3072) + 16
+
+
+def test_pack_rejects_nan_scale():
+    L = GpuLayer(4, 2, 256, 192, 1)
+    L.canon["down"]["scales"][2, 5, 3] = 0x7F
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_pack_weights(L.h, L.canon, L.packed)
+    assert ei.value.status == 3
+
+
+# ------------------------------------------------------------------ parity, small
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 7, 8, 11])
+def test_tiny_layer_parity(C):
+    L = GpuLayer(32, 4, 256, 192, 16)
+    x = gapped_tokens(0, 0, C, 256, L.Wr, 4)
+    check_layer(L, x, f"tiny C={C}")
+
+
+@pytest.mark.parametrize("E,k,H,I,C", [(12, 3, 64, 96, 5), (40, 8, 576, 320, 2), (64, 32, 128, 64, 3),
+                                       (7, 7, 192, 1088, 1)])
+def test_odd_shapes_parity(E, k, H, I, C):
+    L = GpuLayer(E, k, H, I, C, seed=3)
+    x = gapped_tokens(3, 0, C, H, L.Wr, k)
+    check_layer(L, x, f"E{E} k{k} H{H} I{I} C{C}")
+
+
+def test_forward_is_deterministic():
+    L = GpuLayer(32, 4, 256, 192, 8)
+    x = gapped_tokens(0, 0, 8, 256, L.Wr, 4)
+    _, _, y1 = L.run(x)
+    _, _, y2 = L.run(x)
+    assert (y1 == y2).all()
+
+
+def test_bad_and_duplicate_ids_are_flagged_and_skipped():
+    L = GpuLayer(32, 4, 256, 192, 2)
+    x_bits = gapped_tokens(0, 0, 2, 256, L.Wr, 4)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV)
+    ids = torch.tensor([[1, 5, 40, 9], [3, 3, 7, 8]], dtype=torch.int32, device=DEV)
+    w = torch.tensor([[0.1, 0.2, 0.3, 0.4], [0.25, 0.25, 0.25, 0.25]], dtype=torch.float32, device=DEV)
+    y = torch.empty((2, 256), dtype=torch.float32, device=DEV)
+    moe.moe_forward(L.h, x, 2, ids, w, L.packed, y, L.ws)
+    flags = moe.moe_get_device_status(L.h, L.ws)
+    assert flags & moe.FLAG_BAD_EXPERT_ID and flags & moe.FLAG_DUPLICATE_ID
+    # token 0 without its bad slot is exact; token 1 keeps one copy of expert 3
+    y0 = oracle.moe_forward(L.host_weights(range(32)), x_bits[:1], np.array([[1, 5, 9]], np.int32),
+                            np.array([[0.1, 0.2, 0.4]]))
+    assert_close(y.cpu().numpy()[:1], y0, "bad id")
+    y1 = oracle.moe_forward(L.host_weights(range(32)), x_bits[1:], np.array([[3, 7, 8]], np.int32),
+                            np.array([[0.25, 0.25, 0.25]]))
+    assert_close(y.cpu().numpy()[1:], y1, "duplicate id")
+    assert moe.moe_get_device_status(L.h, L.ws) == 0    # cleared
+
+
+def test_argument_errors_return_status_without_launch():
+    L = GpuLayer(32, 4, 256, 192, 2)
+    x = torch.zeros((2, 256), dtype=torch.int16, device=DEV)
+    ids = torch.zeros((2, 4), dtype=torch.int32, device=DEV)
+    w = torch.zeros((2, 4), dtype=torch.float32, device=DEV)
+    y = torch.empty((2, 256), dtype=torch.float32, device=DEV)
+    small = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_forward(L.h, x, 2, ids, w, L.packed, y, small)
+    assert ei.value.status == 4
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_forward(L.h, x, 3, ids, w, L.packed, y, L.ws)       # C > max_tokens
+    assert ei.value.status == 1
+    ybuf = torch.empty(2 * 256 + 1, dtype=torch.float32, device=DEV)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_forward(L.h, x, 2, ids, w, L.packed, ybuf[1:], L.ws)  # misaligned y
+    assert ei.value.status == 1
+    for bad in [(0, 4, 256, 192), (32, 0, 256, 192), (32, 33, 256, 192), (32, 4, 100, 192), (32, 4, 256, 8192),
+                (2000, 4, 256, 192)]:
+        with pytest.raises(moe.MoEError):
+            moe.Layer(*bad, 1)
+
+
+# ------------------------------------------------------------------ K3 shape
+
+@pytest.fixture(scope="module")
+def k3_layer():
+    L = GpuLayer(896, 16, 3584, 3072, 8, seed=0, device_gen=True)
+    yield L
+    del L.canon
+
+
+def test_k3_router_parity(k3_layer):
+    L = k3_layer
+    x = gapped_tokens(0, 0, 8, 3584, L.Wr, 16)
+    for C in (1, 8):
+        xd = torch.from_numpy(x[:C].view(np.int16)).to(DEV)
+        ids = torch.empty((C, 16), dtype=torch.int32, device=DEV)
+        w = torch.empty((C, 16), dtype=torch.float32, device=DEV)
+        moe.moe_route(L.h, xd, C, L.Wr_d, None, ids, w, L.ws)
+        oids, ow, _ = oracle.route(oracle.router_logits(L.Wr, x[:C]), 16)
+        assert (ids.cpu().numpy() == oids).all()
+        np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-5, atol=1e-7)
+
+
+def test_k3_decode_batch1_parity(k3_layer):
+    L = k3_layer
+    x = gapped_tokens(0, 0, 1, 3584, L.Wr, 16)
+    check_layer(L, x, "k3 C=1 top-16")
+
+
+@pytest.mark.parametrize("k", [8, 16])
+def test_k3_decode_batch7_parity(k3_layer, k):
+    L = k3_layer
+    if k != 16:
+        h = moe.Layer(896, k, 3584, 3072, 8)
+        L = _retarget(k3_layer, h, k)
+    x = gapped_tokens(1, 0, 7, 3584, L.Wr, k)
+    check_layer(L, x, f"k3 C=7 top-{k}")
+
+
+def _retarget(L, h, k):
+    """Same weights, another top-k: a new handle over the same packed buffer."""
+    class View:
+        pass
+    v = View()
+    v.__dict__.update(L.__dict__)
+    v.h, v.k = h, k
+    v.ws = moe.alloc_workspace(h, 8)
+    v.run = GpuLayer.run.__get__(v)
+    v.oracle = GpuLayer.oracle.__get__(v)
+    v.host_weights = GpuLayer.host_weights.__get__(v)
+    return v
