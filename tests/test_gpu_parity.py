@@ -170,7 +170,7 @@ def test_tiny_layer_parity(C):
     check_layer(L, x, f"tiny C={C}")
 
 
-@pytest.mark.parametrize("E,k,H,I,C", [(12, 3, 64, 96, 5), (40, 8, 576, 320, 2), (64, 32, 128, 64, 3),
+@pytest.mark.parametrize("E,k,H,I,C", [(12, 3, 64, 128, 5), (40, 8, 576, 320, 2), (64, 32, 128, 64, 3),
                                        (7, 7, 192, 1088, 1)])
 def test_odd_shapes_parity(E, k, H, I, C):
     L = GpuLayer(E, k, H, I, C, seed=3)
