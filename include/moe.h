@@ -154,6 +154,23 @@ moe_status moe_get_device_status(moe_layer_t layer, void *ws, cudaStream_t strea
  * concurrent moe_forward calls on the same handle. */
 moe_status moe_set_stage_events(moe_layer_t layer, cudaEvent_t *events, int n_events);
 
+/* moe_route without a workspace.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- code running
+ * while a stream is captured in a mode that forbids cudaMalloc, plug-ins whose
+ * host framework owns every device buffer, and latency-critical loops that
+ * must not pay cudaMalloc's implicit synchronisation.  It computes exactly
+ * what moe_route computes (same kernel), keeping the router logits and its
+ * completion counter in a fixed 32 KiB + 256 B array inside the library
+ * (resident on every GPU that loads the library until the process exits).
+ * Arguments as moe_route, minus the workspace.  Limits: C <= 8 and
+ * C * num_experts <= 8192, otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
+ * is queued.  The first call on a device looks up the array's address; make
+ * it outside any stream capture.  All calls share the array, so calls that
+ * overlap on the GPU race: serialise them on one stream.  Allocates nothing. */
+moe_status moe_route_noalloc(moe_layer_t layer, const uint16_t *x, int num_tokens,
+                             const float *w_router, const float *bias, int32_t *ids,
+                             float *weights, cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *moe_status_string(moe_status status);
 

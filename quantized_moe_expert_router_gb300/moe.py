@@ -30,7 +30,7 @@ FLAG_TIMEOUT = 0x4
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",
     "moe_pack_weights", "moe_route", "moe_forward", "moe_get_device_status",
-    "moe_set_stage_events", "moe_status_string",
+    "moe_set_stage_events", "moe_route_noalloc", "moe_status_string",
 )
 
 
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH):
             lib.moe_forward.argtypes = [P, P, I32, P, P, P, P, P, SZ, P]
             lib.moe_get_device_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_set_stage_events.argtypes = [P, P, I32]
+            lib.moe_route_noalloc.argtypes = [P, P, I32, P, P, P, P, P]
             lib.moe_status_string.argtypes = [I32]
             lib.moe_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -166,6 +167,16 @@ def moe_forward(layer, x, num_tokens, ids, weights, packed, y, ws, stream=None) 
     _check("moe_forward", load_library().moe_forward(
         layer.handle, _ptr(x), num_tokens, _ptr(ids), _ptr(weights), _ptr(packed), _ptr(y),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_noalloc(layer, x, num_tokens, w_router, bias, ids, weights, stream=None) -> None:
+    """moe_route for callers that cannot allocate a workspace: the router's
+    scratch lives in a fixed array inside the library (C <= 8 tokens).  Calls
+    that overlap on the GPU share that array and race; the first call on a
+    device must happen outside stream capture."""
+    _check("moe_route_noalloc", load_library().moe_route_noalloc(
+        layer.handle, _ptr(x), num_tokens, _ptr(w_router), _ptr(bias), _ptr(ids), _ptr(weights),
+        _stream(stream)))
 
 
 def moe_get_device_status(layer, ws, stream=None) -> int:
