@@ -65,8 +65,8 @@ typedef enum {
 typedef struct {
   int32_t num_experts;   /* E, 1 .. 1024 */
   int32_t top_k;         /* k, 1 .. min(32, E) */
-  int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 16384 */
-  int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 16384 */
+  int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 4096 */
+  int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 4096 */
   int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
   uint32_t flags;        /* must be 0 */
 } moe_config;
