@@ -2,8 +2,7 @@
 //
 //   mode 0 (gate/up):  for every selected expert e and token t that chose it,
 //       g = G_e x_t, u = U_e x_t,  hbuf[(t,slot)] = w[t][slot] * silu(g) * u
-//   mode 1 (down):     ypair[(t,slot)] = D_e hbuf[(t,slot)], then
-//       y[t] = sum over t's experts, ascending expert id, of ypair[(t,slot)]
+//   mode 1 (down):     ypair[(t,slot)] = D_e hbuf[(t,slot)]
 //
 // The definition is the "MUL_MAT_ID" step of "Kimi-K3 on 2x A40 - measured
 // findings" (section "Why the placement experiments all looked the same") with
@@ -13,34 +12,55 @@
 // (D is linear).
 //
 // Work split.  The selected experts are de-duplicated in every CTA (a bitmap
-// over expert ids, popcount ranks = ascending expert order), so each expert's
-// bytes are streamed once whatever number of tokens chose it.  The flattened
-// list (distinct expert, pair row) is cut into equal contiguous ranges, one
-// per CTA, so every SM streams the same number of bytes (to one pair row).
-// Inside a CTA, thread b owns 16-element block b of K for every pair row: per
-// row it issues one 16-byte load of codes (two rows' blocks) and one 2-byte
-// load of their two e4m3 scales, decodes in registers
-// (cvt.rn.f16x2.e2m1x2) and accumulates in fp32.  Partial sums of 16/NT rows
-// x NT tokens x 2 rows are reduced across the CTA with one warp transpose-
-// reduction and one shared-memory pass.
+// over expert ids; popcount ranks give ascending expert order), so each
+// expert's bytes are streamed once whatever number of tokens chose it.  The
+// flattened list (distinct expert, tile of 8 pair rows) is cut into equal
+// contiguous ranges, one CTA per SM, so every SM streams the same bytes to
+// within one tile.  Tiles are contiguous in the packed layout (pack.cu).
 //
-// Gate/up uses x in f16 scaled by a power of two per token (exact: a bf16
-// value has 8 significant bits; the scale puts max|x| in [2^14, 2^15)) and
-// the sm_100 mixed-precision fma (f16 x f16 + fp32).  Down uses h in fp32
-// and packed fp32x2 fmas on the decoded weights.  The block scale multiplies
-// each 16-element partial sum in fp32; the tensor scale multiplies the row.
+// Streaming.  The CTA is warp-specialised and its warps never meet at a
+// CTA-wide barrier after the dispatch: one producer lane copies each tile with
+// one bulk copy (cp.async.bulk, global -> shared, completion counted on an
+// mbarrier) into a ring of S stage buffers, up to S tiles ahead; G consumer
+// groups of W warps take alternate tiles (warp w of a group owns K-slice w,
+// 32 k-steps of 16 elements) and hand their slice partials to one epilogue
+// warp through a ring of reduction slots, also tracked by mbarriers.  Every
+// wait is bounded (about two seconds of %globaltimer): on expiry the waiting
+// warp sets MOE_FLAG_TIMEOUT and leaves, and the producer waits (bounded) for
+// its copies still in flight before exiting.
 //
-// The down kernel combines without float atomics: every CTA counts, per
-// 64-row chunk, the pair rows it finished; the CTA that completes a chunk
-// (count == experts x rows) sums that chunk's ypair rows for every token in
-// ascending expert order and resets the count.  No CTA waits for another.
+// Compute.  Decoding stays in registers: per k-step a lane converts its 4
+// code bytes with cvt.rn.f16x2.e2m1x2 and multiplies them by the row's e4m3
+// block scale in f16 (exact: at most 2+4 significant bits, |value| <= 2688,
+// no subnormals).  The 16x16 block of decoded weights is the A fragment of
+// mma.m16n8k16 (rows g and g+8 = the two rows of pair row g of the tile), and
+// the MMA accumulates in fp32 across the warp's K-slice; the eight MMA columns
+// carry the decode batch:
+//   gate/up: column n = token n of the group (x in f16, scaled by a power of
+//            two per token and K-slice: exact for bf16 input);
+//   down:    columns 2j, 2j+1 = the hi and lo f16 parts of h for the j-th
+//            token that chose the expert (scaled by a power of two per token
+//            and K-slice), so hi + lo carries h to 2^-22.
+// The slice partials (each rescaled by 2^-s) are summed over the W warps by
+// the epilogue warp, which applies the tensor scale and writes hbuf / ypair.
+//
+// The weighted sum over a token's experts is the separate combine kernel
+// (combine.cu), which reads ypair in ascending expert order: no float atomics,
+// bitwise reproducible.
 #include "moe_internal.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kMaxGemvThreads = 256;   // K <= 4096
+constexpr int kSliceSteps = 32;                  // k-steps per warp K-slice
+constexpr int kMaxSliceWarps = 8;                // K <= 4096
+constexpr int kMaxGroups = 2;
+constexpr int kMaxCtaThreads = 512;              // 16 warps of 128 registers fill the register file
+constexpr int kRedSlots = 4;                     // consumer -> epilogue reduction ring
+constexpr int kMaxPasses = 2;                    // down kernel: 4 token slots per pass, C <= 8
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct DispatchSmem {
   uint32_t bitmap[kMaxExperts / 32];
@@ -48,18 +68,114 @@ struct DispatchSmem {
   int n;
   int16_t expert[kMaxPairs];
   uint32_t tokmask[kMaxPairs];
-  int16_t pair[kMaxPairs][kGemvTokens];
+  int pair[kMaxPairs][kGemvTokens];            // by token (lowest slot of a repeated id)
+  int16_t slot_pair[kMaxPairs][kGemvTokens];   // by slot (tokens in ascending order)
+  uint8_t nslot[kMaxPairs];
+  float wt[kMaxPairs];                         // router weight of pair p
+  float scal[kMaxPairs][3];                    // tensor scales g_gate, g_up, g_down of rank d
 };
 
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with `parity` to complete; false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; it++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void group_sync(int group, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// e4m3 pair (low byte: rowA scale, high byte: rowB scale) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v16));
+  return r;
+}
+// a * (s.lo, s.lo) and a * (s.hi, s.hi) in f16x2 (exact for code x scale).
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), __low2half2(*reinterpret_cast<const __half2 *>(&s)));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), __high2half2(*reinterpret_cast<const __half2 *>(&s)));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
+// Power of two 2^s with amax * 2^s in [2^14, 2^15) (s clamped to +-120);
+// returns 2^s and writes 2^-s.
+__device__ __forceinline__ float f16_range_scale(float amax, float *inv) {
+  int s = 0;
+  if (amax > 0.f) s = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127);
+  s = max(-120, min(120, s));
+  *inv = __uint_as_float((uint32_t)(127 - s) << 23);
+  return __uint_as_float((uint32_t)(127 + s) << 23);
+}
+
+// ---------------------------------------------------------------- dispatch
 // Distinct selected experts of this token group in ascending id order, with
-// for each the mask of tokens that chose it and the (token, slot) pair index
-// p = t*k + slot.  Ids outside [0,E) and repeats inside a token are flagged
-// and skipped.
-__device__ void build_dispatch(DispatchSmem &s, const int32_t *ids, int C, int k, int E,
-                               int32_t *flags) {
+// for each the tokens that chose it (mask, and the (token, slot) pair index
+// p = t*k + slot both by token and in ascending token order).  Ids outside
+// [0,E) are flagged and skipped; an id repeated inside a token is flagged and
+// only its lowest slot is used (the combine kernel applies the same rule).
+__device__ void build_dispatch(DispatchSmem &s, const int32_t *ids, const float *weights,
+                               const float *scalars, int C, int k, int E, int32_t *flags) {
   const int tid = threadIdx.x, nt = blockDim.x, P = C * k;
   for (int i = tid; i < kMaxExperts / 32; i += nt) s.bitmap[i] = 0u;
   for (int i = tid; i < P; i += nt) s.tokmask[i] = 0u;
+  for (int i = tid; i < P * kGemvTokens; i += nt) (&s.pair[0][0])[i] = 0x7FFFFFFF;
   __syncthreads();
   for (int p = tid; p < P; p += nt) {
     const int e = ids[p];
@@ -88,305 +204,346 @@ __device__ void build_dispatch(DispatchSmem &s, const int32_t *ids, int C, int k
     const int r = s.base[w] + __popc(s.bitmap[w] & ((1u << (e & 31)) - 1u));
     const int t = p / k;
     const uint32_t old = atomicOr(&s.tokmask[r], 1u << t);
-    if ((old >> t) & 1u)
-      atomicOr(flags, MOE_FLAG_DUPLICATE_ID);
-    else
-      s.pair[r][t] = (int16_t)p;
+    if ((old >> t) & 1u) atomicOr(flags, MOE_FLAG_DUPLICATE_ID);
+    atomicMin(&s.pair[r][t], p);
     s.expert[r] = (int16_t)e;
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += nt) s.wt[p] = weights[p];
+  for (int r = tid; r < s.n; r += nt) {
+    const float *sc = scalars + (size_t)s.expert[r] * 6;
+    s.scal[r][0] = sc[0];
+    s.scal[r][1] = sc[2];
+    s.scal[r][2] = sc[4];
+    uint32_t m = s.tokmask[r];
+    int j = 0;
+    while (m) {
+      const int t = __ffs(m) - 1;
+      m &= m - 1u;
+      s.slot_pair[r][j++] = (int16_t)s.pair[r][t];
+    }
+    s.nslot[r] = (uint8_t)j;
   }
   __syncthreads();
 }
 
-// Sum 32 per-lane values over the warp; lane l returns the sum of value l.
-// Five butterfly steps, each halving the values a lane keeps.
-__device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; i++) {
-      const float send = up ? v[i] : v[i + o];
-      const float keep = up ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFull, send, o);
-    }
-  }
-  return v[0];
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
-
-template <int MODE, int NT>
-__global__ void __launch_bounds__(kMaxGemvThreads) expert_gemv_kernel(const GemvArgs a) {
-  constexpr int R = 16 / NT;          // pair rows per batch
-  constexpr int V = 2 * NT * R;       // partial sums per thread per batch
-  static_assert(V == 32, "one value per lane after the transpose-reduction");
+template <int MODE>
+__global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];   // [S][stage_bytes] then the reduction slots
   __shared__ DispatchSmem ds;
-  __shared__ float red[kMaxGemvThreads / 32][33];
-  __shared__ float tok_inv[NT];
-  __shared__ uint32_t tok_amax[kMaxGemvThreads / 32][NT];
-  __shared__ int s_chunk;
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t red_full[kRedSlots];
+  __shared__ __align__(8) uint64_t red_empty[kRedSlots];
 
-  const int b = threadIdx.x, TPR = blockDim.x;
-  const int lane = b & 31, warp = b >> 5, nwarps = TPR >> 5;
-  const int kb = 16 * b;                          // first K element of this thread
-  const uint64_t pol = l2_evict_first_policy();
+  const int W = a.slice_warps, G = a.groups, S = a.stages;
+  // reduction slots [kRedSlots][passes][W][32 lanes] of float4, after the ring
+  float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);
+  const int npass_max = MODE == 0 ? 1 : kMaxPasses;
+  auto red_at = [&](int rs, int pass, int ww, int l) -> float4 & {
+    return red[(((size_t)rs * npass_max + pass) * W + ww) * 32 + l];
+  };
+  const int ncons_warps = W * G;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool is_producer = warp == ncons_warps;
+  const bool is_epilogue = warp == ncons_warps + 1;
+  const bool is_consumer = warp < ncons_warps;
+  const int grp = warp / W, w = warp % W;
+  const int g = lane >> 2, q = lane & 3;
+  const int K = MODE == 0 ? a.H : a.I;          // real K of this region's rows
 
-  // ---------------- operand prologue (does not depend on the previous kernel)
-  uint32_t xh[MODE == 0 ? NT : 1][8];
-  float hv[MODE == 1 ? NT : 1][16];
-  if constexpr (MODE == 0) {
-    float xf[NT][16];
-#pragma unroll
-    for (int t = 0; t < NT; t++) {
-      uint32_t am = 0;
-      if (t < a.C && kb < a.H) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + kb);
-        const uint4 v0 = src[0], v1 = src[1];
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          xf[t][2 * i] = __uint_as_float(w[i] << 16);
-          xf[t][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; i++) am = max(am, __float_as_uint(fabsf(xf[t][i])));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; i++) xf[t][i] = 0.f;
-      }
-      am = __reduce_max_sync(kFull, am);
-      if (lane == 0) tok_amax[warp][t] = am;
+  if (tid == 32 * ncons_warps) {
+    for (int s = 0; s < S; s++) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], W);
     }
-    __syncthreads();
+    for (int s = 0; s < kRedSlots; s++) {
+      mbar_init(&red_full[s], W);
+      mbar_init(&red_empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  // ---------------- B fragments of x (gate/up), independent of the router
+  uint32_t bf[kSliceSteps][2];
+  float colinv0 = 1.f, colinv1 = 1.f;           // 2^-s of accumulator columns 2q, 2q+1
+  if constexpr (MODE == 0) {
+    if (is_consumer) {
+      float am = 0.f;
+      const bool tok = g < a.C;
+      const uint16_t *xr = a.x + (size_t)(tok ? g : 0) * a.H;
 #pragma unroll
-    for (int t = 0; t < NT; t++) {
-      uint32_t am = 0;
-      for (int w = 0; w < nwarps; w++) am = max(am, tok_amax[w][t]);
-      // power of two putting max|x| in [2^14, 2^15): exact rescale into f16
-      int s = 0;
-      if (am != 0u) s = 14 - ((int)((am >> 23) & 0xFF) - 127);
-      s = max(-126, min(126, s));
-      const float up = __uint_as_float((uint32_t)(127 + s) << 23);
-      if (b == 0) tok_inv[t] = __uint_as_float((uint32_t)(127 - s) << 23);
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const __half2 h = __floats2half2_rn(xf[t][2 * i] * up, xf[t][2 * i + 1] * up);
-        xh[t][i] = *reinterpret_cast<const uint32_t *>(&h);
+      for (int s = 0; s < kSliceSteps; s++) {
+        const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
+        uint32_t v0 = 0, v1 = 0;
+        if (tok && k0 < K) {
+          v0 = *reinterpret_cast<const uint32_t *>(xr + k0);
+          v1 = *reinterpret_cast<const uint32_t *>(xr + k0 + 8);
+        }
+        bf[s][0] = v0;
+        bf[s][1] = v1;
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(__uint_as_float(v0 << 16)), fabsf(__uint_as_float(v0 & 0xFFFF0000u))),
+                             fmaxf(fabsf(__uint_as_float(v1 << 16)), fabsf(__uint_as_float(v1 & 0xFFFF0000u)))));
       }
+      am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+      float inv;
+      const float up = f16_range_scale(am, &inv);
+#pragma unroll
+      for (int s = 0; s < kSliceSteps; s++)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const uint32_t v = bf[s][h];
+          bf[s][h] = pack_half2(__uint_as_float(v << 16) * up, __uint_as_float(v & 0xFFFF0000u) * up);
+        }
+      colinv0 = __shfl_sync(kFull, inv, (2 * q) * 4);
+      colinv1 = __shfl_sync(kFull, inv, (2 * q + 1) * 4);
     }
   }
 
-  pdl_wait();   // ids/weights (router) for gate/up; hbuf (gate/up) for down
-  build_dispatch(ds, a.ids, a.C, a.k, a.E, a.flags);
+  if constexpr (MODE == 0) pdl_wait();           // ids/weights come from the router
+  build_dispatch(ds, a.ids, a.weights, a.scalars, a.C, a.k, a.E, a.flags);
   pdl_launch_dependents();
 
   const int n = ds.n;
-  if (MODE == 1 && n == 0) {
-    // nothing routed: the combine never triggers, so write zeros here
-    if (blockIdx.x == 0)
-      for (int i = b; i < a.C * a.H; i += TPR) a.y[i] = 0.f;
+  const long long T = (long long)n * a.tiles;
+  const long long t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
+  const int nstage = (int)(t1 - t0);
+
+  if (is_producer) {
+    // ------------------------------------------------ producer: bulk copies
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int i = 0;
+      bool ok = true;
+      for (; i < nstage; i++) {
+        const int slot = i % S;
+        const uint32_t use = (uint32_t)(i / S);
+        if (use > 0 && !mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1u)) {
+          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const long long u = t0 + i;
+        const int d = (int)(u / a.tiles), tile = (int)(u % a.tiles);
+        const uint8_t *src = a.packed + (size_t)ds.expert[d] * a.expert_bytes + a.region_off +
+                             (size_t)tile * a.tile_bytes;
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)a.tile_bytes);
+        bulk_copy_g2s(ring + (size_t)slot * a.stage_bytes, src, (uint32_t)a.tile_bytes, &full_bar[slot], pol);
+      }
+      if (!ok) {
+        // leave no copy in flight: wait (bounded) for the last use of each slot
+        for (int j = (i > S ? i - S : 0); j < i; j++)
+          mbar_wait_bounded(&full_bar[j % S], (uint32_t)(j / S) & 1u);
+      }
+    }
     return;
   }
-  const long long Q = (long long)n * a.rows;
-  long long q = Q * blockIdx.x / gridDim.x;
-  const long long q1 = Q * (blockIdx.x + 1) / gridDim.x;
-  int cur_d = -1;
-  if (b == 0) s_chunk = -1;
 
-  while (q < q1) {
-    const int d = (int)(q / a.rows), r = (int)(q % a.rows);
-    int nr = (int)min((long long)R, q1 - q);
-    nr = min(nr, a.rows - r);
-    if (MODE == 1) nr = min(nr, kChunkPairRows - (r % kChunkPairRows));
-    const int e = ds.expert[d];
-    const uint32_t mask = ds.tokmask[d];
-
-    if constexpr (MODE == 1) {
-      if (d != cur_d) {
-        cur_d = d;
-#pragma unroll
-        for (int t = 0; t < NT; t++) {
-          if (((mask >> t) & 1u) && kb < a.I) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.hbuf + (size_t)ds.pair[d][t] * a.I + kb);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const float4 v = __ldcg(src + i);
-              hv[t][4 * i] = v.x; hv[t][4 * i + 1] = v.y; hv[t][4 * i + 2] = v.z; hv[t][4 * i + 3] = v.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; i++) hv[t][i] = 0.f;
-          }
+  if (is_epilogue) {
+    // ------------------------------------------------ epilogue warp
+    if constexpr (MODE == 1) pdl_wait();
+    for (int i = 0; i < nstage; i++) {
+      const int rs = i % kRedSlots;
+      if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(i / kRedSlots) & 1u)) {
+        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+        break;
+      }
+      const long long u = t0 + i;
+      const int d = (int)(u / a.tiles), tile = (int)(u % a.tiles);
+      const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
+      for (int pass = 0; pass < npass; pass++) {
+        float4 sum = red_at(rs, pass, 0, lane);
+        for (int ww = 1; ww < W; ww++) {
+          const float4 v = red_at(rs, pass, ww, lane);
+          sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
         }
-      }
-    }
-
-    const uint8_t *rowp = a.packed + (size_t)e * a.expert_bytes + a.region_off + (size_t)r * a.pair_bytes;
-    uint4 cw[R];
-    uint32_t sw[R];
-#pragma unroll
-    for (int j = 0; j < R; j++) {
-      if (j < nr) {
-        const uint8_t *p = rowp + (size_t)j * a.pair_bytes;
-        cw[j] = ld_stream_v4(p + b * 16, pol);
-        sw[j] = ld_stream_u16(p + (size_t)TPR * 16 + b * 2, pol);
-      } else {
-        cw[j] = make_uint4(0, 0, 0, 0);
-        sw[j] = 0u;
-      }
-    }
-
-    float acc[V];
-#pragma unroll
-    for (int j = 0; j < R; j++) {
-      const float2 sc = e4m3x2_to_float2(sw[j]);
-      uint32_t hA[8], hB[8];
-      {
-        uint32_t t4[4];
-        e2m1x8_to_f16x2(cw[j].x, t4);
-        hA[0] = t4[0]; hA[1] = t4[1]; hA[2] = t4[2]; hA[3] = t4[3];
-        e2m1x8_to_f16x2(cw[j].y, t4);
-        hA[4] = t4[0]; hA[5] = t4[1]; hA[6] = t4[2]; hA[7] = t4[3];
-        e2m1x8_to_f16x2(cw[j].z, t4);
-        hB[0] = t4[0]; hB[1] = t4[1]; hB[2] = t4[2]; hB[3] = t4[3];
-        e2m1x8_to_f16x2(cw[j].w, t4);
-        hB[4] = t4[0]; hB[5] = t4[1]; hB[6] = t4[2]; hB[7] = t4[3];
-      }
-#pragma unroll
-      for (int t = 0; t < NT; t++) {
-        float dA = 0.f, dB = 0.f;
-        if ((mask >> t) & 1u) {
-          if constexpr (MODE == 0) {
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-              dA = fma2_f16_f32(hA[i], xh[t][i], dA);
-              dB = fma2_f16_f32(hB[i], xh[t][i], dB);
-            }
-          } else {
-            float2 pA = make_float2(0.f, 0.f), pB = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-              const float2 hvi = make_float2(hv[t][2 * i], hv[t][2 * i + 1]);
-              pA = ffma2(__half22float2(*reinterpret_cast<const __half2 *>(&hA[i])), hvi, pA);
-              pB = ffma2(__half22float2(*reinterpret_cast<const __half2 *>(&hB[i])), hvi, pB);
-            }
-            dA = pA.x + pA.y;
-            dB = pB.x + pB.y;
-          }
-        }
-        acc[(j * NT + t) * 2] = dA * sc.x;
-        acc[(j * NT + t) * 2 + 1] = dB * sc.y;
-      }
-    }
-
-    const float val = warp_transpose_reduce32(acc, lane);
-    red[warp][lane] = val;
-    __syncthreads();
-    if (warp == 0) {
-      float s = 0.f;
-      for (int w = 0; w < nwarps; w++) s += red[w][lane];
-      const float other = __shfl_xor_sync(kFull, s, 1);
-      const int jt = lane >> 1, j = jt / NT, t = jt % NT;
-      if ((lane & 1) == 0 && j < nr && ((mask >> t) & 1u)) {
-        const int p = ds.pair[d][t];
-        const float *sc = a.scalars + (size_t)e * 6;
         if constexpr (MODE == 0) {
-          const float inv = tok_inv[t];
-          const float g = s * sc[0] * inv, u = other * sc[2] * inv;
-          a.hbuf[(size_t)p * a.I + r + j] = a.weights[p] * silu(g) * u;
+          const int r = tile * 8 + g;
+          const uint32_t mask = ds.tokmask[d];
+#pragma unroll
+          for (int c2 = 0; c2 < 2; c2++) {
+            const int t = 2 * q + c2;
+            if (t < a.C && ((mask >> t) & 1u)) {
+              const int p = ds.pair[d][t];
+              const float gg = (c2 ? sum.y : sum.x) * ds.scal[d][0];
+              const float uu = (c2 ? sum.w : sum.z) * ds.scal[d][1];
+              a.hbuf[(size_t)p * a.I + r] = ds.wt[p] * silu(gg) * uu;
+            }
+          }
         } else {
-          const float gd = sc[4];
-          *reinterpret_cast<float2 *>(a.ypair + (size_t)p * a.H + 2 * (r + j)) = make_float2(s * gd, other * gd);
+          const int sl = 4 * pass + q;
+          if (sl < ds.nslot[d]) {
+            const int p = ds.slot_pair[d][sl];
+            const int pr = tile * 8 + g;
+            const float gd = ds.scal[d][2];
+            *reinterpret_cast<float2 *>(a.ypair + (size_t)p * a.H + 2 * pr) =
+                make_float2((sum.x + sum.y) * gd, (sum.z + sum.w) * gd);
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[rs]);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------- consumers
+  if constexpr (MODE == 1) pdl_wait();           // hbuf comes from the gate/up kernel
+  int cur_key = -1;                              // (expert rank, slot group) of bf
+  for (int i = grp; i < nstage; i += G) {
+    const int slot = i % S;
+    const long long u = t0 + i;
+    const int d = (int)(u / a.tiles);
+    const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
+
+    if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
+      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+      break;
+    }
+    const uint8_t *codes = ring + (size_t)slot * a.stage_bytes + (size_t)w * 4096;
+    const uint8_t *scales = ring + (size_t)slot * a.stage_bytes + (size_t)W * 4096 + (size_t)w * 512;
+    float4 res[kMaxPasses];
+
+    for (int pass = 0; pass < npass; pass++) {
       if constexpr (MODE == 1) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) {
-          const int c = r / kChunkPairRows;
-          const int csize = min(kChunkPairRows, a.rows - c * kChunkPairRows);
-          const unsigned old = atomicAdd(a.chunk_cnt + c, (unsigned)nr);
-          s_chunk = (old + nr == (unsigned)(n * csize)) ? c : -1;
+        const int key = d * 2 + pass;
+        if (key != cur_key) {
+          // B fragments of h: column g = slot 4*pass + g/2, hi (g even) / lo (g odd)
+          cur_key = key;
+          const int sl = 4 * pass + (g >> 1);
+          const bool have = sl < ds.nslot[d];
+          const float *hr = a.hbuf + (size_t)(have ? ds.slot_pair[d][sl] : 0) * a.I;
+          float am = 0.f;                        // first pass: max |h| of the slice
+#pragma unroll 8
+          for (int s = 0; s < kSliceSteps; s++) {
+            const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
+            if (have && k0 < K) {
+              const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(hr + k0));
+              const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(hr + k0 + 8));
+              am = fmaxf(am, fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v1.x), fabsf(v1.y))));
+            }
+          }
+          am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+          am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+          float inv;
+          const float up = f16_range_scale(am, &inv);
+          const bool lo = (g & 1) != 0;
+#pragma unroll
+          for (int s = 0; s < kSliceSteps; s++) {  // second pass: hi or lo f16 parts
+            const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
+            float2 v[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            if (have && k0 < K) {
+              v[0] = __ldcg(reinterpret_cast<const float2 *>(hr + k0));
+              v[1] = __ldcg(reinterpret_cast<const float2 *>(hr + k0 + 8));
+            }
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+              const float x0 = v[h].x * up, x1 = v[h].y * up;
+              const __half2 hi = __floats2half2_rn(x0, x1);
+              if (lo) {
+                const float2 hf = __half22float2(hi);
+                bf[s][h] = pack_half2(x0 - hf.x, x1 - hf.y);
+              } else {
+                bf[s][h] = *reinterpret_cast<const uint32_t *>(&hi);
+              }
+            }
+          }
+          // columns 2q (hi) and 2q+1 (lo) of this lane belong to slot q
+          colinv0 = colinv1 = __shfl_sync(kFull, inv, (2 * q) * 4);
         }
       }
-    }
-    __syncthreads();
-    if constexpr (MODE == 1) {
-      const int c = s_chunk;
-      if (c >= 0) {
-        __threadfence();
-        const int row0 = 2 * c * kChunkPairRows;
-        const int nrow = min(2 * kChunkPairRows, a.H - row0);
-        for (int it = b; it < nrow * a.C; it += TPR) {
-          const int t = it / nrow, row = row0 + it % nrow;
-          float sum = 0.f;
-          for (int dd = 0; dd < n; dd++)
-            if ((ds.tokmask[dd] >> t) & 1u) sum += __ldcg(a.ypair + (size_t)ds.pair[dd][t] * a.H + row);
-          a.y[(size_t)t * a.H + row] = sum;
+
+      // four independent accumulator chains (k-step s feeds chain s % 4) so
+      // consecutive MMAs of a warp do not wait on each other's results
+      float acc4[4][4] = {};
+      uint4 sc = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int qg = 0; qg < 8; qg++) {
+        const uint4 cw = *reinterpret_cast<const uint4 *>(codes + ((size_t)qg * 32 + lane) * 16);
+        if ((qg & 1) == 0) sc = *reinterpret_cast<const uint4 *>(scales + ((size_t)(qg >> 1) * 8 + g) * 16);
+        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+          const int s = 4 * qg + jj;
+          const int ks = (qg & 1) * 4 + jj;              // k-step inside the 8-step scale unit
+          const uint32_t s2 = e4m3x2_to_f16x2(scs[ks >> 1] >> (16 * (ks & 1)));
+          uint32_t A[4];
+          e2m1x8_to_f16x2(cws[jj], A);
+          A[0] = hmul2_lo(A[0], s2);
+          A[1] = hmul2_hi(A[1], s2);
+          A[2] = hmul2_lo(A[2], s2);
+          A[3] = hmul2_hi(A[3], s2);
+          mma16816(acc4[jj], A, bf[s][0], bf[s][1]);
         }
-        if (b == 0) a.chunk_cnt[c] = 0u;
       }
+      float acc[4];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; c4++) acc[c4] = (acc4[0][c4] + acc4[1][c4]) + (acc4[2][c4] + acc4[3][c4]);
+      res[pass] = make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
     }
-    q += nr;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);       // stage buffer may be refilled
+
+    const int rs = i % kRedSlots;
+    const uint32_t ruse = (uint32_t)(i / kRedSlots);
+    if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
+      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+      break;
+    }
+    for (int pass = 0; pass < npass; pass++) red_at(rs, pass, w, lane) = res[pass];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&red_full[rs]);
   }
 }
 
-template <int MODE, int NT>
-static cudaError_t launch_one(const GemvArgs &a, int threads, int grid, bool pdl, cudaStream_t stream) {
+// ------------------------------------------------------------------ host side
+// Ring geometry.  Each ring slot must belong to one consumer group (S a
+// multiple of G): a slot shared by two groups lets a consumer that runs ahead
+// of the other group wait on a barrier phase two uses ahead, whose parity
+// aliases the current one, and arrive on the other group's phase.
+void gemv_geometry(int mode, int slice_warps, int *groups, int *stages, int *stage_bytes, int *smem_bytes) {
+  const int G = (32 * (kMaxGroups * slice_warps + 2) <= kMaxCtaThreads) ? kMaxGroups : 1;
+  const int tile = slice_warps * kTileSliceBytes;
+  const int red = kRedSlots * (mode == 0 ? 1 : kMaxPasses) * slice_warps * 32 * (int)sizeof(float4);
+  int s = (kGemvSmemBytes - red) / tile;
+  if (s > kMaxStages) s = kMaxStages;
+  s -= s % G;
+  if (s < G) s = G;
+  *groups = G;
+  *stage_bytes = tile;
+  *stages = s;
+  *smem_bytes = s * tile + red;
+}
+
+template <int MODE>
+static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(32 * (a.slice_warps * a.groups + 2));   // + producer + epilogue warps
+  cfg.dynamicSmemBytes = (size_t)a.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE, NT>, a);
+  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE>, a);
 }
 
-cudaError_t launch_expert_gemv(int mode, int nt, const GemvArgs &a, int threads, int grid,
-                               bool pdl, cudaStream_t stream) {
-  if (mode == 0) {
-    switch (nt) {
-      case 1: return launch_one<0, 1>(a, threads, grid, pdl, stream);
-      case 2: return launch_one<0, 2>(a, threads, grid, pdl, stream);
-      case 4: return launch_one<0, 4>(a, threads, grid, pdl, stream);
-      default: return launch_one<0, 8>(a, threads, grid, pdl, stream);
-    }
-  }
-  switch (nt) {
-    case 1: return launch_one<1, 1>(a, threads, grid, pdl, stream);
-    case 2: return launch_one<1, 2>(a, threads, grid, pdl, stream);
-    case 4: return launch_one<1, 4>(a, threads, grid, pdl, stream);
-    default: return launch_one<1, 8>(a, threads, grid, pdl, stream);
-  }
+cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
+  return mode == 0 ? launch_one<0>(a, grid, pdl, stream) : launch_one<1>(a, grid, pdl, stream);
 }
 
-template <int MODE, int NT>
-static int occ_one(int threads) {
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, expert_gemv_kernel<MODE, NT>, threads, 0) != cudaSuccess)
-    return 1;
-  return occ > 0 ? occ : 1;
-}
-
-int gemv_occupancy(int mode, int nt, int threads) {
-  if (mode == 0) {
-    switch (nt) {
-      case 1: return occ_one<0, 1>(threads);
-      case 2: return occ_one<0, 2>(threads);
-      case 4: return occ_one<0, 4>(threads);
-      default: return occ_one<0, 8>(threads);
-    }
-  }
-  switch (nt) {
-    case 1: return occ_one<1, 1>(threads);
-    case 2: return occ_one<1, 2>(threads);
-    case 4: return occ_one<1, 4>(threads);
-    default: return occ_one<1, 8>(threads);
-  }
+cudaError_t gemv_setup() {
+  // the largest dynamic shared memory any geometry requests (the attribute is
+  // per kernel and device, so it must not depend on the layer that sets it)
+  const int smem = kGemvSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(expert_gemv_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(expert_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return err;
 }
 
 }  // namespace moe

@@ -11,8 +11,8 @@ struct PackArgs {
   const float *gate_g, *gate_a, *up_g, *up_a, *down_g, *down_a;
   uint8_t *packed;
   int32_t *status;   // in the packed trailer
-  int E, H, I, tpr_gu, tpr_dn;
-  size_t gu_pair_bytes, dn_pair_bytes, dn_region_off, expert_bytes, scalars_off;
+  int E, H, I, w_gu, w_dn;
+  size_t dn_region_off, expert_bytes, scalars_off;
 };
 cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream);
 
@@ -30,8 +30,8 @@ struct RouteArgs {
 cudaError_t launch_route_fused(const RouteArgs &a, int grid, cudaStream_t stream);
 // Router for larger C: tiled logits kernel, then one warp per token for top-k.
 cudaError_t launch_route_batched(const RouteArgs &a, cudaStream_t stream);
-// Opt-in shared memory for the fused router; call once per device.
-cudaError_t route_setup(int H);
+// Opt-in shared memory for the fused router (once per device; idempotent).
+cudaError_t route_setup();
 
 struct GemvArgs {
   const uint8_t *packed;
@@ -43,18 +43,31 @@ struct GemvArgs {
   float *ypair;              // [C*k][H]
   float *y;                  // [C][H]
   int32_t *flags;
-  uint32_t *chunk_cnt;
   int C, k, E, H, I;
   size_t expert_bytes;
   size_t region_off;         // 0 (gate/up) or the down region offset
-  int pair_bytes;            // bytes of one pair row of this region
-  int rows;                  // pair rows per expert: I (gate/up) or H/2 (down)
+  int tiles;                 // tiles per expert: I/8 (gate/up) or H/16 (down)
+  int tile_bytes;            // slice_warps * kTileSliceBytes
+  int slice_warps;           // W: consumer warps of a group = padded K / 512
+  int groups;                // consumer groups per CTA (alternate tiles)
+  int stages;                // shared-memory ring stages (a multiple of groups)
+  int stage_bytes;           // bytes of one ring stage (one tile)
+  int smem_bytes;            // dynamic shared memory: ring + reduction slots
 };
+// Ring geometry, consumer groups and dynamic shared memory of one kernel.
+void gemv_geometry(int mode, int slice_warps, int *groups, int *stages, int *stage_bytes, int *smem_bytes);
+// Opt-in shared memory of the expert kernels (once per device; idempotent).
+cudaError_t gemv_setup();
 // mode 0: gate/up + SwiGLU -> hbuf; mode 1: down -> ypair -> combine -> y.
-// nt: tokens compiled for (1, 2, 4 or 8) >= C.
-cudaError_t launch_expert_gemv(int mode, int nt, const GemvArgs &a, int threads, int grid,
-                               bool pdl, cudaStream_t stream);
-// CTAs per SM the gemv kernel reaches with `threads` threads.
-int gemv_occupancy(int mode, int nt, int threads);
+cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream);
+
+struct CombineArgs {
+  const int32_t *ids;        // [C][k]
+  const float *ypair;        // [C*k][H]
+  float *y;                  // [C][H]
+  int C, k, E, H;
+};
+// y[t] = sum of ypair over token t's valid slots in ascending expert id order.
+cudaError_t launch_combine(const CombineArgs &a, int num_sms, bool pdl, cudaStream_t stream);
 
 }  // namespace moe

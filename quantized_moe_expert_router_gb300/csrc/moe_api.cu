@@ -32,18 +32,11 @@ struct DeviceGuard {
   }
 };
 
-int nt_index(int nt) { return nt <= 1 ? 0 : nt <= 2 ? 1 : nt <= 4 ? 2 : 3; }
-
-int gemv_grid(const moe_layer &L, int mode, int nt, long long max_rows) {
-  const int occ = L.gemv_occ[mode][nt_index(nt)];
-  long long g = (long long)L.num_sms * occ;
-  // at least two rows per CTA so that the CTA count never exceeds the work
-  const long long cap = (max_rows + 1) / 2;
-  if (g > cap) g = cap;
+int gemv_grid(const moe_layer &L, long long max_tiles) {
+  long long g = L.num_sms;                 // one CTA per SM (the ring uses most of shared memory)
+  if (g > max_tiles) g = max_tiles;
   return (int)(g < 1 ? 1 : g);
 }
-
-int pow2_tokens(int c) { return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8; }
 
 }  // namespace
 
@@ -86,22 +79,21 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   L->num_sms = sms;
   L->Hp = (int)align_up(c.hidden, moe::kKAlign);
   L->Ip = (int)align_up(c.intermediate, moe::kKAlign);
-  L->tpr_gu = L->Hp / 16;
-  L->tpr_dn = L->Ip / 16;
-  L->gu_pair_bytes = (size_t)L->tpr_gu * 18;
-  L->dn_pair_bytes = (size_t)L->tpr_dn * 18;
-  L->dn_region_off = (size_t)c.intermediate * L->gu_pair_bytes;
-  L->expert_bytes = L->dn_region_off + (size_t)(c.hidden / 2) * L->dn_pair_bytes;
+  L->w_gu = L->Hp / moe::kKAlign;
+  L->w_dn = L->Ip / moe::kKAlign;
+  L->gu_tile_bytes = (size_t)L->w_gu * moe::kTileSliceBytes;
+  L->dn_tile_bytes = (size_t)L->w_dn * moe::kTileSliceBytes;
+  L->dn_region_off = (size_t)(c.intermediate / 8) * L->gu_tile_bytes;
+  L->expert_bytes = L->dn_region_off + (size_t)(c.hidden / 16) * L->dn_tile_bytes;
   L->scalars_off = (size_t)c.num_experts * L->expert_bytes;
   L->trailer_off = align_up(L->scalars_off + (size_t)c.num_experts * 6 * sizeof(float), 16);
   L->packed_bytes = L->trailer_off + 16;
-  L->n_chunks = (c.hidden / 2 + moe::kChunkPairRows - 1) / moe::kChunkPairRows;
   L->stage_events_on = 0;
-  for (int j = 0; j < 4; j++) {
-    L->gemv_occ[0][j] = moe::gemv_occupancy(0, 1 << j, L->tpr_gu);
-    L->gemv_occ[1][j] = moe::gemv_occupancy(1, 1 << j, L->tpr_dn);
+  if (moe::gemv_setup() != cudaSuccess) {
+    delete L;
+    return MOE_ERR_CUDA;
   }
-  if (moe::route_setup(c.hidden) != cudaSuccess) {
+  if (moe::route_setup() != cudaSuccess) {
     delete L;
     return MOE_ERR_CUDA;
   }
@@ -151,8 +143,7 @@ moe_status moe_pack_weights(moe_layer_t L, const moe_canonical_weights *cw, void
   a.packed = pk;
   a.status = status;
   a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.I = L->cfg.intermediate;
-  a.tpr_gu = L->tpr_gu; a.tpr_dn = L->tpr_dn;
-  a.gu_pair_bytes = L->gu_pair_bytes; a.dn_pair_bytes = L->dn_pair_bytes;
+  a.w_gu = L->w_gu; a.w_dn = L->w_dn;
   a.dn_region_off = L->dn_region_off; a.expert_bytes = L->expert_bytes;
   a.scalars_off = L->scalars_off;
   err = moe::launch_pack(a, L->num_sms, stream);
@@ -210,7 +201,6 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
   a.hbuf = reinterpret_cast<float *>(w + wl.hbuf);
   a.ypair = reinterpret_cast<float *>(w + wl.ypair);
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
-  a.chunk_cnt = reinterpret_cast<uint32_t *>(w + wl.chunk_cnt);
   a.k = k; a.E = L->cfg.num_experts; a.H = H; a.I = I;
   a.expert_bytes = L->expert_bytes;
 
@@ -218,7 +208,6 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
   for (int t0 = 0; t0 < C && err == cudaSuccess; t0 += moe::kGemvTokens) {
     const int Cg = (C - t0) < moe::kGemvTokens ? (C - t0) : moe::kGemvTokens;
-    const int nt = pow2_tokens(Cg);
     a.C = Cg;
     a.x = x + (size_t)t0 * H;
     a.ids = ids + (size_t)t0 * k;
@@ -227,19 +216,27 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     const long long max_pairs = (long long)Cg * k;
     // gate/up + SwiGLU
     a.region_off = 0;
-    a.pair_bytes = (int)L->gu_pair_bytes;
-    a.rows = I;
-    err = moe::launch_expert_gemv(0, nt, a, L->tpr_gu,
-                                  gemv_grid(*L, 0, nt, max_pairs * I), true, stream);
+    a.tiles = I / 8;
+    a.tile_bytes = (int)L->gu_tile_bytes;
+    a.slice_warps = L->w_gu;
+    moe::gemv_geometry(0, a.slice_warps, &a.groups, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    err = moe::launch_expert_gemv(0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
     if (err != cudaSuccess) break;
     // down + combine
     a.region_off = L->dn_region_off;
-    a.pair_bytes = (int)L->dn_pair_bytes;
-    a.rows = H / 2;
-    err = moe::launch_expert_gemv(1, nt, a, L->tpr_dn,
-                                  gemv_grid(*L, 1, nt, max_pairs * (H / 2)), true, stream);
+    a.tiles = H / 16;
+    a.tile_bytes = (int)L->dn_tile_bytes;
+    a.slice_warps = L->w_dn;
+    moe::gemv_geometry(1, a.slice_warps, &a.groups, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    err = moe::launch_expert_gemv(1, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
+    if (err != cudaSuccess) break;
+    // weighted sum over each token's experts, ascending expert id
+    moe::CombineArgs cb;
+    cb.ids = a.ids; cb.ypair = a.ypair; cb.y = a.y;
+    cb.C = Cg; cb.k = k; cb.E = a.E; cb.H = H;
+    err = moe::launch_combine(cb, L->num_sms, true, stream);
   }
   if (err == cudaSuccess && L->stage_events_on) err = cudaEventRecord(L->stage_events[2], stream);
   return cuda_status(err);

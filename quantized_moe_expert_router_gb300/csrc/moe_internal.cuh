@@ -20,8 +20,9 @@ constexpr int kMaxTopK = 32;             // one top-k slot per lane
 constexpr int kGemvTokens = 8;           // tokens per GEMV group (token mask bits)
 constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
-constexpr int kChunkPairRows = 32;       // down/combine row chunk: 64 output rows
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
+constexpr int kGemvSmemBytes = 212992;   // dynamic shared memory of one expert-GEMV CTA (+ ~19 KB static)
+constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
 
 // Workspace control block (first 256 bytes of the workspace).
 struct WsControl {
@@ -34,7 +35,6 @@ static_assert(sizeof(WsControl) == 256, "control block is 256 bytes");
 // Byte offsets of the workspace regions for a group of up to kGemvTokens
 // tokens (GEMV path) and C tokens of router logits.
 struct WsLayout {
-  size_t chunk_cnt;   // uint32 [n_chunks]
   size_t logits;      // float  [C][E]
   size_t hbuf;        // float  [kGemvTokens * k][I]  w * silu(g) * u per (token, slot)
   size_t ypair;       // float  [kGemvTokens * k][H]  D_e h per (token, slot)
@@ -50,16 +50,14 @@ struct moe_layer {
   int device;
   int num_sms;
   int Hp, Ip;                 // K of gate/up and of down, padded to kKAlign
-  int tpr_gu, tpr_dn;         // threads of one pair row = Kp / 16
-  size_t gu_pair_bytes;       // tpr_gu * 18
-  size_t dn_pair_bytes;       // tpr_dn * 18
-  size_t dn_region_off;       // offset of the down pair rows inside an expert
+  int w_gu, w_dn;             // 512-element K-slices (= consumer warps of a group)
+  size_t gu_tile_bytes;       // w_gu * kTileSliceBytes: 8 gate/up pair rows
+  size_t dn_tile_bytes;       // w_dn * kTileSliceBytes: 8 down pair rows
+  size_t dn_region_off;       // offset of the down tiles inside an expert
   size_t expert_bytes;        // packed bytes of one expert (without scalars)
   size_t scalars_off;         // float [E][6] : g_gate a_gate g_up a_up g_down a_down
   size_t trailer_off;         // 16-byte status trailer written by the packer
   size_t packed_bytes;
-  int n_chunks;               // ceil((H/2) / kChunkPairRows)
-  int gemv_occ[2][4];         // CTAs per SM of the gemv kernels [mode][log2 NT]
   cudaEvent_t stage_events[3];
   int stage_events_on;
 };
@@ -71,8 +69,6 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline WsLayout ws_layout(const moe_layer &L, int C) {
   WsLayout w;
   size_t off = sizeof(WsControl);
-  w.chunk_cnt = off;
-  off = align_up(off + sizeof(uint32_t) * (size_t)L.n_chunks, 256);
   w.logits = off;
   off = align_up(off + sizeof(float) * (size_t)C * L.cfg.num_experts, 256);
   const size_t pairs = (size_t)kGemvTokens * L.cfg.top_k;

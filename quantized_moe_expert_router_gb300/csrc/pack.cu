@@ -1,21 +1,28 @@
-// pack.cu -- canonical NVFP4 expert weights -> the packed layout the expert
-// kernels stream (byte moves only; no value changes).
+// pack.cu -- canonical NVFP4 expert weights -> the packed "tile" layout the
+// expert kernels stream (byte moves only; no value changes).
 //
-// Packed expert e (at e * expert_bytes):
-//   gate/up pair rows r = 0 .. I-1, each gu_pair_bytes = tpr_gu * 18 bytes:
-//     codes : for block b < tpr_gu, 16 bytes = gate row r block b (8 bytes)
-//             followed by up row r block b (8 bytes)
-//     scales: for block b, 2 bytes = gate scale (r, b), up scale (r, b)
-//   down pair rows p = 0 .. H/2-1 (at dn_region_off), each dn_pair_bytes:
-//     codes : block b: down row 2p block b (8 bytes), down row 2p+1 block b
-//     scales: block b: scale (2p, b), scale (2p+1, b)
-//   Blocks past the real K (padding to a multiple of 512 elements) are zero.
-// After all experts: float [E][6] = g_gate a_gate g_up a_up g_down a_down,
-// then a 16-byte trailer whose first int32 is set when a NaN scale is seen.
+// A pair row is two matrix rows that share K: gate row r with up row r
+// (region 0, I pair rows per expert), or down rows 2p and 2p+1 (region 1, H/2
+// pair rows).  A tile is 8 consecutive pair rows over the whole K, padded
+// with zero codes and zero scales to Kp (a multiple of 512), split into
+// W = Kp/512 slices of 32 k-steps of 16 elements.  Inside a tile:
 //
-// One thread moves one 16-byte code word and its two scale bytes, so
-// consecutive threads read consecutive 8-byte canonical chunks and write
-// consecutive 16-byte packed words.
+//   codes  [W][8 groups of 4 k-steps][32 lanes][16 bytes]   (W * 4096 bytes)
+//   scales [W][4 groups of 8 k-steps][8 rows g][16 bytes]   (W * 512 bytes)
+//
+// Lane l = 4g + q (g = l / 4 is the pair row in the tile, q = l % 4) holds for
+// k-step s one 32-bit word of four code bytes: rowA byte 8s+q, rowB byte
+// 8s+q, rowA byte 8s+q+4, rowB byte 8s+q+4, which are the elements
+// (16s+2q, 16s+2q+1) and (16s+2q+8, 16s+2q+9) of the two rows.  That is the
+// register fragment of operand A of mma.m16n8k16 (row g = rowA, row g+8 =
+// rowB), so a warp loads a 16x16 weight block per k-step with one 4-byte
+// share of a 16-byte shared-memory load.  The scale unit of row g holds, for
+// 8 k-steps, the two e4m3 bytes (rowA scale, rowB scale) of each k-step.
+//
+// Packed expert e (at e * expert_bytes): I/8 gate/up tiles, then H/16 down
+// tiles.  After all experts: float [E][6] = g_gate a_gate g_up a_up g_down
+// a_down, then a 16-byte trailer whose first int32 is set when a NaN scale
+// byte is seen.  The packed size equals the canonical size plus the trailer.
 #include "moe_internal.cuh"
 #include "kernels.h"
 
@@ -23,61 +30,95 @@ namespace moe {
 
 __device__ __forceinline__ bool e4m3_is_nan(uint32_t b) { return (b & 0x7F) == 0x7F; }
 
+// One thread per (expert, region, tile, slice w, pair row g): reads the two
+// rows' 256 code bytes and 32 scale bytes of the slice, writes 8 code units
+// for each of the 4 lanes of row g and 4 scale units.
 __global__ void pack_kernel(const PackArgs a) {
-  const int64_t gu_items = (int64_t)a.E * a.I * a.tpr_gu;
-  const int64_t dn_items = (int64_t)a.E * (a.H / 2) * a.tpr_dn;
+  const int64_t gu_items = (int64_t)a.E * (a.I / 8) * a.w_gu * 8;
+  const int64_t dn_items = (int64_t)a.E * (a.H / 16) * a.w_dn * 8;
   const int64_t total = gu_items + dn_items + a.E;
-  const int gu_blocks = a.H / 16, dn_blocks = a.I / 16;
   int nan_seen = 0;
   for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < total;
        it += (int64_t)gridDim.x * blockDim.x) {
-    if (it < gu_items) {
-      const int b = (int)(it % a.tpr_gu);
-      const int64_t er = it / a.tpr_gu;              // e * I + r
-      const int64_t e = er / a.I, r = er % a.I;
-      uint8_t *dst = a.packed + e * a.expert_bytes + r * a.gu_pair_bytes;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      uint32_t s = 0;
-      if (b < gu_blocks) {
-        const uint2 g = *reinterpret_cast<const uint2 *>(a.gate_codes + er * (a.H / 2) + b * 8);
-        const uint2 u = *reinterpret_cast<const uint2 *>(a.up_codes + er * (a.H / 2) + b * 8);
-        const uint32_t gs = a.gate_scales[er * gu_blocks + b];
-        const uint32_t us = a.up_scales[er * gu_blocks + b];
-        nan_seen |= e4m3_is_nan(gs) | e4m3_is_nan(us);
-        w = make_uint4(g.x, g.y, u.x, u.y);
-        s = gs | (us << 8);
-      }
-      *reinterpret_cast<uint4 *>(dst + b * 16) = w;
-      *reinterpret_cast<uint16_t *>(dst + (size_t)a.tpr_gu * 16 + b * 2) = (uint16_t)s;
-    } else if (it < gu_items + dn_items) {
-      const int64_t j = it - gu_items;
-      const int b = (int)(j % a.tpr_dn);
-      const int64_t ep = j / a.tpr_dn;               // e * (H/2) + p
-      const int64_t e = ep / (a.H / 2), p = ep % (a.H / 2);
-      uint8_t *dst = a.packed + e * a.expert_bytes + a.dn_region_off + p * a.dn_pair_bytes;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      uint32_t s = 0;
-      if (b < dn_blocks) {
-        const int64_t row0 = e * a.H + 2 * p;        // global row index of down row 2p
-        const uint2 c0 = *reinterpret_cast<const uint2 *>(a.down_codes + row0 * (a.I / 2) + b * 8);
-        const uint2 c1 = *reinterpret_cast<const uint2 *>(a.down_codes + (row0 + 1) * (a.I / 2) + b * 8);
-        const uint32_t s0 = a.down_scales[row0 * dn_blocks + b];
-        const uint32_t s1 = a.down_scales[(row0 + 1) * dn_blocks + b];
-        nan_seen |= e4m3_is_nan(s0) | e4m3_is_nan(s1);
-        w = make_uint4(c0.x, c0.y, c1.x, c1.y);
-        s = s0 | (s1 << 8);
-      }
-      *reinterpret_cast<uint4 *>(dst + b * 16) = w;
-      *reinterpret_cast<uint16_t *>(dst + (size_t)a.tpr_dn * 16 + b * 2) = (uint16_t)s;
-    } else {
+    if (it >= gu_items + dn_items) {
       const int64_t e = it - gu_items - dn_items;
       float *dst = reinterpret_cast<float *>(a.packed + a.scalars_off) + e * 6;
-      dst[0] = a.gate_g[e];
-      dst[1] = a.gate_a[e];
-      dst[2] = a.up_g[e];
-      dst[3] = a.up_a[e];
-      dst[4] = a.down_g[e];
-      dst[5] = a.down_a[e];
+      dst[0] = a.gate_g[e]; dst[1] = a.gate_a[e];
+      dst[2] = a.up_g[e];   dst[3] = a.up_a[e];
+      dst[4] = a.down_g[e]; dst[5] = a.down_a[e];
+      continue;
+    }
+    const bool gu = it < gu_items;
+    const int64_t j = gu ? it : it - gu_items;
+    const int W = gu ? a.w_gu : a.w_dn;
+    const int g = (int)(j % 8);
+    const int w = (int)((j / 8) % W);
+    const int64_t et = j / (8 * (int64_t)W);             // e * tiles + tile
+    const int64_t tiles = gu ? a.I / 8 : a.H / 16;
+    const int64_t e = et / tiles, tile = et % tiles;
+    const int K = gu ? a.H : a.I;                        // real K of the rows
+    const int64_t p = tile * 8 + g;                      // pair row
+    const uint8_t *ca, *cb, *sa, *sb;
+    if (gu) {
+      const int64_t row = e * a.I + p;
+      ca = a.gate_codes + row * (K / 2); cb = a.up_codes + row * (K / 2);
+      sa = a.gate_scales + row * (K / 16); sb = a.up_scales + row * (K / 16);
+    } else {
+      const int64_t row = e * a.H + 2 * p;
+      ca = a.down_codes + row * (K / 2); cb = ca + K / 2;
+      sa = a.down_scales + row * (K / 16); sb = sa + K / 16;
+    }
+    uint8_t *tb = a.packed + e * a.expert_bytes + (gu ? 0 : a.dn_region_off) +
+                  tile * (size_t)W * kTileSliceBytes;
+    // code bytes of this slice (k-steps 32w .. 32w+31), zero past K
+    const int kstep0 = 32 * w, ksteps = K / 16;
+#pragma unroll 1
+    for (int qg = 0; qg < 8; qg++) {                     // groups of 4 k-steps
+      uint32_t words[4][4];                              // [lane q][k-step j]
+#pragma unroll
+      for (int jj = 0; jj < 4; jj++) {
+        const int s = kstep0 + 4 * qg + jj;
+        uint2 A = make_uint2(0, 0), B = make_uint2(0, 0);
+        if (s < ksteps) {
+          A = *reinterpret_cast<const uint2 *>(ca + 8 * s);
+          B = *reinterpret_cast<const uint2 *>(cb + 8 * s);
+        }
+        const uint8_t *ab = reinterpret_cast<const uint8_t *>(&A);
+        const uint8_t *bb = reinterpret_cast<const uint8_t *>(&B);
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+          words[q][jj] = (uint32_t)ab[q] | ((uint32_t)bb[q] << 8) | ((uint32_t)ab[q + 4] << 16) |
+                         ((uint32_t)bb[q + 4] << 24);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const int lane = 4 * g + q;
+        *reinterpret_cast<uint4 *>(tb + (size_t)w * 4096 + ((size_t)qg * 32 + lane) * 16) =
+            make_uint4(words[q][0], words[q][1], words[q][2], words[q][3]);
+      }
+    }
+    uint8_t *sbase = tb + (size_t)W * 4096;
+#pragma unroll 1
+    for (int q8 = 0; q8 < 4; q8++) {
+      uint32_t sw[4];
+#pragma unroll
+      for (int h = 0; h < 4; h++) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i2 = 0; i2 < 2; i2++) {
+          const int s = kstep0 + 8 * q8 + 2 * h + i2;
+          uint32_t xa = 0, xb = 0;
+          if (s < ksteps) {
+            xa = sa[s];
+            xb = sb[s];
+            nan_seen |= e4m3_is_nan(xa) | e4m3_is_nan(xb);
+          }
+          v |= (xa | (xb << 8)) << (16 * i2);
+        }
+        sw[h] = v;
+      }
+      *reinterpret_cast<uint4 *>(sbase + (size_t)w * 512 + ((size_t)q8 * 8 + g) * 16) =
+          make_uint4(sw[0], sw[1], sw[2], sw[3]);
     }
   }
   if (nan_seen) atomicOr(a.status, 1);

@@ -197,15 +197,17 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const RouteArgs a) {
 
 static size_t fused_smem(int ct, int H) { return sizeof(float) * (size_t)ct * H; }
 
-cudaError_t route_setup(int H) {
-  cudaError_t err = cudaSuccess;
-  err = cudaFuncSetAttribute(route_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(1, H));
+// Opt-in shared memory for the largest hidden size the library accepts, so
+// the attribute does not depend on which layer set it.
+cudaError_t route_setup() {
+  constexpr int kMaxHidden = 4096;
+  cudaError_t err = cudaFuncSetAttribute(route_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(1, kMaxHidden));
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(route_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(2, H));
+    err = cudaFuncSetAttribute(route_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(2, kMaxHidden));
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(route_fused_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(4, H));
+    err = cudaFuncSetAttribute(route_fused_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(4, kMaxHidden));
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(route_fused_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(8, H));
+    err = cudaFuncSetAttribute(route_fused_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(8, kMaxHidden));
   return err;
 }
 

@@ -107,30 +107,41 @@ def test_device_generator_matches_host_k3_expert():
 
 # ------------------------------------------------------------------ packer
 
+def _unpack_tiles(buf, ntiles, W, K):
+    """Tiles of 8 pair rows -> (rowA codes, rowB codes, rowA scales, rowB scales),
+    each indexed [pair row][...] (the inverse of the packer's byte moves)."""
+    tb = W * 4608
+    t = buf[: ntiles * tb].reshape(ntiles, tb)
+    codes = t[:, : W * 4096].reshape(ntiles, W, 8, 8, 4, 4, 4)     # tile w qg g q j byte
+    codes = codes.transpose(0, 3, 1, 2, 5, 4, 6)                   # tile g w qg j q byte
+    S = W * 32
+    A = np.empty((ntiles, 8, S, 8), np.uint8)
+    B = np.empty((ntiles, 8, S, 8), np.uint8)
+    c = codes.reshape(ntiles, 8, S, 4, 4)                          # tile g S q byte
+    A[..., :4], A[..., 4:] = c[..., 0], c[..., 2]
+    B[..., :4], B[..., 4:] = c[..., 1], c[..., 3]
+    sc = t[:, W * 4096:].reshape(ntiles, W, 4, 8, 8, 2)            # tile w q8 g i ab
+    sc = sc.transpose(0, 3, 1, 2, 4, 5).reshape(ntiles, 8, S, 2)   # tile g S ab
+    rows = ntiles * 8
+    return (A.reshape(rows, S * 8)[:, : K // 2], B.reshape(rows, S * 8)[:, : K // 2],
+            sc[..., 0].reshape(rows, S)[:, : K // 16], sc[..., 1].reshape(rows, S)[:, : K // 16])
+
+
 def unpack_host(packed, E, H, I):
-    """Reverse the packed layout on the host (byte moves only)."""
-    Hp, Ip = -(-H // 512) * 512, -(-I // 512) * 512
-    tg, td = Hp // 16, Ip // 16
-    gpb, dpb = tg * 18, td * 18
-    ebytes = I * gpb + (H // 2) * dpb
+    """Reverse the packed tile layout on the host (byte moves only)."""
+    Wg, Wd = -(-H // 512), -(-I // 512)
+    gu_bytes = (I // 8) * Wg * 4608
+    ebytes = gu_bytes + (H // 16) * Wd * 4608
     out = {n: {"codes": np.zeros((E, r, K // 2), np.uint8), "scales": np.zeros((E, r, K // 16), np.uint8)}
            for n, r, K in (("gate", I, H), ("up", I, H), ("down", H, I))}
     for e in range(E):
         base = e * ebytes
-        gu = packed[base: base + I * gpb].reshape(I, gpb)
-        codes = gu[:, :tg * 16].reshape(I, tg, 16)[:, :H // 16]
-        sc = gu[:, tg * 16:].reshape(I, tg, 2)[:, :H // 16]
-        out["gate"]["codes"][e] = codes[:, :, :8].reshape(I, H // 2)
-        out["up"]["codes"][e] = codes[:, :, 8:].reshape(I, H // 2)
-        out["gate"]["scales"][e] = sc[:, :, 0]
-        out["up"]["scales"][e] = sc[:, :, 1]
-        dn = packed[base + I * gpb: base + ebytes].reshape(H // 2, dpb)
-        codes = dn[:, :td * 16].reshape(H // 2, td, 16)[:, :I // 16]
-        sc = dn[:, td * 16:].reshape(H // 2, td, 2)[:, :I // 16]
-        out["down"]["codes"][e][0::2] = codes[:, :, :8].reshape(H // 2, I // 2)
-        out["down"]["codes"][e][1::2] = codes[:, :, 8:].reshape(H // 2, I // 2)
-        out["down"]["scales"][e][0::2] = sc[:, :, 0]
-        out["down"]["scales"][e][1::2] = sc[:, :, 1]
+        ga, ub, gs, us = _unpack_tiles(packed[base: base + gu_bytes], I // 8, Wg, H)
+        out["gate"]["codes"][e], out["up"]["codes"][e] = ga, ub
+        out["gate"]["scales"][e], out["up"]["scales"][e] = gs, us
+        da, db, das, dbs = _unpack_tiles(packed[base + gu_bytes: base + ebytes], H // 16, Wd, I)
+        out["down"]["codes"][e][0::2], out["down"]["codes"][e][1::2] = da, db
+        out["down"]["scales"][e][0::2], out["down"]["scales"][e][1::2] = das, dbs
     scal = packed[E * ebytes: E * ebytes + E * 24].view(np.float32).reshape(E, 6)
     return out, scal
 
