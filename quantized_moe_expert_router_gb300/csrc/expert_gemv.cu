@@ -152,7 +152,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
-__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+// silu(v) = v / (1 + e^-v), with the SFU exponential and reciprocal (relative
+// error ~2^-21, far below the output tolerance).
+__device__ __forceinline__ float silu(float g) { return g * __frcp_rn(1.f + __expf(-g)); }
 
 // Power of two 2^s with amax * 2^s in [2^14, 2^15) (s clamped to +-120);
 // returns 2^s and writes 2^-s.
@@ -239,10 +241,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   const int W = a.slice_warps, G = a.groups, S = a.stages;
   // reduction slots [kRedSlots][passes][W][32 lanes] of float4, after the ring
   float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);
-  const int npass_max = MODE == 0 ? 1 : kMaxPasses;
-  auto red_at = [&](int rs, int pass, int ww, int l) -> float4 & {
-    return red[(((size_t)rs * npass_max + pass) * W + ww) * 32 + l];
-  };
+  const int red_slot_f4 = (MODE == 0 ? 1 : kMaxPasses) * W * 32;   // float4 per reduction slot
   const int ncons_warps = W * G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_producer = warp == ncons_warps;
@@ -316,7 +315,9 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       const uint64_t pol = l2_evict_first_policy();
       int i = 0;
       bool ok = true;
-      for (; i < nstage; i++) {
+      int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
+      for (; i < nstage; i++, tile++) {
+        if (tile == a.tiles) { tile = 0; d++; }
         const int slot = i % S;
         const uint32_t use = (uint32_t)(i / S);
         if (use > 0 && !mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1u)) {
@@ -324,8 +325,6 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
           ok = false;
           break;
         }
-        const long long u = t0 + i;
-        const int d = (int)(u / a.tiles), tile = (int)(u % a.tiles);
         const uint8_t *src = a.packed + (size_t)ds.expert[d] * a.expert_bytes + a.region_off +
                              (size_t)tile * a.tile_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)a.tile_bytes);
@@ -343,47 +342,51 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   if (is_epilogue) {
     // ------------------------------------------------ epilogue warp
     if constexpr (MODE == 1) pdl_wait();
+    // (expert rank, tile) of stage i, advanced incrementally (no 64-bit division)
+    int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
     for (int i = 0; i < nstage; i++) {
       const int rs = i % kRedSlots;
       if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(i / kRedSlots) & 1u)) {
         atomicOr(a.flags, MOE_FLAG_TIMEOUT);
         break;
       }
-      const long long u = t0 + i;
-      const int d = (int)(u / a.tiles), tile = (int)(u % a.tiles);
+      const float4 *slot_red = red + (size_t)rs * red_slot_f4 + lane;
       const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
       for (int pass = 0; pass < npass; pass++) {
-        float4 sum = red_at(rs, pass, 0, lane);
-        for (int ww = 1; ww < W; ww++) {
-          const float4 v = red_at(rs, pass, ww, lane);
-          sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        const float4 *pr4 = slot_red + (size_t)pass * W * 32;
+        float4 sum = pr4[0];
+#pragma unroll
+        for (int ww = 1; ww < kMaxSliceWarps; ww++) {
+          if (ww < W) {
+            const float4 v = pr4[ww * 32];
+            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+          }
         }
         if constexpr (MODE == 0) {
-          const int r = tile * 8 + g;
           const uint32_t mask = ds.tokmask[d];
+          float *hrow = a.hbuf + tile * 8 + g;
 #pragma unroll
           for (int c2 = 0; c2 < 2; c2++) {
             const int t = 2 * q + c2;
-            if (t < a.C && ((mask >> t) & 1u)) {
+            if ((mask >> t) & 1u) {
               const int p = ds.pair[d][t];
               const float gg = (c2 ? sum.y : sum.x) * ds.scal[d][0];
               const float uu = (c2 ? sum.w : sum.z) * ds.scal[d][1];
-              a.hbuf[(size_t)p * a.I + r] = ds.wt[p] * silu(gg) * uu;
+              hrow[(size_t)p * a.I] = ds.wt[p] * silu(gg) * uu;
             }
           }
         } else {
           const int sl = 4 * pass + q;
           if (sl < ds.nslot[d]) {
-            const int p = ds.slot_pair[d][sl];
-            const int pr = tile * 8 + g;
             const float gd = ds.scal[d][2];
-            *reinterpret_cast<float2 *>(a.ypair + (size_t)p * a.H + 2 * pr) =
+            *reinterpret_cast<float2 *>(a.ypair + (size_t)ds.slot_pair[d][sl] * a.H + 2 * (tile * 8 + g)) =
                 make_float2((sum.x + sum.y) * gd, (sum.z + sum.w) * gd);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rs]);
+      if (++tile == a.tiles) { tile = 0; d++; }
     }
     return;
   }
@@ -391,10 +394,10 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   // ---------------------------------------------------- consumers
   if constexpr (MODE == 1) pdl_wait();           // hbuf comes from the gate/up kernel
   int cur_key = -1;                              // (expert rank, slot group) of bf
-  for (int i = grp; i < nstage; i += G) {
+  int d = (int)((t0 + grp) / a.tiles), tile = (int)((t0 + grp) - (long long)d * a.tiles);
+  for (int i = grp; i < nstage; i += G, tile += G) {
+    while (tile >= a.tiles) { tile -= a.tiles; d++; }
     const int slot = i % S;
-    const long long u = t0 + i;
-    const int d = (int)(u / a.tiles);
     const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
 
     if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
@@ -403,7 +406,13 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
     }
     const uint8_t *codes = ring + (size_t)slot * a.stage_bytes + (size_t)w * 4096;
     const uint8_t *scales = ring + (size_t)slot * a.stage_bytes + (size_t)W * 4096 + (size_t)w * 512;
-    float4 res[kMaxPasses];
+    const int rs = i % kRedSlots;
+    const uint32_t ruse = (uint32_t)(i / kRedSlots);
+    if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
+      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+      break;
+    }
+    float4 *my_red = red + (size_t)rs * red_slot_f4 + (size_t)w * 32 + lane;
 
     for (int pass = 0; pass < npass; pass++) {
       if constexpr (MODE == 1) {
@@ -481,20 +490,14 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       float acc[4];
 #pragma unroll
       for (int c4 = 0; c4 < 4; c4++) acc[c4] = (acc4[0][c4] + acc4[1][c4]) + (acc4[2][c4] + acc4[3][c4]);
-      res[pass] = make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
+      my_red[(size_t)pass * W * 32] =
+          make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[slot]);       // stage buffer may be refilled
-
-    const int rs = i % kRedSlots;
-    const uint32_t ruse = (uint32_t)(i / kRedSlots);
-    if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
-      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-      break;
+    if (lane == 0) {
+      mbar_arrive(&empty_bar[slot]);                   // stage buffer may be refilled
+      mbar_arrive(&red_full[rs]);                      // slice partials are in the reduction slot
     }
-    for (int pass = 0; pass < npass; pass++) red_at(rs, pass, w, lane) = res[pass];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&red_full[rs]);
   }
 }
 
