@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   }
   __syncthreads();
   pdl_wait();                                   // ypair comes from the down kernel
+  if (blockIdx.x == 0)                          // the down kernel has read every |h| maximum
+    for (int i = tid; i < a.C * a.k; i += blockDim.x) a.hamax[i] = 0u;
   const int H4 = a.H / 4;
   for (int it = blockIdx.x * blockDim.x + tid; it < a.C * H4; it += gridDim.x * blockDim.x) {
     const int t = it / H4, c4 = it - t * H4;

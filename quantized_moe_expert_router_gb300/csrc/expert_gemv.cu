@@ -21,28 +21,32 @@
 // Streaming.  The CTA is warp-specialised and its warps never meet at a
 // CTA-wide barrier after the dispatch: one producer lane copies each tile with
 // one bulk copy (cp.async.bulk, global -> shared, completion counted on an
-// mbarrier) into a ring of S stage buffers, up to S tiles ahead; G consumer
-// groups of W warps take alternate tiles (warp w of a group owns K-slice w,
-// 32 k-steps of 16 elements) and hand their slice partials to one epilogue
-// warp through a ring of reduction slots, also tracked by mbarriers.  Every
-// wait is bounded (about two seconds of %globaltimer): on expiry the waiting
-// warp sets MOE_FLAG_TIMEOUT and leaves, and the producer waits (bounded) for
-// its copies still in flight before exiting.
+// mbarrier) into a ring of S stage buffers, up to S tiles ahead.  The W
+// consumer warps all work on the same tile, each on its own 256-element
+// K range (16 k-steps: half of one of the tile's 512-element slices), and hand
+// their partials to one epilogue warp through a ring of reduction slots, also
+// tracked by mbarriers (one item per tile and token pass).  Every wait is
+// bounded (about two seconds of %globaltimer): on expiry the waiting warp sets
+// MOE_FLAG_TIMEOUT and leaves, and the producer waits (bounded) for its copies
+// still in flight before exiting.
 //
 // Compute.  Decoding stays in registers: per k-step a lane converts its 4
 // code bytes with cvt.rn.f16x2.e2m1x2 and multiplies them by the row's e4m3
 // block scale in f16 (exact: at most 2+4 significant bits, |value| <= 2688,
 // no subnormals).  The 16x16 block of decoded weights is the A fragment of
 // mma.m16n8k16 (rows g and g+8 = the two rows of pair row g of the tile), and
-// the MMA accumulates in fp32 across the warp's K-slice; the eight MMA columns
+// the MMA accumulates in fp32 across the warp's K range; the eight MMA columns
 // carry the decode batch:
 //   gate/up: column n = token n of the group (x in f16, scaled by a power of
-//            two per token and K-slice: exact for bf16 input);
+//            two per token and warp K range: exact for bf16 input);
 //   down:    columns 2j, 2j+1 = the hi and lo f16 parts of h for the j-th
-//            token that chose the expert (scaled by a power of two per token
-//            and K-slice), so hi + lo carries h to 2^-22.
-// The slice partials (each rescaled by 2^-s) are summed over the W warps by
-// the epilogue warp, which applies the tensor scale and writes hbuf / ypair.
+//            token that chose the expert (scaled by a power of two set by
+//            that token slot's max |h|), so hi + lo carries h to 2^-22 of
+//            its largest element.
+// The partials (each rescaled by 2^-s) are summed over the W warps in a fixed
+// order by the epilogue warp, which applies the tensor scale and writes hbuf
+// (plus the running max |h| per token slot, which sets the down kernel's
+// power-of-two scale) or ypair.
 //
 // The weighted sum over a token's experts is the separate combine kernel
 // (combine.cu), which reads ypair in ascending expert order: no float atomics,
@@ -53,12 +57,11 @@
 namespace moe {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kSliceSteps = 32;                  // k-steps per warp K-slice
-constexpr int kMaxSliceWarps = 8;                // K <= 4096
-constexpr int kMaxGroups = 2;
-constexpr int kMaxCtaThreads = 512;              // 16 warps of 128 registers fill the register file
+constexpr int kSliceSteps = 32;                  // k-steps of one 512-element K-slice of a tile
+constexpr int kWarpSteps = 16;                   // k-steps per consumer warp (half a slice)
+constexpr int kMaxKWarps = 16;                   // consumer warps: K <= 4096
+constexpr int kMaxCtaThreads = 32 * (kMaxKWarps + 2);   // + producer and epilogue warps
 constexpr int kRedSlots = 4;                     // consumer -> epilogue reduction ring
-constexpr int kMaxPasses = 2;                    // down kernel: 4 token slots per pass, C <= 8
 constexpr int kMaxStages = 8;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -122,9 +125,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
-__device__ __forceinline__ void group_sync(int group, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(nthreads) : "memory");
-}
 
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -164,6 +164,14 @@ __device__ __forceinline__ float f16_range_scale(float amax, float *inv) {
   s = max(-120, min(120, s));
   *inv = __uint_as_float((uint32_t)(127 - s) << 23);
   return __uint_as_float((uint32_t)(127 + s) << 23);
+}
+
+// Position of element k of an h vector in hbuf: each 16-element block is
+// stored in the order the down kernel's B operand reads it, so that lane
+// (g, q) finds elements 2q, 2q+1, 2q+8, 2q+9 of a k-step as one float4.
+__device__ __forceinline__ int operand_order(int k) {
+  const int r = k & 15;
+  return (k & ~15) + 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
 }
 
 // ---------------------------------------------------------------- dispatch
@@ -238,20 +246,20 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   __shared__ __align__(8) uint64_t red_full[kRedSlots];
   __shared__ __align__(8) uint64_t red_empty[kRedSlots];
 
-  const int W = a.slice_warps, G = a.groups, S = a.stages;
-  // reduction slots [kRedSlots][passes][W][32 lanes] of float4, after the ring
+  const int NS = a.slices, W = 2 * NS, S = a.stages;
+  // reduction slots [kRedSlots][W][32 lanes] of float4, after the ring
   float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);
-  const int red_slot_f4 = (MODE == 0 ? 1 : kMaxPasses) * W * 32;   // float4 per reduction slot
-  const int ncons_warps = W * G;
+  const int red_slot_f4 = W * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool is_producer = warp == ncons_warps;
-  const bool is_epilogue = warp == ncons_warps + 1;
-  const bool is_consumer = warp < ncons_warps;
-  const int grp = warp / W, w = warp % W;
+  const bool is_producer = warp == W;
+  const bool is_epilogue = warp == W + 1;
+  const bool is_consumer = warp < W;
+  const int slice = warp >> 1, half = warp & 1;  // consumer: k-steps 32*slice + 16*half + [0, 16)
+  const int ks0 = kSliceSteps * slice + kWarpSteps * half;
   const int g = lane >> 2, q = lane & 3;
   const int K = MODE == 0 ? a.H : a.I;          // real K of this region's rows
 
-  if (tid == 32 * ncons_warps) {
+  if (tid == 32 * W) {
     for (int s = 0; s < S; s++) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], W);
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   }
 
   // ---------------- B fragments of x (gate/up), independent of the router
-  uint32_t bf[kSliceSteps][2];
+  uint32_t bf[kWarpSteps][2];
   float colinv0 = 1.f, colinv1 = 1.f;           // 2^-s of accumulator columns 2q, 2q+1
   if constexpr (MODE == 0) {
     if (is_consumer) {
@@ -272,8 +280,8 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       const bool tok = g < a.C;
       const uint16_t *xr = a.x + (size_t)(tok ? g : 0) * a.H;
 #pragma unroll
-      for (int s = 0; s < kSliceSteps; s++) {
-        const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
+      for (int s = 0; s < kWarpSteps; s++) {
+        const int k0 = 16 * (ks0 + s) + 2 * q;
         uint32_t v0 = 0, v1 = 0;
         if (tok && k0 < K) {
           v0 = *reinterpret_cast<const uint32_t *>(xr + k0);
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       float inv;
       const float up = f16_range_scale(am, &inv);
 #pragma unroll
-      for (int s = 0; s < kSliceSteps; s++)
+      for (int s = 0; s < kWarpSteps; s++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
           const uint32_t v = bf[s][h];
@@ -339,24 +347,51 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
     return;
   }
 
+  // Items of the reduction ring: one per (stage, pass), in stage order; the
+  // down kernel makes one pass per 4 token slots of the tile's expert.
   if (is_epilogue) {
     // ------------------------------------------------ epilogue warp
     if constexpr (MODE == 1) pdl_wait();
     // (expert rank, tile) of stage i, advanced incrementally (no 64-bit division)
     int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
-    for (int i = 0; i < nstage; i++) {
-      const int rs = i % kRedSlots;
-      if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(i / kRedSlots) & 1u)) {
-        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-        break;
+    // gate/up: running max |h| of tokens 2q, 2q+1 for expert rank d, merged
+    // into hamax when d changes and at the end
+    float hm0 = 0.f, hm1 = 0.f;
+    auto flush_hmax = [&](int dd) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        hm0 = fmaxf(hm0, __shfl_xor_sync(kFull, hm0, o));
+        hm1 = fmaxf(hm1, __shfl_xor_sync(kFull, hm1, o));
       }
-      const float4 *slot_red = red + (size_t)rs * red_slot_f4 + lane;
+      if (g == 0) {
+        const uint32_t mask = ds.tokmask[dd];
+        if ((mask >> (2 * q)) & 1u) atomicMax(a.hamax + ds.pair[dd][2 * q], __float_as_uint(hm0));
+        if ((mask >> (2 * q + 1)) & 1u) atomicMax(a.hamax + ds.pair[dd][2 * q + 1], __float_as_uint(hm1));
+      }
+      hm0 = hm1 = 0.f;
+    };
+    int cur_d = d;
+    int item = 0;
+    bool ok = true;
+    for (int i = 0; i < nstage && ok; i++) {
+      if constexpr (MODE == 0) {
+        if (d != cur_d) {
+          flush_hmax(cur_d);
+          cur_d = d;
+        }
+      }
       const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
-      for (int pass = 0; pass < npass; pass++) {
-        const float4 *pr4 = slot_red + (size_t)pass * W * 32;
+      for (int pass = 0; pass < npass; pass++, item++) {
+        const int rs = item % kRedSlots;
+        if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(item / kRedSlots) & 1u)) {
+          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const float4 *pr4 = red + (size_t)rs * red_slot_f4 + lane;
         float4 sum = pr4[0];
 #pragma unroll
-        for (int ww = 1; ww < kMaxSliceWarps; ww++) {
+        for (int ww = 1; ww < kMaxKWarps; ww++) {
           if (ww < W) {
             const float4 v = pr4[ww * 32];
             sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
@@ -364,7 +399,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         }
         if constexpr (MODE == 0) {
           const uint32_t mask = ds.tokmask[d];
-          float *hrow = a.hbuf + tile * 8 + g;
+          float *hrow = a.hbuf + operand_order(tile * 8 + g);
 #pragma unroll
           for (int c2 = 0; c2 < 2; c2++) {
             const int t = 2 * q + c2;
@@ -372,7 +407,9 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
               const int p = ds.pair[d][t];
               const float gg = (c2 ? sum.y : sum.x) * ds.scal[d][0];
               const float uu = (c2 ? sum.w : sum.z) * ds.scal[d][1];
-              hrow[(size_t)p * a.I] = ds.wt[p] * silu(gg) * uu;
+              const float h = ds.wt[p] * silu(gg) * uu;
+              hrow[(size_t)p * a.I] = h;
+              if (c2) hm1 = fmaxf(hm1, fabsf(h)); else hm0 = fmaxf(hm0, fabsf(h));
             }
           }
         } else {
@@ -383,79 +420,72 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
                 make_float2((sum.x + sum.y) * gd, (sum.z + sum.w) * gd);
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_empty[rs]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_empty[rs]);
       if (++tile == a.tiles) { tile = 0; d++; }
+    }
+    if constexpr (MODE == 0) {
+      if (nstage > 0) flush_hmax(cur_d);
     }
     return;
   }
 
   // ---------------------------------------------------- consumers
   if constexpr (MODE == 1) pdl_wait();           // hbuf comes from the gate/up kernel
-  int cur_key = -1;                              // (expert rank, slot group) of bf
-  int d = (int)((t0 + grp) / a.tiles), tile = (int)((t0 + grp) - (long long)d * a.tiles);
-  for (int i = grp; i < nstage; i += G, tile += G) {
-    while (tile >= a.tiles) { tile -= a.tiles; d++; }
+  int cur_key = -1;                              // (expert rank, pass) of bf
+  int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
+  int item = 0;
+  bool ok = true;
+  for (int i = 0; i < nstage && ok; i++) {
     const int slot = i % S;
     const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
-
     if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
       atomicOr(a.flags, MOE_FLAG_TIMEOUT);
       break;
     }
-    const uint8_t *codes = ring + (size_t)slot * a.stage_bytes + (size_t)w * 4096;
-    const uint8_t *scales = ring + (size_t)slot * a.stage_bytes + (size_t)W * 4096 + (size_t)w * 512;
-    const int rs = i % kRedSlots;
-    const uint32_t ruse = (uint32_t)(i / kRedSlots);
-    if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
-      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-      break;
-    }
-    float4 *my_red = red + (size_t)rs * red_slot_f4 + (size_t)w * 32 + lane;
+    const uint8_t *codes = ring + (size_t)slot * a.stage_bytes + (size_t)slice * 4096 + (size_t)half * 2048;
+    const uint8_t *scales =
+        ring + (size_t)slot * a.stage_bytes + (size_t)NS * 4096 + (size_t)slice * 512 + (size_t)half * 256;
 
-    for (int pass = 0; pass < npass; pass++) {
+    for (int pass = 0; pass < npass; pass++, item++) {
+      const int rs = item % kRedSlots;
+      const uint32_t ruse = (uint32_t)(item / kRedSlots);
+      if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
+        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+        ok = false;
+        break;
+      }
       if constexpr (MODE == 1) {
         const int key = d * 2 + pass;
         if (key != cur_key) {
-          // B fragments of h: column g = slot 4*pass + g/2, hi (g even) / lo (g odd)
+          // B fragments of h: column g = slot 4*pass + g/2, hi (g even) / lo
+          // (g odd) f16 part of h * 2^s, with 2^s set by the slot's max |h|.
+          // Lane (g, q) reads the four values of each k-step it needs as one
+          // float4 (hbuf keeps every 16-element block in operand order).
           cur_key = key;
           const int sl = 4 * pass + (g >> 1);
           const bool have = sl < ds.nslot[d];
-          const float *hr = a.hbuf + (size_t)(have ? ds.slot_pair[d][sl] : 0) * a.I;
-          float am = 0.f;                        // first pass: max |h| of the slice
-#pragma unroll 8
-          for (int s = 0; s < kSliceSteps; s++) {
-            const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
-            if (have && k0 < K) {
-              const float2 v0 = __ldcg(reinterpret_cast<const float2 *>(hr + k0));
-              const float2 v1 = __ldcg(reinterpret_cast<const float2 *>(hr + k0 + 8));
-              am = fmaxf(am, fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v1.x), fabsf(v1.y))));
-            }
-          }
-          am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
-          am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+          const int pr = have ? ds.slot_pair[d][sl] : 0;
+          const float4 *hr4 = reinterpret_cast<const float4 *>(a.hbuf + (size_t)pr * a.I) + q;
+          const float am = have ? __uint_as_float(__ldcg(a.hamax + pr)) : 0.f;
           float inv;
           const float up = f16_range_scale(am, &inv);
           const bool lo = (g & 1) != 0;
 #pragma unroll
-          for (int s = 0; s < kSliceSteps; s++) {  // second pass: hi or lo f16 parts
-            const int k0 = 16 * (kSliceSteps * w + s) + 2 * q;
-            float2 v[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            if (have && k0 < K) {
-              v[0] = __ldcg(reinterpret_cast<const float2 *>(hr + k0));
-              v[1] = __ldcg(reinterpret_cast<const float2 *>(hr + k0 + 8));
-            }
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-              const float x0 = v[h].x * up, x1 = v[h].y * up;
-              const __half2 hi = __floats2half2_rn(x0, x1);
-              if (lo) {
-                const float2 hf = __half22float2(hi);
-                bf[s][h] = pack_half2(x0 - hf.x, x1 - hf.y);
-              } else {
-                bf[s][h] = *reinterpret_cast<const uint32_t *>(&hi);
-              }
+          for (int s = 0; s < kWarpSteps; s++) {
+            const int ks = ks0 + s;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (have && 16 * ks < K) v = __ldcg(hr4 + 4 * ks);
+            const float x0 = v.x * up, x1 = v.y * up, x2 = v.z * up, x3 = v.w * up;
+            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+            if (lo) {
+              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+              bf[s][0] = pack_half2(x0 - f01.x, x1 - f01.y);
+              bf[s][1] = pack_half2(x2 - f23.x, x3 - f23.y);
+            } else {
+              bf[s][0] = *reinterpret_cast<const uint32_t *>(&h01);
+              bf[s][1] = *reinterpret_cast<const uint32_t *>(&h23);
             }
           }
           // columns 2q (hi) and 2q+1 (lo) of this lane belong to slot q
@@ -468,7 +498,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       float acc4[4][4] = {};
       uint4 sc = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int qg = 0; qg < 8; qg++) {
+      for (int qg = 0; qg < kWarpSteps / 4; qg++) {
         const uint4 cw = *reinterpret_cast<const uint4 *>(codes + ((size_t)qg * 32 + lane) * 16);
         if ((qg & 1) == 0) sc = *reinterpret_cast<const uint4 *>(scales + ((size_t)(qg >> 1) * 8 + g) * 16);
         const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -490,31 +520,25 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       float acc[4];
 #pragma unroll
       for (int c4 = 0; c4 < 4; c4++) acc[c4] = (acc4[0][c4] + acc4[1][c4]) + (acc4[2][c4] + acc4[3][c4]);
-      my_red[(size_t)pass * W * 32] =
+      red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
           make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_full[rs]);     // this warp's partials are in the reduction slot
     }
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&empty_bar[slot]);                   // stage buffer may be refilled
-      mbar_arrive(&red_full[rs]);                      // slice partials are in the reduction slot
-    }
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);    // stage buffer may be refilled
+    if (++tile == a.tiles) { tile = 0; d++; }
   }
 }
 
 // ------------------------------------------------------------------ host side
-// Ring geometry.  Each ring slot must belong to one consumer group (S a
-// multiple of G): a slot shared by two groups lets a consumer that runs ahead
-// of the other group wait on a barrier phase two uses ahead, whose parity
-// aliases the current one, and arrive on the other group's phase.
-void gemv_geometry(int mode, int slice_warps, int *groups, int *stages, int *stage_bytes, int *smem_bytes) {
-  const int G = (32 * (kMaxGroups * slice_warps + 2) <= kMaxCtaThreads) ? kMaxGroups : 1;
-  const int tile = slice_warps * kTileSliceBytes;
-  const int red = kRedSlots * (mode == 0 ? 1 : kMaxPasses) * slice_warps * 32 * (int)sizeof(float4);
+// Ring geometry: as many tile stages as fit beside the reduction slots.
+void gemv_geometry(int slices, int *stages, int *stage_bytes, int *smem_bytes) {
+  const int tile = slices * kTileSliceBytes;
+  const int red = kRedSlots * 2 * slices * 32 * (int)sizeof(float4);
   int s = (kGemvSmemBytes - red) / tile;
   if (s > kMaxStages) s = kMaxStages;
-  s -= s % G;
-  if (s < G) s = G;
-  *groups = G;
+  if (s < 2) s = 2;
   *stage_bytes = tile;
   *stages = s;
   *smem_bytes = s * tile + red;
@@ -524,7 +548,7 @@ template <int MODE>
 static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(32 * (a.slice_warps * a.groups + 2));   // + producer + epilogue warps
+  cfg.blockDim = dim3(32 * (2 * a.slices + 2));   // consumers + producer + epilogue warps
   cfg.dynamicSmemBytes = (size_t)a.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

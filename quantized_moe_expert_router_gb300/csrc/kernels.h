@@ -24,6 +24,7 @@ struct RouteArgs {
   float *weights;        // [C][k]
   float *logits;         // workspace [C][E]
   uint32_t *ticket;      // workspace counter (0 between calls)
+  int32_t *flags;        // workspace flag word (MOE_FLAG_TIMEOUT)
   int C, E, H, k;
 };
 // Router GEMV fused with top-k (C <= 8): grid is fixed per layer.
@@ -39,7 +40,8 @@ struct GemvArgs {
   const uint16_t *x;         // bf16 bits [C][H]
   const int32_t *ids;        // [C][k]
   const float *weights;      // [C][k]
-  float *hbuf;               // [C*k][I]
+  float *hbuf;               // [C*k][I], 16-element blocks in operand order
+  uint32_t *hamax;           // [C*k] max |h| (float bits), zero outside a call
   float *ypair;              // [C*k][H]
   float *y;                  // [C][H]
   int32_t *flags;
@@ -47,15 +49,14 @@ struct GemvArgs {
   size_t expert_bytes;
   size_t region_off;         // 0 (gate/up) or the down region offset
   int tiles;                 // tiles per expert: I/8 (gate/up) or H/16 (down)
-  int tile_bytes;            // slice_warps * kTileSliceBytes
-  int slice_warps;           // W: consumer warps of a group = padded K / 512
-  int groups;                // consumer groups per CTA (alternate tiles)
-  int stages;                // shared-memory ring stages (a multiple of groups)
+  int tile_bytes;            // slices * kTileSliceBytes
+  int slices;                // 512-element K-slices per tile (padded K / 512); 2 consumer warps each
+  int stages;                // shared-memory ring stages
   int stage_bytes;           // bytes of one ring stage (one tile)
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
 };
-// Ring geometry, consumer groups and dynamic shared memory of one kernel.
-void gemv_geometry(int mode, int slice_warps, int *groups, int *stages, int *stage_bytes, int *smem_bytes);
+// Ring geometry and dynamic shared memory of one kernel.
+void gemv_geometry(int slices, int *stages, int *stage_bytes, int *smem_bytes);
 // Opt-in shared memory of the expert kernels (once per device; idempotent).
 cudaError_t gemv_setup();
 // mode 0: gate/up + SwiGLU -> hbuf; mode 1: down -> ypair -> combine -> y.
@@ -64,6 +65,7 @@ cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, 
 struct CombineArgs {
   const int32_t *ids;        // [C][k]
   const float *ypair;        // [C*k][H]
+  uint32_t *hamax;           // [C*k], reset to zero once the down kernel is done
   float *y;                  // [C][H]
   int C, k, E, H;
 };

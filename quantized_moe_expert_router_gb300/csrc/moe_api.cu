@@ -170,10 +170,11 @@ moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_rou
   a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
   a.logits = reinterpret_cast<float *>(w + wl.logits);
   a.ticket = &reinterpret_cast<moe::WsControl *>(w)->route_ticket;
+  a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
   cudaError_t err;
   if (C <= moe::kRouteFusedTokens) {
-    const int grid = (a.E + 7) / 8 < L->num_sms ? (a.E + 7) / 8 : L->num_sms;
+    const int grid = a.E < L->num_sms ? a.E : L->num_sms;   // router rows dealt round-robin
     err = moe::launch_route_fused(a, grid, stream);
   } else {
     err = moe::launch_route_batched(a, stream);
@@ -199,6 +200,7 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
   a.packed = pk;
   a.scalars = reinterpret_cast<const float *>(pk + L->scalars_off);
   a.hbuf = reinterpret_cast<float *>(w + wl.hbuf);
+  a.hamax = reinterpret_cast<uint32_t *>(w + wl.hamax);
   a.ypair = reinterpret_cast<float *>(w + wl.ypair);
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.k = k; a.E = L->cfg.num_experts; a.H = H; a.I = I;
@@ -218,8 +220,8 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.region_off = 0;
     a.tiles = I / 8;
     a.tile_bytes = (int)L->gu_tile_bytes;
-    a.slice_warps = L->w_gu;
-    moe::gemv_geometry(0, a.slice_warps, &a.groups, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    a.slices = L->w_gu;
+    moe::gemv_geometry(a.slices, &a.stages, &a.stage_bytes, &a.smem_bytes);
     err = moe::launch_expert_gemv(0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
@@ -228,13 +230,13 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.region_off = L->dn_region_off;
     a.tiles = H / 16;
     a.tile_bytes = (int)L->dn_tile_bytes;
-    a.slice_warps = L->w_dn;
-    moe::gemv_geometry(1, a.slice_warps, &a.groups, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    a.slices = L->w_dn;
+    moe::gemv_geometry(a.slices, &a.stages, &a.stage_bytes, &a.smem_bytes);
     err = moe::launch_expert_gemv(1, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     // weighted sum over each token's experts, ascending expert id
     moe::CombineArgs cb;
-    cb.ids = a.ids; cb.ypair = a.ypair; cb.y = a.y;
+    cb.ids = a.ids; cb.ypair = a.ypair; cb.y = a.y; cb.hamax = a.hamax;
     cb.C = Cg; cb.k = k; cb.E = a.E; cb.H = H;
     err = moe::launch_combine(cb, L->num_sms, true, stream);
   }

@@ -36,7 +36,9 @@ static_assert(sizeof(WsControl) == 256, "control block is 256 bytes");
 // tokens (GEMV path) and C tokens of router logits.
 struct WsLayout {
   size_t logits;      // float  [C][E]
-  size_t hbuf;        // float  [kGemvTokens * k][I]  w * silu(g) * u per (token, slot)
+  size_t hbuf;        // float  [kGemvTokens * k][I]  w * silu(g) * u per (token, slot), each
+                      //        16-element block stored in MMA operand order (see expert_gemv.cu)
+  size_t hamax;       // uint32 [kGemvTokens * k]     max |h| per (token, slot) as float bits
   size_t ypair;       // float  [kGemvTokens * k][H]  D_e h per (token, slot)
   size_t total;
 };
@@ -74,6 +76,8 @@ inline WsLayout ws_layout(const moe_layer &L, int C) {
   const size_t pairs = (size_t)kGemvTokens * L.cfg.top_k;
   w.hbuf = off;
   off = align_up(off + sizeof(float) * pairs * L.cfg.intermediate, 256);
+  w.hamax = off;
+  off = align_up(off + sizeof(uint32_t) * pairs, 256);
   w.ypair = off;
   off = align_up(off + sizeof(float) * pairs * L.cfg.hidden, 256);
   w.total = off;

@@ -9,10 +9,11 @@
 // softmax denominator cancels).  ids are written in ascending expert order.
 //
 // Small C (decode): one kernel.  Each warp owns whole router rows and streams
-// them once with 16-byte loads against x held in shared memory; every CTA
-// then takes a ticket, and the last CTA to finish runs the top-k of each token
-// in one warp (the ticket is reset for the next call).  No CTA ever waits for
-// another.  Large C: a tiled fp32 logits kernel and a top-k kernel.
+// them once with 16-byte loads (a whole row in flight per warp) against x held
+// in shared memory; every CTA then takes a ticket, and the last CTA to finish
+// runs the top-k of each token with all its warps (the ticket is reset for
+// the next call).  No CTA ever waits for another.  Large C: a tiled fp32
+// logits kernel and a top-k kernel with one CTA per token.
 #include "moe_internal.cuh"
 #include "kernels.h"
 
@@ -34,50 +35,75 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float(u);
 }
 
-// Top-k of one token's E logits by one warp.  Lane l holds experts l + 32 i.
-// Each round takes the warp maximum key (redux.sync), breaks ties by the
-// lowest expert index (redux.sync min), and removes the winner.
-__device__ void warp_topk(const float *logits, int E, int k, int32_t *ids_out,
-                          float *w_out) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[kMaxExperts / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; i++) {
-    const int e = lane + 32 * i;
-    key[i] = (e < E) ? order_key(__ldcg(logits + e)) : 0u;
-  }
-  uint32_t bk = 0;
-  int bi = 0x7FFFFFFF;
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; i++)
-    if (key[i] > bk) { bk = key[i]; bi = lane + 32 * i; }
+// Strict total order of the selection: larger key first, equal keys -> lower
+// expert index first.
+__device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
 
-  uint32_t my_key = 0;
-  int my_idx = 0x7FFFFFFF;
-  for (int r = 0; r < k; r++) {
-    const uint32_t wmax = __reduce_max_sync(kFull, bk);
-    const uint32_t cand = (bk == wmax) ? (uint32_t)bi : 0xFFFFFFFFu;
-    const int widx = (int)__reduce_min_sync(kFull, cand);
-    if (lane == r) { my_key = wmax; my_idx = widx; }
-    if ((widx & 31) == lane) {
-      const int slot = widx >> 5;
+// Sorts a lane's V candidates into the total order (odd-even transposition:
+// V rounds of independent compare-exchanges, all in registers).
+template <int V>
+__device__ __forceinline__ void lane_sort(uint32_t (&key)[V], int (&idx)[V]) {
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; i++)
-        if (i == slot) key[i] = 0u;
-      bk = 0;
-      bi = 0x7FFFFFFF;
+  for (int r = 0; r < V; r++) {
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; i++)
-        if (key[i] > bk) { bk = key[i]; bi = lane + 32 * i; }
+    for (int i = r & 1; i + 1 < V; i += 2) {
+      const bool sw = precedes(key[i + 1], idx[i + 1], key[i], idx[i]);
+      const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
+      const int i0 = sw ? idx[i + 1] : idx[i], i1 = sw ? idx[i] : idx[i + 1];
+      key[i] = k0; key[i + 1] = k1; idx[i] = i0; idx[i + 1] = i1;
     }
   }
-  // renormalised softmax over the kept logits; lane 0 holds the largest
+}
+
+// The first k (key, expert) in the total order among the warp's 32 V
+// candidates, each lane's V already sorted (key 0 = absent).  Lane r ends with
+// the r-th (key 0 if there is none).  A round takes the warp maximum of the
+// lane heads (redux.sync); when several lanes hold it (equal keys) the lowest
+// expert index wins (a second redux.sync, rarely needed); the winning lane
+// pops its head, predicated, without branches.
+template <int V>
+__device__ __forceinline__ void warp_pop_select(uint32_t (&key)[V], int (&idx)[V], int k,
+                                                uint32_t &my_key, int &my_idx) {
+  const int lane = threadIdx.x & 31;
+  my_key = 0u;
+  my_idx = 0x7FFFFFFF;
+  for (int r = 0; r < k; r++) {
+    const uint32_t hk = key[0];
+    const uint32_t wmax = __reduce_max_sync(kFull, hk);
+    if (wmax == 0u) break;
+    const bool top = hk == wmax;
+    const unsigned holders = __ballot_sync(kFull, top);
+    bool win = top;
+    int wl = __ffs(holders) - 1;
+    if (holders & (holders - 1)) {             // equal keys in several lanes
+      const int widx = (int)__reduce_min_sync(kFull, top ? (uint32_t)idx[0] : 0xFFFFFFFFu);
+      win = top && idx[0] == widx;
+      wl = __ffs(__ballot_sync(kFull, win)) - 1;
+    }
+    const int widx = __shfl_sync(kFull, idx[0], wl);
+    my_key = (lane == r) ? wmax : my_key;
+    my_idx = (lane == r) ? widx : my_idx;
+#pragma unroll
+    for (int i = 0; i + 1 < V; i++) {
+      key[i] = win ? key[i + 1] : key[i];
+      idx[i] = win ? idx[i + 1] : idx[i];
+    }
+    key[V - 1] = win ? 0u : key[V - 1];
+  }
+}
+
+// Renormalised softmax over the selected logits (lane r holds the r-th
+// largest key) and output in ascending expert order.
+__device__ __forceinline__ void write_selection(uint32_t my_key, int my_idx, int k, int32_t *ids_out,
+                                                float *w_out) {
+  const int lane = threadIdx.x & 31;
   const float lmax = __shfl_sync(kFull, key_value(my_key), 0);
   const float ex = (lane < k) ? expf(key_value(my_key) - lmax) : 0.f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-  // rank in ascending expert order
   int rank = 0;
   for (int j = 0; j < k; j++) {
     const int other = __shfl_sync(kFull, my_idx, j);
@@ -89,51 +115,165 @@ __device__ void warp_topk(const float *logits, int E, int k, int32_t *ids_out,
   }
 }
 
-template <int CT>
-__global__ void __launch_bounds__(256) route_fused_kernel(const RouteArgs a) {
-  extern __shared__ float4 xs4[];          // [CT][H/4] float4
-  float *xs = reinterpret_cast<float *>(xs4);
-  __shared__ int s_last;
-  pdl_wait();
-  const int H4 = a.H / 4;
-  for (int i = threadIdx.x; i < CT * a.H; i += blockDim.x) {
-    const int t = i / a.H, j = i - t * a.H;
-    xs[i] = (t < a.C) ? __uint_as_float((uint32_t)a.x[(size_t)t * a.H + j] << 16) : 0.f;
+constexpr int kRouteWarps = 8;
+constexpr int kChunkVals = kMaxExperts / 32 / kRouteWarps;   // experts per lane in a warp's chunk
+
+struct TopkSmem {
+  uint32_t key[kRouteWarps][32];   // per warp: its first k in the total order (absent beyond)
+  int idx[kRouteWarps][32];
+};
+
+// Top-k (k <= 32) of one token's E <= 1024 logits by the 8 warps of a CTA.
+// Warp w selects the first k of experts [128 w, 128 w + 128) (four per lane);
+// the union of the 8 sorted lists holds the token's first k, and warp 0
+// selects them from the lists (lane l holds 8 consecutive entries of list
+// l / 4, so each lane's candidates are already sorted).  All threads of the
+// CTA must call this.
+__device__ void cta_topk(const float *lg, int E, int k, int32_t *ids_out, float *w_out, TopkSmem &s) {
+  static_assert(kChunkVals == 4, "four experts per lane");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    uint32_t key[kChunkVals];
+    int idx[kChunkVals];
+#pragma unroll
+    for (int c = 0; c < kChunkVals; c++) {
+      const int e = warp * 32 * kChunkVals + 32 * c + lane;
+      idx[c] = e < E ? e : 0x7FFFFFFF;
+      key[c] = (e < E) ? order_key(__ldcg(lg + e)) : 0u;
+    }
+    lane_sort(key, idx);
+    uint32_t my_key;
+    int my_idx;
+    warp_pop_select(key, idx, k, my_key, my_idx);
+    s.key[warp][lane] = my_key;                 // lanes >= k hold key 0 (absent)
+    s.idx[warp][lane] = my_idx;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const uint64_t pol = l2_evict_first_policy();
-  for (int e = blockIdx.x * nwarps + warp; e < a.E; e += gridDim.x * nwarps) {
-    const float4 *wrow = reinterpret_cast<const float4 *>(a.w_router + (size_t)e * a.H);
-    float acc[CT];
+  if (warp == 0) {
+    uint32_t key[8];
+    int idx[8];
 #pragma unroll
-    for (int t = 0; t < CT; t++) acc[t] = 0.f;
-#pragma unroll 7
-    for (int j = lane; j < H4; j += 32) {
-      const uint4 wr = ld_stream_v4(wrow + j, pol);
-      const float4 w = make_float4(__uint_as_float(wr.x), __uint_as_float(wr.y),
-                                   __uint_as_float(wr.z), __uint_as_float(wr.w));
-#pragma unroll
-      for (int t = 0; t < CT; t++) {
-        const float4 xv = xs4[t * H4 + j];
-        acc[t] = fmaf(w.x, xv.x, acc[t]);
-        acc[t] = fmaf(w.y, xv.y, acc[t]);
-        acc[t] = fmaf(w.z, xv.z, acc[t]);
-        acc[t] = fmaf(w.w, xv.w, acc[t]);
-      }
+    for (int i = 0; i < 8; i++) {
+      key[i] = s.key[lane >> 2][8 * (lane & 3) + i];
+      idx[i] = s.idx[lane >> 2][8 * (lane & 3) + i];
     }
+    uint32_t my_key;
+    int my_idx;
+    warp_pop_select(key, idx, k, my_key, my_idx);
+    write_selection(my_key, my_idx, k, ids_out, w_out);
+  }
+  __syncthreads();                               // s is reused by the next token
+}
+
+// Shared memory of the fused router: x of up to CT tokens as fp32, then the
+// CTA's router rows (one round of at most kRouteRowSmem bytes).
+constexpr int kRouteSmemBytes = 200 * 1024;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+template <int CT>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const RouteArgs a) {
+  extern __shared__ __align__(128) float4 xs4[];   // [CT][H/4] then [rows][H/4]
+  __shared__ int s_last;
+  __shared__ TopkSmem tk;
+  __shared__ __align__(8) uint64_t rows_bar;
+  pdl_wait();
+  pdl_launch_dependents();                 // the expert kernel may start its prologue
+  const int H4 = a.H / 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t row_bytes = (size_t)a.H * sizeof(float);
+  float4 *rows4 = xs4 + (size_t)CT * H4;
+  const int max_rows = (int)((kRouteSmemBytes - (size_t)CT * row_bytes) / row_bytes);
+  // this CTA's router rows: a contiguous range, streamed into shared memory
+  // with bulk copies in rounds of at most max_rows rows
+  const int r0 = (int)((long long)a.E * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)a.E * (blockIdx.x + 1) / gridDim.x);
+  const uint64_t pol = l2_evict_first_policy();
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rows_bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  bool ok = true;
+  for (int rb = r0, round = 0; rb < r1; rb += max_rows, round++) {
+    const int nr = (r1 - rb) < max_rows ? (r1 - rb) : max_rows;
+    if (threadIdx.x == 0) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rows_bar)),
+                   "r"((uint32_t)(nr * row_bytes)) : "memory");
+      for (int r = 0; r < nr; r++)
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+            ::"r"(smem_addr(rows4 + (size_t)r * H4)), "l"(a.w_router + (size_t)(rb + r) * a.H),
+            "r"((uint32_t)row_bytes), "r"(smem_addr(&rows_bar)), "l"(pol) : "memory");
+    }
+    if (round == 0) {
+      // x -> fp32 in shared memory, 8 bf16 per 16-byte load, all loads of a
+      // thread issued together
+      const int H8 = a.H / 8;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < CT * H8; i += blockDim.x) {
+        const int t = i / H8, j = i - t * H8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < a.C) v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H) + j);
+        xs4[2 * i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                 __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+        xs4[2 * i + 1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                     __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+      }
+      __syncthreads();
+    }
+    // bounded wait for the round's rows (about two seconds of %globaltimer)
+    {
+      uint32_t done = 0;
+      unsigned long long t0 = 0;
+      for (uint32_t it = 0;; it++) {
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(smem_addr(&rows_bar)), "r"((uint32_t)(round & 1)) : "memory");
+        if (done) break;
+        unsigned long long now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        if (it == 0) t0 = now;
+        else if (now - t0 > 2000000000ull) break;
+      }
+      ok = __syncthreads_and(done != 0) != 0;    // one decision for the whole CTA
+      if (!ok && threadIdx.x == 0) atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+    }
+    if (!ok) break;
+    // dot products: warp w takes rows w, w + 8, ... of the round
+    for (int r = warp; r < nr; r += kRouteWarps) {
+      const float4 *wrow = rows4 + (size_t)r * H4;
+      float acc[CT];
 #pragma unroll
-    for (int t = 0; t < CT; t++)
+      for (int t = 0; t < CT; t++) acc[t] = 0.f;
+      for (int j = lane; j < H4; j += 32) {
+        const float4 w = wrow[j];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(kFull, acc[t], o);
-    if (lane == 0) {
-      const float b = a.bias ? a.bias[e] : 0.f;
+        for (int t = 0; t < CT; t++) {
+          const float4 xv = xs4[t * H4 + j];
+          acc[t] = fmaf(w.x, xv.x, acc[t]);
+          acc[t] = fmaf(w.y, xv.y, acc[t]);
+          acc[t] = fmaf(w.z, xv.z, acc[t]);
+          acc[t] = fmaf(w.w, xv.w, acc[t]);
+        }
+      }
 #pragma unroll
       for (int t = 0; t < CT; t++)
-        if (t < a.C) a.logits[(size_t)t * a.E + e] = acc[t] + b;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(kFull, acc[t], o);
+      if (lane == 0) {
+        const int e = rb + r;
+        const float b = a.bias ? a.bias[e] : 0.f;
+#pragma unroll
+        for (int t = 0; t < CT; t++)
+          if (t < a.C) a.logits[(size_t)t * a.E + e] = acc[t] + b;
+      }
     }
+    __syncthreads();                       // the rows buffer is refilled by the next round
   }
-  // last CTA to finish runs the top-k
+  if (!ok) return;                         // the flag is set; no copy of this CTA is left in flight
+  // the last CTA to finish runs the top-k
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -143,9 +283,8 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (warp < a.C)
-    warp_topk(a.logits + (size_t)warp * a.E, a.E, a.k, a.ids + (size_t)warp * a.k,
-              a.weights + (size_t)warp * a.k);
+  for (int t = 0; t < a.C; t++)
+    cta_topk(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
@@ -188,14 +327,13 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs
     }
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const RouteArgs a) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= a.C) return;
-  warp_topk(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k,
-            a.weights + (size_t)t * a.k);
+__global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const RouteArgs a) {
+  __shared__ TopkSmem tk;
+  const int t = blockIdx.x;
+  cta_topk(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
 }
 
-static size_t fused_smem(int ct, int H) { return sizeof(float) * (size_t)ct * H; }
+static size_t fused_smem(int ct, int H) { (void)ct; (void)H; return kRouteSmemBytes; }
 
 // Opt-in shared memory for the largest hidden size the library accepts, so
 // the attribute does not depend on which layer set it.
@@ -228,7 +366,7 @@ cudaError_t launch_route_batched(const RouteArgs &a, cudaStream_t stream) {
   route_logits_tiled_kernel<<<g1, 256, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  route_topk_kernel<<<(a.C + 7) / 8, 256, 0, stream>>>(a);
+  route_topk_kernel<<<a.C, kRouteWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

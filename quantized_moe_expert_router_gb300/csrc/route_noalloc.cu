@@ -72,14 +72,15 @@ extern "C" moe_status moe_route_noalloc(moe_layer_t L, const uint16_t *x, int C,
   if (prev != L->device && cudaSetDevice(L->device) != cudaSuccess) return MOE_ERR_CUDA;
   unsigned char *scratch = nullptr;
   cudaError_t err = scratch_address(L->device, &scratch);
-  if (err == cudaSuccess) err = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), stream);
+  if (err == cudaSuccess) err = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), stream);
   if (err == cudaSuccess) {
     moe::RouteArgs a;
     a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
     a.logits = reinterpret_cast<float *>(scratch + 256);
     a.ticket = reinterpret_cast<uint32_t *>(scratch);
+    a.flags = reinterpret_cast<int32_t *>(scratch + sizeof(uint32_t));
     a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
-    const int grid = (a.E + 7) / 8 < L->num_sms ? (a.E + 7) / 8 : L->num_sms;
+    const int grid = a.E < L->num_sms ? a.E : L->num_sms;
     err = moe::launch_route_fused(a, grid, stream);
   }
   if (prev != L->device) cudaSetDevice(prev);
