@@ -66,6 +66,8 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
+    p.add_argument("--experts", type=int, default=None,
+                   help="use this many experts instead of the workload's (a smaller case for profiler captures)")
     return p.parse_args()
 
 
@@ -243,7 +245,10 @@ def run_reference(args, cfg, rank):
 
 def main():
     args = parse()
-    cfg = CONFIGS[args.config]
+    cfg = dict(CONFIGS[args.config])
+    if args.experts:
+        cfg["E"] = args.experts
+        cfg["workload"] += f" [reduced to {args.experts} experts for profiling]"
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, cfg, rank)
@@ -463,7 +468,9 @@ def main():
             "distinct_experts_per_step": avg_distinct,
             "roofline": roofline,
             "e2e": e2e,
-            "gpu_launches": 3 * args.steps * (C + 7) // 8 if C > 8 else 3 * args.steps,
+            # per step: the router (one kernel, two for C > 8) and, per group of
+            # 8 tokens, the gate/up, down and combine kernels
+            "gpu_launches": args.steps * ((1 if C <= 8 else 2) + 3 * ((C + 7) // 8)),
             "clocks": clocks,
             "host_s": t_host,
             "device_flags": flags,

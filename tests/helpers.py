@@ -42,3 +42,19 @@ def gapped_tokens(seed, layer, C, H, Wr, k, bias=None, min_gap=MIN_GAP, max_atte
             attempts[t] += 1
         x = synth.tokens(seed, layer, C, H, attempts)
     raise RuntimeError("could not draw tokens with the required logit gap")
+
+
+def golden_figures(name="k3_figures.txt"):
+    """Parse a `name = value ; page ; section` fixture under tests/golden."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+    out = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split("=", 1)
+            value = rest.split(";", 1)[0].strip()
+            out[key.strip()] = float(value) if "." in value else int(value)
+    return out

@@ -1,8 +1,9 @@
 """Pins of the oracle's number decoding and layout size against things other
 than the oracle: the e2m1 value set of the OCP Microscaling format, torch's
-float8_e4m3fn and bfloat16 conversions, and the byte count per expert printed
-in "Kimi-K3 on the same pod, two engines", section "Same hardware, same
-weights"."""
+float8_e4m3fn and bfloat16 conversions, and the sizes the pages print for the
+K3 layer (tests/golden/k3_figures.txt: "Kimi-K3 on the same pod, two
+engines", sections "Same hardware, same weights" and "Reason 1 -- slice every
+expert across all eight Sparks"; "SparkInfer-K3", "The model")."""
 import math
 
 import numpy as np
@@ -10,6 +11,8 @@ import pytest
 import torch
 
 import oracle
+
+from helpers import golden_figures
 
 # The eight e2m1 magnitudes of the OCP MX v1.0 FP4 (E2M1) format, codes 0..7.
 E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
@@ -54,12 +57,32 @@ def test_bf16_matches_torch():
 
 
 def test_expert_bytes_match_the_k3_checkpoint():
-    # "82,432 routed experts of 18,579,480 bytes each" at H 3584, I 3072.
-    assert oracle.expert_bytes(3584, 3072) == 18_579_480
+    fig = golden_figures()
+    H, I = fig["expert_latent_width"], fig["expert_ffn_width"]
+    assert oracle.expert_bytes(H, I) == fig["expert_bytes_h3584_i3072"]
     # the small test layer (H 256, I 192)
     assert oracle.expert_bytes(256, 192) == 82_968
-    # 93 layers minus the leading dense block times 896 experts = 82,432
-    assert 92 * 896 == 82_432
+    # every layer but the leading dense one holds the routed experts
+    assert (fig["layers"] - 1) * fig["routed_experts_per_layer"] == fig["routed_experts_per_checkpoint"]
+
+
+def test_expert_slice_of_eight_matches_the_printed_size():
+    # One eighth of the intermediate columns of an expert (gate/up rows and the
+    # matching down columns, with their own scalars) is the printed ~2.32 MB.
+    fig = golden_figures()
+    H, I = fig["expert_latent_width"], fig["expert_ffn_width"]
+    slice_bytes = oracle.expert_bytes(H, I // 8)
+    assert round(slice_bytes / 1e6, 2) == fig["slice_megabytes_of_eight"]
+    # the eight slices hold the whole expert except 7 extra copies of the 24 scalar bytes
+    assert 8 * slice_bytes - oracle.expert_bytes(H, I) == 7 * 24
+
+
+def test_expert_bands_of_eight_ranks():
+    # 896 experts in 8 equal contiguous bands; the printed bands of ranks 3 and 7.
+    fig = golden_figures()
+    band = fig["routed_experts_per_layer"] // 8
+    assert (3 * band, 4 * band) == (fig["expert_band_rank3_lo"], fig["expert_band_rank3_hi"])
+    assert (7 * band, 8 * band) == (fig["expert_band_rank7_lo"], fig["expert_band_rank7_hi"])
 
 
 def test_dequant_layout_nibbles_blocks_rows():
