@@ -299,7 +299,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        sample_x = np.concatenate(x_host[:4], axis=0)[:8]
+        sample_x = np.concatenate(x_host, axis=0)[:16]
         host_cache = {}
 
         def weights_for(sel):
