@@ -15,12 +15,14 @@
 
 namespace moe {
 
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+constexpr int kCombineBatch = 16;
+constexpr int kCombineThreads = 64;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
   __shared__ int order[kGemvTokens][kMaxTopK];
   __shared__ int cnt[kGemvTokens];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp < a.C) {
-    const int t = warp;
+  for (int t = warp; t < a.C; t += kCombineThreads / 32) {
     const int e = lane < a.k ? a.ids[(size_t)t * a.k + lane] : -1;
     // valid: in range, and not a repeat of a lower slot's id
     bool valid = lane < a.k && (unsigned)e < (unsigned)a.E;
@@ -46,11 +48,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   const int H4 = a.H / 4;
   for (int it = blockIdx.x * blockDim.x + tid; it < a.C * H4; it += gridDim.x * blockDim.x) {
     const int t = it / H4, c4 = it - t * H4;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     const int n = cnt[t];
-    for (int j = 0; j < n; j++) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.ypair + (size_t)order[t][j] * a.H) + c4);
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    // all loads of a batch in flight together, then summed in slot order
+    for (int j0 = 0; j0 < n; j0 += kCombineBatch) {
+      float4 v[kCombineBatch];
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; j++)
+        v[j] = j0 + j < n ? __ldcg(reinterpret_cast<const float4 *>(a.ypair + (size_t)order[t][j0 + j] * a.H) + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; j++) {
+        if (j0 + j < n) {
+          s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
+        }
+      }
     }
     reinterpret_cast<float4 *>(a.y + (size_t)t * a.H)[c4] = s;
   }
@@ -58,11 +70,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 cudaError_t launch_combine(const CombineArgs &a, int num_sms, bool pdl, cudaStream_t stream) {
   const int items = a.C * (a.H / 4);
-  int grid = (items + 255) / 256;
+  int grid = (items + kCombineThreads - 1) / kCombineThreads;
   if (grid > num_sms) grid = num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

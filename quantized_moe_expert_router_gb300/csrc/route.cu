@@ -16,154 +16,12 @@
 // logits kernel and a top-k kernel with one CTA per token.
 #include "moe_internal.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-
-// Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 is
-// folded onto +0.  Key 0 (the image of one negative NaN pattern) marks
-// "taken / absent".
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7FFFFFFFu) == 0) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t k) {
-  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(u);
-}
-
-// Strict total order of the selection: larger key first, equal keys -> lower
-// expert index first.
-__device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int ib) {
-  return ka > kb || (ka == kb && ia < ib);
-}
-
-// Sorts a lane's V candidates into the total order (odd-even transposition:
-// V rounds of independent compare-exchanges, all in registers).
-template <int V>
-__device__ __forceinline__ void lane_sort(uint32_t (&key)[V], int (&idx)[V]) {
-#pragma unroll
-  for (int r = 0; r < V; r++) {
-#pragma unroll
-    for (int i = r & 1; i + 1 < V; i += 2) {
-      const bool sw = precedes(key[i + 1], idx[i + 1], key[i], idx[i]);
-      const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
-      const int i0 = sw ? idx[i + 1] : idx[i], i1 = sw ? idx[i] : idx[i + 1];
-      key[i] = k0; key[i + 1] = k1; idx[i] = i0; idx[i + 1] = i1;
-    }
-  }
-}
-
-// The first k (key, expert) in the total order among the warp's 32 V
-// candidates, each lane's V already sorted (key 0 = absent).  Lane r ends with
-// the r-th (key 0 if there is none).  A round takes the warp maximum of the
-// lane heads (redux.sync); when several lanes hold it (equal keys) the lowest
-// expert index wins (a second redux.sync, rarely needed); the winning lane
-// pops its head, predicated, without branches.
-template <int V>
-__device__ __forceinline__ void warp_pop_select(uint32_t (&key)[V], int (&idx)[V], int k,
-                                                uint32_t &my_key, int &my_idx) {
-  const int lane = threadIdx.x & 31;
-  my_key = 0u;
-  my_idx = 0x7FFFFFFF;
-  for (int r = 0; r < k; r++) {
-    const uint32_t hk = key[0];
-    const uint32_t wmax = __reduce_max_sync(kFull, hk);
-    if (wmax == 0u) break;
-    const bool top = hk == wmax;
-    const unsigned holders = __ballot_sync(kFull, top);
-    bool win = top;
-    int wl = __ffs(holders) - 1;
-    if (holders & (holders - 1)) {             // equal keys in several lanes
-      const int widx = (int)__reduce_min_sync(kFull, top ? (uint32_t)idx[0] : 0xFFFFFFFFu);
-      win = top && idx[0] == widx;
-      wl = __ffs(__ballot_sync(kFull, win)) - 1;
-    }
-    const int widx = __shfl_sync(kFull, idx[0], wl);
-    my_key = (lane == r) ? wmax : my_key;
-    my_idx = (lane == r) ? widx : my_idx;
-#pragma unroll
-    for (int i = 0; i + 1 < V; i++) {
-      key[i] = win ? key[i + 1] : key[i];
-      idx[i] = win ? idx[i + 1] : idx[i];
-    }
-    key[V - 1] = win ? 0u : key[V - 1];
-  }
-}
-
-// Renormalised softmax over the selected logits (lane r holds the r-th
-// largest key) and output in ascending expert order.
-__device__ __forceinline__ void write_selection(uint32_t my_key, int my_idx, int k, int32_t *ids_out,
-                                                float *w_out) {
-  const int lane = threadIdx.x & 31;
-  const float lmax = __shfl_sync(kFull, key_value(my_key), 0);
-  const float ex = (lane < k) ? expf(key_value(my_key) - lmax) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-  int rank = 0;
-  for (int j = 0; j < k; j++) {
-    const int other = __shfl_sync(kFull, my_idx, j);
-    rank += (other < my_idx);
-  }
-  if (lane < k) {
-    ids_out[rank] = my_idx;
-    w_out[rank] = ex / sum;
-  }
-}
-
 constexpr int kRouteWarps = 8;
-constexpr int kChunkVals = kMaxExperts / 32 / kRouteWarps;   // experts per lane in a warp's chunk
-
-struct TopkSmem {
-  uint32_t key[kRouteWarps][32];   // per warp: its first k in the total order (absent beyond)
-  int idx[kRouteWarps][32];
-};
-
-// Top-k (k <= 32) of one token's E <= 1024 logits by the 8 warps of a CTA.
-// Warp w selects the first k of experts [128 w, 128 w + 128) (four per lane);
-// the union of the 8 sorted lists holds the token's first k, and warp 0
-// selects them from the lists (lane l holds 8 consecutive entries of list
-// l / 4, so each lane's candidates are already sorted).  All threads of the
-// CTA must call this.
-__device__ void cta_topk(const float *lg, int E, int k, int32_t *ids_out, float *w_out, TopkSmem &s) {
-  static_assert(kChunkVals == 4, "four experts per lane");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  {
-    uint32_t key[kChunkVals];
-    int idx[kChunkVals];
-#pragma unroll
-    for (int c = 0; c < kChunkVals; c++) {
-      const int e = warp * 32 * kChunkVals + 32 * c + lane;
-      idx[c] = e < E ? e : 0x7FFFFFFF;
-      key[c] = (e < E) ? order_key(__ldcg(lg + e)) : 0u;
-    }
-    lane_sort(key, idx);
-    uint32_t my_key;
-    int my_idx;
-    warp_pop_select(key, idx, k, my_key, my_idx);
-    s.key[warp][lane] = my_key;                 // lanes >= k hold key 0 (absent)
-    s.idx[warp][lane] = my_idx;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t key[8];
-    int idx[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      key[i] = s.key[lane >> 2][8 * (lane & 3) + i];
-      idx[i] = s.idx[lane >> 2][8 * (lane & 3) + i];
-    }
-    uint32_t my_key;
-    int my_idx;
-    warp_pop_select(key, idx, k, my_key, my_idx);
-    write_selection(my_key, my_idx, k, ids_out, w_out);
-  }
-  __syncthreads();                               // s is reused by the next token
-}
 
 // Shared memory of the fused router: x of up to CT tokens as fp32, then the
 // CTA's router rows (one round of at most kRouteRowSmem bytes).
@@ -177,7 +35,7 @@ template <int CT>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const RouteArgs a) {
   extern __shared__ __align__(128) float4 xs4[];   // [CT][H/4] then [rows][H/4]
   __shared__ int s_last;
-  __shared__ TopkSmem tk;
+  __shared__ SelectSmem tk;
   __shared__ __align__(8) uint64_t rows_bar;
   pdl_wait();
   pdl_launch_dependents();                 // the expert kernel may start its prologue
@@ -284,7 +142,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   if (!s_last) return;
   __threadfence();
   for (int t = 0; t < a.C; t++)
-    cta_topk(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
+    cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
@@ -328,9 +186,9 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs
 }
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const RouteArgs a) {
-  __shared__ TopkSmem tk;
+  __shared__ SelectSmem tk;
   const int t = blockIdx.x;
-  cta_topk(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
+  cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
 }
 
 static size_t fused_smem(int ct, int H) { (void)ct; (void)H; return kRouteSmemBytes; }

@@ -240,6 +240,29 @@ def test_argument_errors_return_status_without_launch():
             moe.Layer(*bad, 1)
 
 
+@pytest.mark.parametrize("C,k", [(1, 8), (3, 12), (11, 8)])
+def test_router_ties_take_lower_ids(C, k):
+    # Zero router weights: every logit is its bias exactly.  Ten experts share
+    # each bias value (with +0 and -0 in one group), so the k-th boundary
+    # falls inside a tie and the lower expert ids must be kept.
+    E, H = 40, 64
+    h = moe.Layer(E, k, H, 64, 16)
+    ws = moe.alloc_workspace(h, 16)
+    rng = np.random.default_rng(7)
+    bias = rng.permutation(np.repeat(np.array([2.0, 1.0, 0.0, -1.0], np.float32), 10))
+    zero_idx = np.nonzero(bias == 0.0)[0]
+    bias[zero_idx[::2]] = -0.0
+    xb = synth.tokens(7, 0, C, H)
+    x = torch.from_numpy(xb.view(np.int16)).to(DEV)
+    ids = torch.empty((C, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((C, k), dtype=torch.float32, device=DEV)
+    Wr = torch.zeros((E, H), dtype=torch.float32, device=DEV)
+    moe.moe_route(h, x, C, Wr, torch.from_numpy(bias).to(DEV), ids, w, ws)
+    oids, ow, _ = oracle.route(np.tile(bias.astype(np.float64), (C, 1)), k)
+    assert (ids.cpu().numpy() == oids).all(), (ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-8)
+
+
 # ------------------------------------------------------------------ K3 shape
 
 @pytest.fixture(scope="module")
