@@ -19,8 +19,9 @@
  *     on the device (an expert id out of range or repeated within a token) set
  *     bits in a flag word inside the workspace: read them with
  *     moe_get_device_status.  No kernel traps or asserts.
- *   - moe_route and moe_forward allocate nothing and never synchronise the
- *     host, so a sequence of them can be captured into a CUDA graph.
+ *   - moe_route, moe_forward and moe_route_forward allocate nothing and never
+ *     synchronise the host, so a sequence of them can be captured into a CUDA
+ *     graph.
  *   - The handle is immutable after creation; concurrent calls on different
  *     streams need different workspaces and output buffers.
  *
@@ -141,6 +142,14 @@ moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
 moe_status moe_forward(moe_layer_t layer, const uint16_t *x, int num_tokens,
                        const int32_t *ids, const float *weights, const void *packed,
                        float *y, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The whole layer for C tokens: moe_route then moe_forward on `stream`
+ * (ids and weights are written).  Arguments and errors as those two calls;
+ * nothing is queued when an argument is rejected. */
+moe_status moe_route_forward(moe_layer_t layer, const uint16_t *x, int num_tokens,
+                             const float *w_router, const float *bias, const void *packed,
+                             int32_t *ids, float *weights, float *y, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
 
 /* Synchronise `stream`, return the device flag bits accumulated in `ws` since
  * the last call (MOE_FLAG_*), and clear them. */

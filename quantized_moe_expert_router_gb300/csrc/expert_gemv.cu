@@ -53,189 +53,9 @@
 // bitwise reproducible.
 #include "moe_internal.cuh"
 #include "kernels.h"
+#include "gemv_core.cuh"
 
 namespace moe {
-
-constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kSliceSteps = 32;                  // k-steps of one 512-element K-slice of a tile
-constexpr int kWarpSteps = 16;                   // k-steps per consumer warp (half a slice)
-constexpr int kMaxKWarps = 16;                   // consumer warps: K <= 4096
-constexpr int kMaxCtaThreads = 32 * (kMaxKWarps + 2);   // + producer and epilogue warps
-constexpr int kRedSlots = 4;                     // consumer -> epilogue reduction ring
-constexpr int kMaxStages = 8;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-
-struct DispatchSmem {
-  uint32_t bitmap[kMaxExperts / 32];
-  int base[kMaxExperts / 32];
-  int n;
-  int16_t expert[kMaxPairs];
-  uint32_t tokmask[kMaxPairs];
-  int pair[kMaxPairs][kGemvTokens];            // by token (lowest slot of a repeated id)
-  int16_t slot_pair[kMaxPairs][kGemvTokens];   // by slot (tokens in ascending order)
-  uint8_t nslot[kMaxPairs];
-  float wt[kMaxPairs];                         // router weight of pair p
-  float scal[kMaxPairs][3];                    // tensor scales g_gate, g_up, g_down of rank d
-};
-
-// ---------------------------------------------------------------- mbarrier
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Bounded wait for the phase with `parity` to complete; false on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; it++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                              uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- math
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// e4m3 pair (low byte: rowA scale, high byte: rowB scale) -> f16x2.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v16));
-  return r;
-}
-// a * (s.lo, s.lo) and a * (s.hi, s.hi) in f16x2 (exact for code x scale).
-__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), __low2half2(*reinterpret_cast<const __half2 *>(&s)));
-  return *reinterpret_cast<const uint32_t *>(&r);
-}
-__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), __high2half2(*reinterpret_cast<const __half2 *>(&s)));
-  return *reinterpret_cast<const uint32_t *>(&r);
-}
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-// silu(v) = v / (1 + e^-v), with the SFU exponential and reciprocal (relative
-// error ~2^-21, far below the output tolerance).
-__device__ __forceinline__ float silu(float g) { return g * __frcp_rn(1.f + __expf(-g)); }
-
-// Power of two 2^s with amax * 2^s in [2^14, 2^15) (s clamped to +-120);
-// returns 2^s and writes 2^-s.
-__device__ __forceinline__ float f16_range_scale(float amax, float *inv) {
-  int s = 0;
-  if (amax > 0.f) s = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127);
-  s = max(-120, min(120, s));
-  *inv = __uint_as_float((uint32_t)(127 - s) << 23);
-  return __uint_as_float((uint32_t)(127 + s) << 23);
-}
-
-// Position of element k of an h vector in hbuf: each 16-element block is
-// stored in the order the down kernel's B operand reads it, so that lane
-// (g, q) finds elements 2q, 2q+1, 2q+8, 2q+9 of a k-step as one float4.
-__device__ __forceinline__ int operand_order(int k) {
-  const int r = k & 15;
-  return (k & ~15) + 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
-}
-
-// ---------------------------------------------------------------- dispatch
-// Distinct selected experts of this token group in ascending id order, with
-// for each the tokens that chose it (mask, and the (token, slot) pair index
-// p = t*k + slot both by token and in ascending token order).  Ids outside
-// [0,E) are flagged and skipped; an id repeated inside a token is flagged and
-// only its lowest slot is used (the combine kernel applies the same rule).
-__device__ void build_dispatch(DispatchSmem &s, const int32_t *ids, const float *weights,
-                               const float *scalars, int C, int k, int E, int32_t *flags) {
-  const int tid = threadIdx.x, nt = blockDim.x, P = C * k;
-  for (int i = tid; i < kMaxExperts / 32; i += nt) s.bitmap[i] = 0u;
-  for (int i = tid; i < P; i += nt) s.tokmask[i] = 0u;
-  for (int i = tid; i < P * kGemvTokens; i += nt) (&s.pair[0][0])[i] = 0x7FFFFFFF;
-  __syncthreads();
-  for (int p = tid; p < P; p += nt) {
-    const int e = ids[p];
-    if ((unsigned)e < (unsigned)E)
-      atomicOr(&s.bitmap[e >> 5], 1u << (e & 31));
-    else
-      atomicOr(flags, MOE_FLAG_BAD_EXPERT_ID);
-  }
-  __syncthreads();
-  if (tid < 32) {
-    const int c = __popc(s.bitmap[tid]);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(kFull, incl, o);
-      if (tid >= o) incl += v;
-    }
-    s.base[tid] = incl - c;
-    if (tid == 31) s.n = incl;
-  }
-  __syncthreads();
-  for (int p = tid; p < P; p += nt) {
-    const int e = ids[p];
-    if ((unsigned)e >= (unsigned)E) continue;
-    const int w = e >> 5;
-    const int r = s.base[w] + __popc(s.bitmap[w] & ((1u << (e & 31)) - 1u));
-    const int t = p / k;
-    const uint32_t old = atomicOr(&s.tokmask[r], 1u << t);
-    if ((old >> t) & 1u) atomicOr(flags, MOE_FLAG_DUPLICATE_ID);
-    atomicMin(&s.pair[r][t], p);
-    s.expert[r] = (int16_t)e;
-  }
-  __syncthreads();
-  for (int p = tid; p < P; p += nt) s.wt[p] = weights[p];
-  for (int r = tid; r < s.n; r += nt) {
-    const float *sc = scalars + (size_t)s.expert[r] * 6;
-    s.scal[r][0] = sc[0];
-    s.scal[r][1] = sc[2];
-    s.scal[r][2] = sc[4];
-    uint32_t m = s.tokmask[r];
-    int j = 0;
-    while (m) {
-      const int t = __ffs(m) - 1;
-      m &= m - 1u;
-      s.slot_pair[r][j++] = (int16_t)s.pair[r][t];
-    }
-    s.nslot[r] = (uint8_t)j;
-  }
-  __syncthreads();
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
@@ -275,47 +95,17 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   uint32_t bf[kWarpSteps][2];
   float colinv0 = 1.f, colinv1 = 1.f;           // 2^-s of accumulator columns 2q, 2q+1
   if constexpr (MODE == 0) {
-    if (is_consumer) {
-      float am = 0.f;
-      const bool tok = g < a.C;
-      const uint16_t *xr = a.x + (size_t)(tok ? g : 0) * a.H;
-#pragma unroll
-      for (int s = 0; s < kWarpSteps; s++) {
-        const int k0 = 16 * (ks0 + s) + 2 * q;
-        uint32_t v0 = 0, v1 = 0;
-        if (tok && k0 < K) {
-          v0 = *reinterpret_cast<const uint32_t *>(xr + k0);
-          v1 = *reinterpret_cast<const uint32_t *>(xr + k0 + 8);
-        }
-        bf[s][0] = v0;
-        bf[s][1] = v1;
-        am = fmaxf(am, fmaxf(fmaxf(fabsf(__uint_as_float(v0 << 16)), fabsf(__uint_as_float(v0 & 0xFFFF0000u))),
-                             fmaxf(fabsf(__uint_as_float(v1 << 16)), fabsf(__uint_as_float(v1 & 0xFFFF0000u)))));
-      }
-      am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
-      am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
-      float inv;
-      const float up = f16_range_scale(am, &inv);
-#pragma unroll
-      for (int s = 0; s < kWarpSteps; s++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-          const uint32_t v = bf[s][h];
-          bf[s][h] = pack_half2(__uint_as_float(v << 16) * up, __uint_as_float(v & 0xFFFF0000u) * up);
-        }
-      colinv0 = __shfl_sync(kFull, inv, (2 * q) * 4);
-      colinv1 = __shfl_sync(kFull, inv, (2 * q + 1) * 4);
-    }
+    if (is_consumer) build_x_fragments(a.x, a.C, a.H, ks0, bf, colinv0, colinv1);
   }
 
   if constexpr (MODE == 0) pdl_wait();           // ids/weights come from the router
-  build_dispatch(ds, a.ids, a.weights, a.scalars, a.C, a.k, a.E, a.flags);
+  build_dispatch(ds, a.ids, a.weights, a.C, a.k, a.E, a.flags);
   pdl_launch_dependents();
 
   const int n = ds.n;
-  const long long T = (long long)n * a.tiles;
-  const long long t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
-  const int nstage = (int)(t1 - t0);
+  const int T = n * a.tiles;
+  const int t0 = split_point(T, blockIdx.x, gridDim.x), t1 = split_point(T, blockIdx.x + 1, gridDim.x);
+  const int nstage = t1 - t0;
 
   if (is_producer) {
     // ------------------------------------------------ producer: bulk copies
@@ -323,7 +113,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       const uint64_t pol = l2_evict_first_policy();
       int i = 0;
       bool ok = true;
-      int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
+      int d = t0 / a.tiles, tile = t0 - d * a.tiles;
       for (; i < nstage; i++, tile++) {
         if (tile == a.tiles) { tile = 0; d++; }
         const int slot = i % S;
@@ -351,9 +141,10 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   // down kernel makes one pass per 4 token slots of the tile's expert.
   if (is_epilogue) {
     // ------------------------------------------------ epilogue warp
+    // (expert rank, tile) of stage i, advanced incrementally
+    int d = t0 / a.tiles, tile = t0 - d * a.tiles;
+    if (nstage > 0) load_dispatch_scales(ds, a.scalars, d, (t1 - 1) / a.tiles + 1);
     if constexpr (MODE == 1) pdl_wait();
-    // (expert rank, tile) of stage i, advanced incrementally (no 64-bit division)
-    int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
     // gate/up: running max |h| of tokens 2q, 2q+1 for expert rank d, merged
     // into hamax when d changes and at the end
     float hm0 = 0.f, hm1 = 0.f;
@@ -434,7 +225,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   // ---------------------------------------------------- consumers
   if constexpr (MODE == 1) pdl_wait();           // hbuf comes from the gate/up kernel
   int cur_key = -1;                              // (expert rank, pass) of bf
-  int d = (int)(t0 / a.tiles), tile = (int)(t0 - (long long)d * a.tiles);
+  int d = t0 / a.tiles, tile = t0 - d * a.tiles;
   int item = 0;
   bool ok = true;
   for (int i = 0; i < nstage && ok; i++) {
@@ -459,67 +250,14 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       if constexpr (MODE == 1) {
         const int key = d * 2 + pass;
         if (key != cur_key) {
-          // B fragments of h: column g = slot 4*pass + g/2, hi (g even) / lo
-          // (g odd) f16 part of h * 2^s, with 2^s set by the slot's max |h|.
-          // Lane (g, q) reads the four values of each k-step it needs as one
-          // float4 (hbuf keeps every 16-element block in operand order).
           cur_key = key;
           const int sl = 4 * pass + (g >> 1);
-          const bool have = sl < ds.nslot[d];
-          const int pr = have ? ds.slot_pair[d][sl] : 0;
-          const float4 *hr4 = reinterpret_cast<const float4 *>(a.hbuf + (size_t)pr * a.I) + q;
-          const float am = have ? __uint_as_float(__ldcg(a.hamax + pr)) : 0.f;
-          float inv;
-          const float up = f16_range_scale(am, &inv);
-          const bool lo = (g & 1) != 0;
-#pragma unroll
-          for (int s = 0; s < kWarpSteps; s++) {
-            const int ks = ks0 + s;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (have && 16 * ks < K) v = __ldcg(hr4 + 4 * ks);
-            const float x0 = v.x * up, x1 = v.y * up, x2 = v.z * up, x3 = v.w * up;
-            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-            if (lo) {
-              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-              bf[s][0] = pack_half2(x0 - f01.x, x1 - f01.y);
-              bf[s][1] = pack_half2(x2 - f23.x, x3 - f23.y);
-            } else {
-              bf[s][0] = *reinterpret_cast<const uint32_t *>(&h01);
-              bf[s][1] = *reinterpret_cast<const uint32_t *>(&h23);
-            }
-          }
-          // columns 2q (hi) and 2q+1 (lo) of this lane belong to slot q
-          colinv0 = colinv1 = __shfl_sync(kFull, inv, (2 * q) * 4);
+          colinv0 = colinv1 = build_h_fragments(a.hbuf, a.hamax, a.I, ks0, sl < ds.nslot[d] ? ds.slot_pair[d][sl] : -1, bf);
         }
       }
 
-      // four independent accumulator chains (k-step s feeds chain s % 4) so
-      // consecutive MMAs of a warp do not wait on each other's results
-      float acc4[4][4] = {};
-      uint4 sc = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int qg = 0; qg < kWarpSteps / 4; qg++) {
-        const uint4 cw = *reinterpret_cast<const uint4 *>(codes + ((size_t)qg * 32 + lane) * 16);
-        if ((qg & 1) == 0) sc = *reinterpret_cast<const uint4 *>(scales + ((size_t)(qg >> 1) * 8 + g) * 16);
-        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-        const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-          const int s = 4 * qg + jj;
-          const int ks = (qg & 1) * 4 + jj;              // k-step inside the 8-step scale unit
-          const uint32_t s2 = e4m3x2_to_f16x2(scs[ks >> 1] >> (16 * (ks & 1)));
-          uint32_t A[4];
-          e2m1x8_to_f16x2(cws[jj], A);
-          A[0] = hmul2_lo(A[0], s2);
-          A[1] = hmul2_hi(A[1], s2);
-          A[2] = hmul2_lo(A[2], s2);
-          A[3] = hmul2_hi(A[3], s2);
-          mma16816(acc4[jj], A, bf[s][0], bf[s][1]);
-        }
-      }
       float acc[4];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; c4++) acc[c4] = (acc4[0][c4] + acc4[1][c4]) + (acc4[2][c4] + acc4[3][c4]);
+      mma_half_slice(codes, scales, bf, acc);
       red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
           make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
       __syncwarp();

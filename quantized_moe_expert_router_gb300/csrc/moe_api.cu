@@ -244,6 +244,17 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
   return cuda_status(err);
 }
 
+moe_status moe_route_forward(moe_layer_t L, const uint16_t *x, int C, const float *w_router,
+                             const float *bias, const void *packed, int32_t *ids, float *weights, float *y,
+                             void *ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!L || !x || !w_router || !packed || !ids || !weights || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (C < 1 || C > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  const moe_status st = moe_route(L, x, C, w_router, bias, ids, weights, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  return moe_forward(L, x, C, ids, weights, packed, y, ws, ws_bytes, stream);
+}
+
 moe_status moe_get_device_status(moe_layer_t L, void *ws, cudaStream_t stream, int32_t *flags) {
   if (!L || !ws || !flags) return MOE_ERR_INVALID_ARG;
   DeviceGuard guard(L->device);

@@ -21,7 +21,7 @@ constexpr int kGemvTokens = 8;           // tokens per GEMV group (token mask bi
 constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
-constexpr int kGemvSmemBytes = 212992;   // dynamic shared memory of one expert-GEMV CTA (+ ~19 KB static)
+constexpr int kGemvSmemBytes = 211968;   // dynamic shared memory of one expert-GEMV CTA (+ ~20 KB static)
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
 
 // Workspace control block (first 256 bytes of the workspace).
@@ -154,6 +154,13 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
            rc = *reinterpret_cast<uint64_t *>(&c), rd;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
   return *reinterpret_cast<float2 *>(&rd);
+}
+
+// Start of part `part` of `parts` equal contiguous parts of [0, total), in
+// 32-bit arithmetic (total * parts < 2^32 for every use here: the 64-bit
+// division is a long software routine that every thread would run).
+__device__ __forceinline__ int split_point(int total, int part, int parts) {
+  return (int)(((uint32_t)total * (uint32_t)part) / (uint32_t)parts);
 }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -43,11 +43,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t row_bytes = (size_t)a.H * sizeof(float);
   float4 *rows4 = xs4 + (size_t)CT * H4;
-  const int max_rows = (int)((kRouteSmemBytes - (size_t)CT * row_bytes) / row_bytes);
+  const int max_rows = (kRouteSmemBytes - CT * a.H * (int)sizeof(float)) / (a.H * (int)sizeof(float));
   // this CTA's router rows: a contiguous range, streamed into shared memory
   // with bulk copies in rounds of at most max_rows rows
-  const int r0 = (int)((long long)a.E * blockIdx.x / gridDim.x);
-  const int r1 = (int)((long long)a.E * (blockIdx.x + 1) / gridDim.x);
+  const int r0 = split_point(a.E, blockIdx.x, gridDim.x), r1 = split_point(a.E, blockIdx.x + 1, gridDim.x);
   const uint64_t pol = l2_evict_first_policy();
   if (threadIdx.x == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rows_bar)) : "memory");

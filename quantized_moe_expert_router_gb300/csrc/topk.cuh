@@ -175,30 +175,29 @@ __device__ __forceinline__ void cta_select_topk(const float *lg, int E, int k, i
   }
   __syncthreads();
   // (4) output by warp 0: lane l takes candidates l, l + 32, ...; slot = kept
-  // candidates before it (ascending id); the denominator is summed by a fixed
-  // shuffle tree, so every CTA computes bitwise identical weights
+  // candidates before it (ascending id).  The denominator is summed over the
+  // slots by a fixed shuffle tree, so the weights do not depend on how the
+  // candidates were found (bitwise identical in every CTA and for any NT).
   if (warp == 0) {
     const float lmax = key_value(kmax);
     const int nwords = (int)((ncand + 31) >> 5);
     uint32_t before = 0;
-    float part_sum = 0.f;
     for (int w = 0; w < nwords; w++) {
       const uint32_t bits = s.kept[w];
       if ((bits >> lane) & 1u) {
         const unsigned long long me = s.cand[32 * w + lane];
-        const float ex = expf(key_value((uint32_t)(me >> 32)) - lmax);
         const uint32_t slot = before + __popc(bits & ((1u << lane) - 1u));
         ids_out[slot] = kMaxExperts - 1 - (int)(uint32_t)(me & 0xFFFFFFFFull);
-        s.exs[slot] = ex;
-        part_sum += ex;
+        s.exs[slot] = expf(key_value((uint32_t)(me >> 32)) - lmax);
       }
       before += __popc(bits);
     }
-    float denom = part_sum;
+    __syncwarp();
+    const float ex = lane < k ? s.exs[lane] : 0.f;
+    float denom = ex;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(kAll, denom, o);
-    __syncwarp();
-    if (lane < k) w_out[lane] = s.exs[lane] / denom;
+    if (lane < k) w_out[lane] = ex / denom;
   }
   __syncthreads();                               // s is reused by the next call
 }

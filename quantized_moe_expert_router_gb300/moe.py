@@ -30,7 +30,7 @@ FLAG_TIMEOUT = 0x4
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",
     "moe_pack_weights", "moe_route", "moe_forward", "moe_get_device_status",
-    "moe_set_stage_events", "moe_route_noalloc", "moe_status_string",
+    "moe_set_stage_events", "moe_route_noalloc", "moe_route_forward", "moe_status_string",
 )
 
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH):
             lib.moe_get_device_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_set_stage_events.argtypes = [P, P, I32]
             lib.moe_route_noalloc.argtypes = [P, P, I32, P, P, P, P, P]
+            lib.moe_route_forward.argtypes = [P, P, I32, P, P, P, P, P, P, P, SZ, P]
             lib.moe_status_string.argtypes = [I32]
             lib.moe_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -167,6 +168,13 @@ def moe_forward(layer, x, num_tokens, ids, weights, packed, y, ws, stream=None) 
     _check("moe_forward", load_library().moe_forward(
         layer.handle, _ptr(x), num_tokens, _ptr(ids), _ptr(weights), _ptr(packed), _ptr(y),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_forward(layer, x, num_tokens, w_router, bias, packed, ids, weights, y, ws, stream=None) -> None:
+    """The whole layer: routing then the routed experts (ids/weights written)."""
+    _check("moe_route_forward", load_library().moe_route_forward(
+        layer.handle, _ptr(x), num_tokens, _ptr(w_router), _ptr(bias), _ptr(packed), _ptr(ids),
+        _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_route_noalloc(layer, x, num_tokens, w_router, bias, ids, weights, stream=None) -> None:

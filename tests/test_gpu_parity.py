@@ -63,6 +63,17 @@ class GpuLayer:
         torch.cuda.synchronize()
         return ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
 
+    def run_fused(self, x_bits):
+        """The whole layer in one call (moe_route_forward)."""
+        C = x_bits.shape[0]
+        x = torch.from_numpy(x_bits.view(np.int16)).to(DEV)
+        ids = torch.empty((C, self.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((C, self.k), dtype=torch.float32, device=DEV)
+        y = torch.empty((C, self.H), dtype=torch.float32, device=DEV)
+        moe.moe_route_forward(self.h, x, C, self.Wr_d, self.bias_d, self.packed, ids, w, y, self.ws)
+        torch.cuda.synchronize()
+        return ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+
     def oracle(self, x_bits):
         """Oracle routing + forward on the selected experts only."""
         logits = oracle.router_logits(self.Wr, x_bits, self.bias)
@@ -73,8 +84,8 @@ class GpuLayer:
         return ids, w, gap, y
 
 
-def check_layer(L, x_bits, label):
-    ids, w, y = L.run(x_bits)
+def check_layer(L, x_bits, label, fused=False):
+    ids, w, y = (L.run_fused if fused else L.run)(x_bits)
     oids, ow, gap, oy = L.oracle(x_bits)
     assert (gap >= MIN_GAP).all()
     assert (ids == oids).all(), f"{label}: ids differ\n{ids}\n{oids}"
@@ -189,6 +200,27 @@ def test_odd_shapes_parity(E, k, H, I, C):
     check_layer(L, x, f"E{E} k{k} H{H} I{I} C{C}")
 
 
+@pytest.mark.parametrize("C", [1, 3, 8, 11])
+def test_route_forward_equals_route_then_forward(C):
+    # the one-call layer gives the separate calls' results bit for bit, call
+    # after call
+    L = GpuLayer(32, 4, 256, 192, 16)
+    for rep in range(3):
+        x = gapped_tokens(rep, 0, C, 256, L.Wr, 4)
+        ids, w, y = L.run(x)
+        ids2, w2, y2 = L.run_fused(x)
+        assert (ids == ids2).all() and (w == w2).all() and (y == y2).all(), f"C={C} call {rep}"
+        assert moe.moe_get_device_status(L.h, L.ws) == 0
+    check_layer(L, x, f"fused tiny C={C}", fused=True)
+
+
+@pytest.mark.parametrize("E,k,H,I,C", [(12, 3, 64, 128, 5), (7, 7, 192, 1088, 1), (200, 32, 4096, 64, 8)])
+def test_route_forward_odd_shapes(E, k, H, I, C):
+    L = GpuLayer(E, k, H, I, C, seed=5)
+    x = gapped_tokens(5, 0, C, H, L.Wr, k)
+    check_layer(L, x, f"fused E{E} k{k} H{H} I{I} C{C}", fused=True)
+
+
 def test_forward_is_deterministic():
     L = GpuLayer(32, 4, 256, 192, 8)
     x = gapped_tokens(0, 0, 8, 256, L.Wr, 4)
@@ -289,6 +321,7 @@ def test_k3_decode_batch1_parity(k3_layer):
     L = k3_layer
     x = gapped_tokens(0, 0, 1, 3584, L.Wr, 16)
     check_layer(L, x, "k3 C=1 top-16")
+    check_layer(L, x, "k3 C=1 top-16 fused", fused=True)
 
 
 @pytest.mark.parametrize("k", [8, 16])
@@ -299,6 +332,7 @@ def test_k3_decode_batch7_parity(k3_layer, k):
         L = _retarget(k3_layer, h, k)
     x = gapped_tokens(1, 0, 7, 3584, L.Wr, k)
     check_layer(L, x, f"k3 C=7 top-{k}")
+    check_layer(L, x, f"k3 C=7 top-{k} fused", fused=True)
 
 
 def _retarget(L, h, k):
@@ -310,6 +344,7 @@ def _retarget(L, h, k):
     v.h, v.k = h, k
     v.ws = moe.alloc_workspace(h, 8)
     v.run = GpuLayer.run.__get__(v)
+    v.run_fused = GpuLayer.run_fused.__get__(v)
     v.oracle = GpuLayer.oracle.__get__(v)
     v.host_weights = GpuLayer.host_weights.__get__(v)
     return v
