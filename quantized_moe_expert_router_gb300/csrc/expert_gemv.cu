@@ -57,6 +57,8 @@
 
 namespace moe {
 
+constexpr int kDnTilesPerStage = 2;             // down projection: two tiles of 8 pair rows per stage
+
 template <int MODE>
 __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];   // [S][stage_bytes] then the reduction slots
@@ -179,16 +181,13 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
           ok = false;
           break;
         }
-        const float4 *pr4 = red + (size_t)rs * red_slot_f4 + lane;
-        float4 sum = pr4[0];
-#pragma unroll
-        for (int ww = 1; ww < kMaxKWarps; ww++) {
-          if (ww < W) {
+        if constexpr (MODE == 0) {
+          const float4 *pr4 = red + (size_t)rs * red_slot_f4 + lane;
+          float4 sum = pr4[0];
+          for (int ww = 1; ww < W; ww++) {
             const float4 v = pr4[ww * 32];
             sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
           }
-        }
-        if constexpr (MODE == 0) {
           const uint32_t mask = ds.tokmask[d];
           float *hrow = a.hbuf + operand_order(tile * 8 + g);
 #pragma unroll
@@ -204,11 +203,20 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
             }
           }
         } else {
+          const float2 *pr2 = reinterpret_cast<const float2 *>(red + (size_t)rs * red_slot_f4) + lane;
           const int sl = 4 * pass + q;
-          if (sl < ds.nslot[d]) {
-            const float gd = ds.scal[d][2];
-            *reinterpret_cast<float2 *>(a.ypair + (size_t)ds.slot_pair[d][sl] * a.H + 2 * (tile * 8 + g)) =
-                make_float2((sum.x + sum.y) * gd, (sum.z + sum.w) * gd);
+          const float gd = ds.scal[d][2];
+#pragma unroll
+          for (int tt = 0; tt < kDnTilesPerStage; tt++) {
+            float2 sum = pr2[(size_t)tt * W * 32];
+            for (int ww = 1; ww < W; ww++) {
+              const float2 v = pr2[(size_t)(tt * W + ww) * 32];
+              sum.x += v.x; sum.y += v.y;
+            }
+            if (sl < ds.nslot[d])
+              *reinterpret_cast<float2 *>(a.ypair + (size_t)ds.slot_pair[d][sl] * a.H +
+                                          2 * ((tile * kDnTilesPerStage + tt) * 8 + g)) =
+                  make_float2(sum.x * gd, sum.y * gd);
           }
         }
         __syncwarp();
@@ -256,10 +264,21 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         }
       }
 
-      float acc[4];
-      mma_half_slice(codes, scales, bf, acc);
-      red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
-          make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
+      if constexpr (MODE == 0) {
+        float acc[4];
+        mma_half_slice(codes, scales, bf, acc);
+        red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
+            make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
+      } else {
+        // two tiles per stage; the hi and lo columns of a slot are added here
+        // (both carry the slot's 2^-s), so a partial is one float2 per tile
+        const int tb = a.tile_bytes / kDnTilesPerStage;
+        float accA[4], accB[4];
+        mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        float2 *r2 = reinterpret_cast<float2 *>(red + (size_t)rs * red_slot_f4);
+        r2[(size_t)warp * 32 + lane] = make_float2((accA[0] + accA[1]) * colinv0, (accA[2] + accA[3]) * colinv0);
+        r2[(size_t)(W + warp) * 32 + lane] = make_float2((accB[0] + accB[1]) * colinv0, (accB[2] + accB[3]) * colinv0);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[rs]);     // this warp's partials are in the reduction slot
     }
@@ -271,8 +290,8 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
 
 // ------------------------------------------------------------------ host side
 // Ring geometry: as many tile stages as fit beside the reduction slots.
-void gemv_geometry(int slices, int *stages, int *stage_bytes, int *smem_bytes) {
-  const int tile = slices * kTileSliceBytes;
+void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes) {
+  const int tile = tiles_per_stage * slices * kTileSliceBytes;
   const int red = kRedSlots * 2 * slices * 32 * (int)sizeof(float4);
   int s = (kGemvSmemBytes - red) / tile;
   if (s > kMaxStages) s = kMaxStages;

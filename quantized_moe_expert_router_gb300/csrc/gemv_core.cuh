@@ -315,4 +315,46 @@ __device__ __forceinline__ void mma_half_slice(const uint8_t *codes, const uint8
   for (int c4 = 0; c4 < 4; c4++) acc[c4] = (acc4[0][c4] + acc4[1][c4]) + (acc4[2][c4] + acc4[3][c4]);
 }
 
+// The same step for two tiles that share the B fragments (the down
+// projection stages two tiles at a time): per k-step both tiles' 16x16
+// weight blocks are decoded and multiplied, two accumulator chains per tile.
+// accA/accB = each tile's chains summed.
+__device__ __forceinline__ void mma_half_slice_x2(const uint8_t *codesA, const uint8_t *scalesA, const uint8_t *codesB,
+                                                  const uint8_t *scalesB, const uint32_t (&bf)[kWarpSteps][2],
+                                                  float (&accA)[4], float (&accB)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  float ca[2][4] = {}, cb[2][4] = {};
+  uint4 sa = make_uint4(0, 0, 0, 0), sb = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int qg = 0; qg < kWarpSteps / 4; qg++) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(codesA + ((size_t)qg * 32 + lane) * 16);
+    const uint4 wb = *reinterpret_cast<const uint4 *>(codesB + ((size_t)qg * 32 + lane) * 16);
+    if ((qg & 1) == 0) {
+      sa = *reinterpret_cast<const uint4 *>(scalesA + ((size_t)(qg >> 1) * 8 + g) * 16);
+      sb = *reinterpret_cast<const uint4 *>(scalesB + ((size_t)(qg >> 1) * 8 + g) * 16);
+    }
+    const uint32_t was[4] = {wa.x, wa.y, wa.z, wa.w}, wbs[4] = {wb.x, wb.y, wb.z, wb.w};
+    const uint32_t sas[4] = {sa.x, sa.y, sa.z, sa.w}, sbs[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++) {
+      const int s = 4 * qg + jj;
+      const int ks = (qg & 1) * 4 + jj;
+      const uint32_t s2a = e4m3x2_to_f16x2(sas[ks >> 1] >> (16 * (ks & 1)));
+      const uint32_t s2b = e4m3x2_to_f16x2(sbs[ks >> 1] >> (16 * (ks & 1)));
+      uint32_t A[4], B[4];
+      e2m1x8_to_f16x2(was[jj], A);
+      e2m1x8_to_f16x2(wbs[jj], B);
+      A[0] = hmul2_lo(A[0], s2a); A[1] = hmul2_hi(A[1], s2a); A[2] = hmul2_lo(A[2], s2a); A[3] = hmul2_hi(A[3], s2a);
+      B[0] = hmul2_lo(B[0], s2b); B[1] = hmul2_hi(B[1], s2b); B[2] = hmul2_lo(B[2], s2b); B[3] = hmul2_hi(B[3], s2b);
+      mma16816(ca[jj & 1], A, bf[s][0], bf[s][1]);
+      mma16816(cb[jj & 1], B, bf[s][0], bf[s][1]);
+    }
+  }
+#pragma unroll
+  for (int c4 = 0; c4 < 4; c4++) {
+    accA[c4] = ca[0][c4] + ca[1][c4];
+    accB[c4] = cb[0][c4] + cb[1][c4];
+  }
+}
+
 }  // namespace moe

@@ -48,15 +48,15 @@ struct GemvArgs {
   int C, k, E, H, I;
   size_t expert_bytes;
   size_t region_off;         // 0 (gate/up) or the down region offset
-  int tiles;                 // tiles per expert: I/8 (gate/up) or H/16 (down)
-  int tile_bytes;            // slices * kTileSliceBytes
+  int tiles;                 // stage units per expert: I/8 tiles (gate/up) or H/32 tile pairs (down)
+  int tile_bytes;            // bytes of one stage unit: one tile (gate/up) or two (down) of slices * kTileSliceBytes
   int slices;                // 512-element K-slices per tile (padded K / 512); 2 consumer warps each
   int stages;                // shared-memory ring stages
-  int stage_bytes;           // bytes of one ring stage (one tile)
+  int stage_bytes;           // bytes of one ring stage (one stage unit)
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
 };
 // Ring geometry and dynamic shared memory of one kernel.
-void gemv_geometry(int slices, int *stages, int *stage_bytes, int *smem_bytes);
+void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes);
 // Opt-in shared memory of the expert kernels (once per device; idempotent).
 cudaError_t gemv_setup();
 // mode 0: gate/up + SwiGLU -> hbuf; mode 1: down -> ypair -> combine -> y.
