@@ -14,21 +14,25 @@
 // Work split.  The selected experts are de-duplicated in every CTA (a bitmap
 // over expert ids; popcount ranks give ascending expert order), so each
 // expert's bytes are streamed once whatever number of tokens chose it.  The
-// flattened list (distinct expert, tile of 8 pair rows) is cut into equal
-// contiguous ranges, one CTA per SM, so every SM streams the same bytes to
-// within one tile.  Tiles are contiguous in the packed layout (pack.cu).
+// flattened list of (distinct expert, stage unit) is cut into equal contiguous
+// ranges, one CTA per SM, so every SM streams the same bytes to within one
+// unit.  A stage unit is one tile of 8 pair rows (gate/up) or two consecutive
+// tiles (down: the smaller tiles need twice the work per synchronisation);
+// tiles are contiguous in the packed layout (pack.cu).
 //
 // Streaming.  The CTA is warp-specialised and its warps never meet at a
-// CTA-wide barrier after the dispatch: one producer lane copies each tile with
-// one bulk copy (cp.async.bulk, global -> shared, completion counted on an
-// mbarrier) into a ring of S stage buffers, up to S tiles ahead.  The W
-// consumer warps all work on the same tile, each on its own 256-element
-// K range (16 k-steps: half of one of the tile's 512-element slices), and hand
-// their partials to one epilogue warp through a ring of reduction slots, also
-// tracked by mbarriers (one item per tile and token pass).  Every wait is
-// bounded (about two seconds of %globaltimer): on expiry the waiting warp sets
-// MOE_FLAG_TIMEOUT and leaves, and the producer waits (bounded) for its copies
-// still in flight before exiting.
+// CTA-wide barrier after the dispatch: one producer lane copies each stage
+// unit with one bulk copy (cp.async.bulk, global -> shared, completion counted
+// on an mbarrier) into a ring of S stage buffers, up to S units ahead.  The W
+// consumer warps all work on the same unit, each on its own 256-element K
+// range (16 k-steps: half of one of the tile's 512-element slices), write
+// their partials into the reduction slots that belong to the stage buffer and
+// arrive on the stage's "reduced" mbarrier; the epilogue warp sums them and
+// only then releases the stage buffer to the producer, so a consumer waits on
+// nothing but the arrival of its data.  Every wait is bounded (about two
+// seconds of %globaltimer): on expiry the waiting warp sets MOE_FLAG_TIMEOUT
+// and leaves, and the producer waits (bounded) for its copies still in flight
+// before exiting.
 //
 // Compute.  Decoding stays in registers: per k-step a lane converts its 4
 // code bytes with cvt.rn.f16x2.e2m1x2 and multiplies them by the row's e4m3
@@ -65,11 +69,12 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   __shared__ DispatchSmem ds;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t red_full[kRedSlots];
-  __shared__ __align__(8) uint64_t red_empty[kRedSlots];
+  __shared__ __align__(8) uint64_t red_full[kMaxStages];
 
   const int NS = a.slices, W = 2 * NS, S = a.stages;
-  // reduction slots [kRedSlots][W][32 lanes] of float4, after the ring
+  // reduction slots after the ring: [S stages][NP passes][W warps][32 lanes]
+  // of float4 (down: two float2, one per tile of the stage)
+  constexpr int NP = MODE == 0 ? 1 : 2;     // passes per stage: down makes one per 4 token slots, C <= 8
   float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);
   const int red_slot_f4 = W * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -79,16 +84,12 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   const int slice = warp >> 1, half = warp & 1;  // consumer: k-steps 32*slice + 16*half + [0, 16)
   const int ks0 = kSliceSteps * slice + kWarpSteps * half;
   const int g = lane >> 2, q = lane & 3;
-  const int K = MODE == 0 ? a.H : a.I;          // real K of this region's rows
 
   if (tid == 32 * W) {
     for (int s = 0; s < S; s++) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], W);
-    }
-    for (int s = 0; s < kRedSlots; s++) {
+      mbar_init(&empty_bar[s], 1);
       mbar_init(&red_full[s], W);
-      mbar_init(&red_empty[s], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -174,13 +175,14 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         }
       }
       const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
+      const int eslot = i % S;
+      if (!mbar_wait_bounded(&red_full[eslot], (uint32_t)(i / S) & 1u)) {
+        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+        ok = false;
+        break;
+      }
       for (int pass = 0; pass < npass; pass++, item++) {
-        const int rs = item % kRedSlots;
-        if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(item / kRedSlots) & 1u)) {
-          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-          ok = false;
-          break;
-        }
+        const int rs = eslot * NP + pass;
         if constexpr (MODE == 0) {
           const float4 *pr4 = red + (size_t)rs * red_slot_f4 + lane;
           float4 sum = pr4[0];
@@ -219,9 +221,9 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
                   make_float2(sum.x * gd, sum.y * gd);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&red_empty[rs]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[eslot]);   // ring stage and its reduction slots are free
       if (++tile == a.tiles) { tile = 0; d++; }
     }
     if constexpr (MODE == 0) {
@@ -248,13 +250,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         ring + (size_t)slot * a.stage_bytes + (size_t)NS * 4096 + (size_t)slice * 512 + (size_t)half * 256;
 
     for (int pass = 0; pass < npass; pass++, item++) {
-      const int rs = item % kRedSlots;
-      const uint32_t ruse = (uint32_t)(item / kRedSlots);
-      if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
-        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-        ok = false;
-        break;
-      }
+      const int rs = slot * NP + pass;
       if constexpr (MODE == 1) {
         const int key = d * 2 + pass;
         if (key != cur_key) {
@@ -279,26 +275,24 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         r2[(size_t)warp * 32 + lane] = make_float2((accA[0] + accA[1]) * colinv0, (accA[2] + accA[3]) * colinv0);
         r2[(size_t)(W + warp) * 32 + lane] = make_float2((accB[0] + accB[1]) * colinv0, (accB[2] + accB[3]) * colinv0);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_full[rs]);     // this warp's partials are in the reduction slot
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[slot]);    // stage buffer may be refilled
+    if (lane == 0) mbar_arrive(&red_full[slot]);     // this warp's partials of the stage are written
     if (++tile == a.tiles) { tile = 0; d++; }
   }
 }
 
 // ------------------------------------------------------------------ host side
 // Ring geometry: as many tile stages as fit beside the reduction slots.
-void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes) {
+void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes, int passes) {
   const int tile = tiles_per_stage * slices * kTileSliceBytes;
-  const int red = kRedSlots * 2 * slices * 32 * (int)sizeof(float4);
-  int s = (kGemvSmemBytes - red) / tile;
+  const int red1 = passes * 2 * slices * 32 * (int)sizeof(float4);
+  int s = kGemvSmemBytes / (tile + red1);   // stage buffer + its reduction slots
   if (s > kMaxStages) s = kMaxStages;
   if (s < 2) s = 2;
   *stage_bytes = tile;
   *stages = s;
-  *smem_bytes = s * tile + red;
+  *smem_bytes = s * (tile + red1);
 }
 
 template <int MODE>

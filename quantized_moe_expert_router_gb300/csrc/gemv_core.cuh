@@ -14,7 +14,6 @@ constexpr int kSliceSteps = 32;                  // k-steps of one 512-element K
 constexpr int kWarpSteps = 16;                   // k-steps per consumer warp (half a slice)
 constexpr int kMaxKWarps = 16;                   // consumer warps: K <= 4096
 constexpr int kMaxCtaThreads = 32 * (kMaxKWarps + 2);   // + producer and epilogue warps
-constexpr int kRedSlots = 4;                     // consumer -> epilogue reduction ring
 constexpr int kMaxStages = 8;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

@@ -56,7 +56,7 @@ struct GemvArgs {
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
 };
 // Ring geometry and dynamic shared memory of one kernel.
-void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes);
+void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes, int passes);
 // Opt-in shared memory of the expert kernels (once per device; idempotent).
 cudaError_t gemv_setup();
 // mode 0: gate/up + SwiGLU -> hbuf; mode 1: down -> ypair -> combine -> y.

@@ -221,7 +221,7 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.tiles = I / 8;
     a.tile_bytes = (int)L->gu_tile_bytes;
     a.slices = L->w_gu;
-    moe::gemv_geometry(a.slices, 1, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    moe::gemv_geometry(a.slices, 1, &a.stages, &a.stage_bytes, &a.smem_bytes, 1);
     err = moe::launch_expert_gemv(0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
@@ -231,7 +231,7 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.tiles = H / 32;                         // stage units of two tiles of 8 pair rows (H % 64 == 0)
     a.tile_bytes = 2 * (int)L->dn_tile_bytes;
     a.slices = L->w_dn;
-    moe::gemv_geometry(a.slices, 2, &a.stages, &a.stage_bytes, &a.smem_bytes);
+    moe::gemv_geometry(a.slices, 2, &a.stages, &a.stage_bytes, &a.smem_bytes, 2);
     err = moe::launch_expert_gemv(1, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     // weighted sum over each token's experts, ascending expert id
