@@ -63,8 +63,13 @@ namespace moe {
 
 constexpr int kDnTilesPerStage = 2;             // down projection: two tiles of 8 pair rows per stage
 
+// MODE 0: gate/up, one tile per stage; MODE 2: gate/up, two tiles per stage
+// (decode groups of at most 2 tokens: their partials are 1/4 of a warp's
+// accumulators, so a stage's reduction slots stay small); MODE 1: down, two
+// tiles per stage.
 template <int MODE>
 __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
+  constexpr bool GU = MODE != 1;
   extern __shared__ __align__(128) uint8_t ring[];   // [S][stage_bytes] then the reduction slots
   __shared__ DispatchSmem ds;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -72,11 +77,13 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   __shared__ __align__(8) uint64_t red_full[kMaxStages];
 
   const int NS = a.slices, W = 2 * NS, S = a.stages;
-  // reduction slots after the ring: [S stages][NP passes][W warps][32 lanes]
-  // of float4 (down: two float2, one per tile of the stage)
-  constexpr int NP = MODE == 0 ? 1 : 2;     // passes per stage: down makes one per 4 token slots, C <= 8
+  // reduction slots after the ring, a.red_stage_f4 float4 per stage:
+  //   MODE 0: [W warps][32 lanes] float4
+  //   MODE 2: [2 tiles][W warps][8 pair rows] float4 (tokens 0, 1 only)
+  //   MODE 1: [2 passes][2 tiles][W warps][32 lanes] float2 (one pass per 4 token slots, C <= 8)
+  constexpr int NP = MODE == 1 ? 2 : 1;
   float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);
-  const int red_slot_f4 = W * 32;
+  const int red_slot_f4 = a.red_stage_f4 / NP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_producer = warp == W;
   const bool is_epilogue = warp == W + 1;
@@ -97,11 +104,11 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   // ---------------- B fragments of x (gate/up), independent of the router
   uint32_t bf[kWarpSteps][2];
   float colinv0 = 1.f, colinv1 = 1.f;           // 2^-s of accumulator columns 2q, 2q+1
-  if constexpr (MODE == 0) {
+  if constexpr (GU) {
     if (is_consumer) build_x_fragments(a.x, a.C, a.H, ks0, bf, colinv0, colinv1);
   }
 
-  if constexpr (MODE == 0) pdl_wait();           // ids/weights come from the router
+  if constexpr (GU) pdl_wait();                  // ids/weights come from the router
   build_dispatch(ds, a.ids, a.weights, a.C, a.k, a.E, a.flags);
   pdl_launch_dependents();
 
@@ -153,11 +160,11 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
     float hm0 = 0.f, hm1 = 0.f;
     auto flush_hmax = [&](int dd) {
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
+      for (int o = MODE == 2 ? 1 : 4; o < 32; o <<= 1) {   // MODE 2: tokens 0, 1 in every lane
         hm0 = fmaxf(hm0, __shfl_xor_sync(kFull, hm0, o));
         hm1 = fmaxf(hm1, __shfl_xor_sync(kFull, hm1, o));
       }
-      if (g == 0) {
+      if (g == 0 && (MODE != 2 || q == 0)) {
         const uint32_t mask = ds.tokmask[dd];
         if ((mask >> (2 * q)) & 1u) atomicMax(a.hamax + ds.pair[dd][2 * q], __float_as_uint(hm0));
         if ((mask >> (2 * q + 1)) & 1u) atomicMax(a.hamax + ds.pair[dd][2 * q + 1], __float_as_uint(hm1));
@@ -168,13 +175,13 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
     int item = 0;
     bool ok = true;
     for (int i = 0; i < nstage && ok; i++) {
-      if constexpr (MODE == 0) {
+      if constexpr (GU) {
         if (d != cur_d) {
           flush_hmax(cur_d);
           cur_d = d;
         }
       }
-      const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
+      const int npass = GU ? 1 : (ds.nslot[d] + 3) / 4;
       const int eslot = i % S;
       if (!mbar_wait_bounded(&red_full[eslot], (uint32_t)(i / S) & 1u)) {
         atomicOr(a.flags, MOE_FLAG_TIMEOUT);
@@ -204,6 +211,30 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
               if (c2) hm1 = fmaxf(hm1, fabsf(h)); else hm0 = fmaxf(hm0, fabsf(h));
             }
           }
+        } else if constexpr (MODE == 2) {
+          // lanes 0..15: pair row g2 of tile tt of the stage, tokens 0 and 1
+          if (lane < 16) {
+            const int tt = lane >> 3, g2 = lane & 7;
+            const float4 *pr4 = red + (size_t)rs * red_slot_f4 + (size_t)tt * W * 8 + g2;
+            float4 sum = pr4[0];
+            for (int ww = 1; ww < W; ww++) {
+              const float4 v = pr4[ww * 8];
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            const uint32_t mask = ds.tokmask[d];
+            float *hrow = a.hbuf + operand_order((tile * 2 + tt) * 8 + g2);
+#pragma unroll
+            for (int t = 0; t < 2; t++) {
+              if ((mask >> t) & 1u) {
+                const int p = ds.pair[d][t];
+                const float gg = (t ? sum.y : sum.x) * ds.scal[d][0];
+                const float uu = (t ? sum.w : sum.z) * ds.scal[d][1];
+                const float h = ds.wt[p] * silu(gg) * uu;
+                hrow[(size_t)p * a.I] = h;
+                if (t) hm1 = fmaxf(hm1, fabsf(h)); else hm0 = fmaxf(hm0, fabsf(h));
+              }
+            }
+          }
         } else {
           const float2 *pr2 = reinterpret_cast<const float2 *>(red + (size_t)rs * red_slot_f4) + lane;
           const int sl = 4 * pass + q;
@@ -226,7 +257,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       if (lane == 0) mbar_arrive(&empty_bar[eslot]);   // ring stage and its reduction slots are free
       if (++tile == a.tiles) { tile = 0; d++; }
     }
-    if constexpr (MODE == 0) {
+    if constexpr (GU) {
       if (nstage > 0) flush_hmax(cur_d);
     }
     return;
@@ -240,7 +271,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   bool ok = true;
   for (int i = 0; i < nstage && ok; i++) {
     const int slot = i % S;
-    const int npass = MODE == 0 ? 1 : (ds.nslot[d] + 3) / 4;
+    const int npass = GU ? 1 : (ds.nslot[d] + 3) / 4;
     if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
       atomicOr(a.flags, MOE_FLAG_TIMEOUT);
       break;
@@ -265,6 +296,17 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         mma_half_slice(codes, scales, bf, acc);
         red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
             make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
+      } else if constexpr (MODE == 2) {
+        // two tiles per stage; lanes q = 0 hold the columns of tokens 0 and 1
+        const int tb = a.tile_bytes / 2;
+        float accA[4], accB[4];
+        mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        if (q == 0) {
+          float4 *r4 = red + (size_t)rs * red_slot_f4;
+          r4[(size_t)warp * 8 + g] = make_float4(accA[0] * colinv0, accA[1] * colinv1, accA[2] * colinv0, accA[3] * colinv1);
+          r4[(size_t)(W + warp) * 8 + g] =
+              make_float4(accB[0] * colinv0, accB[1] * colinv1, accB[2] * colinv0, accB[3] * colinv1);
+        }
       } else {
         // two tiles per stage; the hi and lo columns of a slot are added here
         // (both carry the slot's 2^-s), so a partial is one float2 per tile
@@ -283,16 +325,13 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
 }
 
 // ------------------------------------------------------------------ host side
-// Ring geometry: as many tile stages as fit beside the reduction slots.
-void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes, int passes) {
-  const int tile = tiles_per_stage * slices * kTileSliceBytes;
-  const int red1 = passes * 2 * slices * 32 * (int)sizeof(float4);
-  int s = kGemvSmemBytes / (tile + red1);   // stage buffer + its reduction slots
+// Ring geometry: as many stages (stage unit + its reduction slots) as fit.
+void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_bytes) {
+  int s = kGemvSmemBytes / (stage_bytes + red_stage_bytes);
   if (s > kMaxStages) s = kMaxStages;
   if (s < 2) s = 2;
-  *stage_bytes = tile;
   *stages = s;
-  *smem_bytes = s * (tile + red1);
+  *smem_bytes = s * (stage_bytes + red_stage_bytes);
 }
 
 template <int MODE>
@@ -311,7 +350,8 @@ static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_
 }
 
 cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
-  return mode == 0 ? launch_one<0>(a, grid, pdl, stream) : launch_one<1>(a, grid, pdl, stream);
+  return mode == 0 ? launch_one<0>(a, grid, pdl, stream)
+                   : mode == 2 ? launch_one<2>(a, grid, pdl, stream) : launch_one<1>(a, grid, pdl, stream);
 }
 
 cudaError_t gemv_setup() {
@@ -321,6 +361,8 @@ cudaError_t gemv_setup() {
   cudaError_t err = cudaFuncSetAttribute(expert_gemv_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(expert_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(expert_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   return err;
 }
 

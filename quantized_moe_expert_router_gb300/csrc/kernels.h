@@ -53,13 +53,15 @@ struct GemvArgs {
   int slices;                // 512-element K-slices per tile (padded K / 512); 2 consumer warps each
   int stages;                // shared-memory ring stages
   int stage_bytes;           // bytes of one ring stage (one stage unit)
+  int red_stage_f4;          // reduction slots of one stage, in float4
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
 };
 // Ring geometry and dynamic shared memory of one kernel.
-void gemv_geometry(int slices, int tiles_per_stage, int *stages, int *stage_bytes, int *smem_bytes, int passes);
+void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_bytes);
 // Opt-in shared memory of the expert kernels (once per device; idempotent).
 cudaError_t gemv_setup();
-// mode 0: gate/up + SwiGLU -> hbuf; mode 1: down -> ypair -> combine -> y.
+// mode 0: gate/up + SwiGLU -> hbuf (one tile per stage); mode 2: the same, two
+// tiles per stage (groups of at most 2 tokens); mode 1: down -> ypair.
 cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream);
 
 struct CombineArgs {

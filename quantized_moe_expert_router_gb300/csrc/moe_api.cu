@@ -216,22 +216,30 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.weights = weights + (size_t)t0 * k;
     a.y = y + (size_t)t0 * H;
     const long long max_pairs = (long long)Cg * k;
-    // gate/up + SwiGLU
+    // gate/up + SwiGLU: two tiles per stage when the group has at most two
+    // tokens (their partials fit small reduction slots), else one
+    const int wq = 2 * L->w_gu;                // consumer warps
+    const bool gu_pairs = Cg <= 2;
     a.region_off = 0;
-    a.tiles = I / 8;
-    a.tile_bytes = (int)L->gu_tile_bytes;
+    a.tiles = gu_pairs ? I / 16 : I / 8;       // I % 64 == 0
+    a.tile_bytes = (gu_pairs ? 2 : 1) * (int)L->gu_tile_bytes;
     a.slices = L->w_gu;
-    moe::gemv_geometry(a.slices, 1, &a.stages, &a.stage_bytes, &a.smem_bytes, 1);
-    err = moe::launch_expert_gemv(0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
+    a.stage_bytes = a.tile_bytes;
+    a.red_stage_f4 = gu_pairs ? 2 * wq * 8 : wq * 32;
+    moe::gemv_geometry(a.stage_bytes, a.red_stage_f4 * 16, &a.stages, &a.smem_bytes);
+    err = moe::launch_expert_gemv(gu_pairs ? 2 : 0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
     if (err != cudaSuccess) break;
-    // down + combine
+    // down: two tiles per stage, reduction slots for two passes of 4 token slots
+    const int wd = 2 * L->w_dn;
     a.region_off = L->dn_region_off;
-    a.tiles = H / 32;                         // stage units of two tiles of 8 pair rows (H % 64 == 0)
+    a.tiles = H / 32;                          // H % 64 == 0
     a.tile_bytes = 2 * (int)L->dn_tile_bytes;
     a.slices = L->w_dn;
-    moe::gemv_geometry(a.slices, 2, &a.stages, &a.stage_bytes, &a.smem_bytes, 2);
+    a.stage_bytes = a.tile_bytes;
+    a.red_stage_f4 = 2 * wd * 32;
+    moe::gemv_geometry(a.stage_bytes, a.red_stage_f4 * 16, &a.stages, &a.smem_bytes);
     err = moe::launch_expert_gemv(1, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
     if (err != cudaSuccess) break;
     // weighted sum over each token's experts, ascending expert id
