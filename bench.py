@@ -50,6 +50,9 @@ CONFIGS = {
                     workload="K3-shape MoE layer, decode batch 7, top-16 of 896, NVFP4, uniform routing"),
     "k3c7k8": dict(E=896, k=8, H=3584, I=3072, C=7, layers=1, zipf=False,
                    workload="K3-shape MoE layer, decode batch 7, top-8 of 896, NVFP4, uniform routing"),
+    "k3x8zipf": dict(E=896, k=16, H=3584, I=3072, C=1, layers=8, zipf=True,
+                     workload="8 K3-shape MoE layers (133 GB resident), decode batch 1, top-16 of 896, NVFP4, "
+                              "Zipf-biased routing (s = 1.1, per-layer permutation)"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -270,27 +273,43 @@ def main():
     from quantized_moe_expert_router_gb300.synth import device as synth_dev
 
     E, k, H, I, C = cfg["E"], cfg["k"], cfg["H"], cfg["I"], cfg["C"]
+    NL = cfg["layers"]
     free, total = torch.cuda.mem_get_info(dev)
-    need = cfg["layers"] * E * EXPERT_BYTES_K3 * (H * I) / (3584 * 3072) * 2.2
+    # the layers' packed weights plus one canonical copy while a layer is packed
+    need = (NL + 1.2) * E * EXPERT_BYTES_K3 * (H * I) / (3584 * 3072)
     if need > free:
         print(json.dumps({"metric": METRIC, "error": f"needs {need / 1e9:.1f} GB free HBM, {free / 1e9:.1f} GB free"}))
         sys.exit(1)
 
+    # one handle serves every layer (it holds the shapes only); per layer its
+    # packed weights, router and (Zipf) router bias
     layer = moe.Layer(E, k, H, I, C, device=local)
-    canon = synth_dev.canonical_layer_device(args.seed, 0, E, H, I, dev)
-    packed = moe.alloc_packed(layer, dev)
-    moe.moe_pack_weights(layer, canon, packed)
     router_std = synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0
-    Wr = synth.router_weights(args.seed, 0, E, H, router_std)
-    bias = synth.zipf_bias(args.seed, 0, E) if cfg["zipf"] else None
-    Wr_d = torch.from_numpy(Wr).to(dev)
-    bias_d = None if bias is None else torch.from_numpy(bias).to(dev)
+    packed, Wr_ds, bias_ds, biases = [], [], [], []
+    canon = None
+    for li in range(NL):
+        cl = synth_dev.canonical_layer_device(args.seed, li, E, H, I, dev)
+        pk = moe.alloc_packed(layer, dev)
+        moe.moe_pack_weights(layer, cl, pk)
+        packed.append(pk)
+        if li == 0:
+            canon = cl                          # kept for the oracle's sample (layer 0)
+        else:
+            del cl
+            torch.cuda.empty_cache()
+        Wl = synth.router_weights(args.seed, li, E, H, router_std)
+        bl = synth.zipf_bias(args.seed, li, E) if cfg["zipf"] else None
+        Wr_ds.append(torch.from_numpy(Wl).to(dev))
+        bias_ds.append(None if bl is None else torch.from_numpy(bl).to(dev))
+        biases.append(bl)
+        if li == 0:
+            Wr, bias = Wl, bl
 
     # rotating token sets, distinct per rank
     x_host = [synth.tokens(args.seed + 1000 * rank, r, C, H) for r in range(ROTATE)]
     xs = [torch.from_numpy(xh.view(np.int16)).to(dev) for xh in x_host]
-    ids = [torch.empty((C, k), dtype=torch.int32, device=dev) for _ in range(ROTATE)]
-    wts = [torch.empty((C, k), dtype=torch.float32, device=dev) for _ in range(ROTATE)]
+    ids = [[torch.empty((C, k), dtype=torch.int32, device=dev) for _ in range(NL)] for _ in range(ROTATE)]
+    wts = [[torch.empty((C, k), dtype=torch.float32, device=dev) for _ in range(NL)] for _ in range(ROTATE)]
     ys = [torch.empty((C, H), dtype=torch.float32, device=dev) for _ in range(ROTATE)]
     ws = moe.alloc_workspace(layer, C, dev)
 
@@ -321,15 +340,28 @@ def main():
     stream = torch.cuda.Stream(dev)
 
     def step(r, s):
-        moe.moe_route(layer, xs[r], C, Wr_d, bias_d, ids[r], wts[r], ws, s)
-        moe.moe_forward(layer, xs[r], C, ids[r], wts[r], packed, ys[r], ws, s)
+        for li in range(NL):
+            moe.moe_route(layer, xs[r], C, Wr_ds[li], bias_ds[li], ids[r][li], wts[r][li], ws, s)
+            moe.moe_forward(layer, xs[r], C, ids[r][li], wts[r][li], packed[li], ys[r], ws, s)
 
-    # distinct experts each rotating input selects (bytes a step streams)
+    # distinct experts each rotating input selects, summed over the layers
+    # (the bytes a step streams)
     with torch.cuda.stream(stream):
         for r in range(ROTATE):
             step(r, stream)
     stream.synchronize()
-    distinct = [len(set(ids[r].cpu().numpy().ravel().tolist())) for r in range(ROTATE)]
+    distinct = [sum(len(set(ids[r][li].cpu().numpy().ravel().tolist())) for li in range(NL)) for r in range(ROTATE)]
+    zipf_stats = None
+    if cfg["zipf"]:
+        # share of the picks that fall on each layer's 104 hottest experts (by bias)
+        hits = picks = 0
+        for li in range(NL):
+            hot = set(np.argsort(-biases[li], kind="stable")[:104].tolist())
+            for r in range(ROTATE):
+                got = ids[r][li].cpu().numpy().ravel().tolist()
+                hits += sum(e in hot for e in got)
+                picks += len(got)
+        zipf_stats = {"top104_pick_share": hits / picks, "picks": picks}
     flags = moe.moe_get_device_status(layer, ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x} after the first pass")
@@ -386,7 +418,8 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     ms_per_step = ms / args.steps
-    tokens = C * args.steps * world
+    # one MoE layer's throughput: a step runs NL layers on the same C tokens
+    tokens = C * args.steps * NL * world
     tok_s = tokens / (ms / 1e3)
     avg_distinct = sum(distinct[(i % ROTATE)] for i in range(args.steps)) / args.steps
     expert_bytes = E and (EXPERT_BYTES_K3 if (H, I) == (3584, 3072) else 3 * (I * H // 2 + I * H // 16 + 8))
@@ -402,21 +435,22 @@ def main():
     with torch.cuda.stream(stream):
         for i in range(n_prof):
             r = i % ROTATE
-            moe.moe_route(layer, xs[r], C, Wr_d, bias_d, ids[r], wts[r], ws, stream)
+            moe.moe_route(layer, xs[r], C, Wr_ds[0], bias_ds[0], ids[r][0], wts[r][0], ws, stream)
             moe.moe_set_stage_events(layer, evs[i])
-            moe.moe_forward(layer, xs[r], C, ids[r], wts[r], packed, ys[r], ws, stream)
+            moe.moe_forward(layer, xs[r], C, ids[r][0], wts[r][0], packed[0], ys[r], ws, stream)
     moe.moe_set_stage_events(layer, None)
     stream.synchronize()
     gu_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof)]
     dn_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_prof)]
     gu_bytes_per_expert = 2 * (I * H // 2 + I * H // 16)
-    gu_units = sum(distinct[i % ROTATE] for i in range(n_prof)) / n_prof
+    gu_units = sum(len(set(ids[i % ROTATE][0].cpu().numpy().ravel().tolist())) for i in range(n_prof)) / n_prof
     gu_avg = float(np.mean(gu_ms))
     dn_avg = float(np.mean(dn_ms))
     hbm_peak, peak_src = measured_peaks()
     achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
     traffic_per_expert = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
-    roofline = {"kernel": "expert_gemv_kernel<0,NT> (gate/up + SwiGLU)", "bound": "hbm",
+    roofline = {"kernel": f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
+                          f"{'two tiles' if C <= 2 else 'one tile'} per stage)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": peak_src,
                 "traffic": None if traffic_per_expert is None else traffic_per_expert * gu_units,
@@ -438,8 +472,9 @@ def main():
         for i in range(n_e2e):
             r = i % ROTATE
             x_stage.copy_(x_pin[r], non_blocking=True)
-            moe.moe_route(layer, x_stage, C, Wr_d, bias_d, ids[r], wts[r], ws, stream)
-            moe.moe_forward(layer, x_stage, C, ids[r], wts[r], packed, ys[r], ws, stream)
+            for li in range(NL):
+                moe.moe_route(layer, x_stage, C, Wr_ds[li], bias_ds[li], ids[r][li], wts[r][li], ws, stream)
+                moe.moe_forward(layer, x_stage, C, ids[r][li], wts[r][li], packed[li], ys[r], ws, stream)
             y_pin.copy_(ys[r], non_blocking=True)
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
@@ -447,7 +482,7 @@ def main():
         tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_s = float(tt.item())
-    e2e = {"value": C * n_e2e * world / e2e_s, "unit": "tok/s", "steps": n_e2e,
+    e2e = {"value": C * n_e2e * NL * world / e2e_s, "unit": "tok/s", "steps": n_e2e,
            "h2d_bytes_per_step": C * H * 2, "d2h_bytes_per_step": C * H * 4,
            "path": "pinned host x -> H2D -> moe_route -> moe_forward -> D2H y, per step, host-timed"}
 
@@ -456,21 +491,24 @@ def main():
         line = {
             "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, f16 mma, f32 accumulate",
+            "data": "synthetic",
             "config": {"workload": cfg["workload"], "experts": E, "top_k": k, "hidden": H,
-                       "intermediate": I, "tokens_per_step": C, "layers": cfg["layers"],
+                       "intermediate": I, "tokens_per_step": C, "layers": NL,
+                       "value": "tokens per second through one MoE layer" + (f" ({NL} layers per step)" if NL > 1 else ""),
                        "parallelism": f"replicas x{world}",
                        "l2": f"{ROTATE} rotating token sets; each step streams ~{avg_distinct * expert_bytes / 1e6:.0f} MB "
                              "of expert weights (> 129 MB L2)" if H == 3584 else "L2-resident (tiny)",
                        "timing": "CUDA graphs of route+forward, CUDA events on the launching stream"},
-            "us_per_layer": 1e3 * ms_per_step,
+            "us_per_layer": 1e3 * ms_per_step / NL,
             "expert_hbm_gbs": hbm_gbs, "expert_hbm_frac": hbm_gbs / world / hbm_peak,
             "distinct_experts_per_step": avg_distinct,
+            **({"routing": zipf_stats} if zipf_stats else {}),
             "roofline": roofline,
             "e2e": e2e,
             # per step: the router (one kernel, two for C > 8) and, per group of
             # 8 tokens, the gate/up, down and combine kernels
-            "gpu_launches": args.steps * ((1 if C <= 8 else 2) + 3 * ((C + 7) // 8)),
+            "gpu_launches": args.steps * NL * ((1 if C <= 8 else 2) + 3 * ((C + 7) // 8)),
             "clocks": clocks,
             "host_s": t_host,
             "device_flags": flags,

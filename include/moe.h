@@ -133,8 +133,11 @@ moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
 /* Routed expert FFN and combine for C tokens:
  *   y[t] = sum_i weights[t][i] * D_e (silu(G_e x[t]) * (U_e x[t])),  e = ids[t][i]
  * x: device bf16 bits [C][H]; ids: device int32 [C][k] (any order; each
- * token's ids must be distinct and in [0,E) -- offending slots are skipped
- * and flagged); weights: device fp32 [C][k]; packed: the buffer written by
+ * token's ids must be distinct and < E -- offending slots are skipped and
+ * flagged; a negative id marks an absent slot, skipped without a flag, which
+ * is how one rank of an expert-parallel split evaluates only the experts it
+ * holds: see quantized_moe_expert_router_gb300/partition.py); weights: device
+ * fp32 [C][k]; packed: the buffer written by
  * moe_pack_weights; y: device fp32 [C][H] (overwritten).  Each selected
  * expert's packed bytes are read once per call whatever number of tokens
  * chose it.  The sum over a token's experts runs in ascending expert id

@@ -130,9 +130,11 @@ __device__ __forceinline__ int operand_order(int k) {
 // ---------------------------------------------------------------- dispatch
 // Distinct selected experts of this token group in ascending id order, with
 // for each the tokens that chose it (mask, and the (token, slot) pair index
-// p = t*k + slot both by token and in ascending token order).  Ids outside
-// [0,E) are flagged and skipped; an id repeated inside a token is flagged and
-// only its lowest slot is used (the combine kernel applies the same rule).
+// p = t*k + slot both by token and in ascending token order).  A negative id
+// is an absent slot (skipped: a caller evaluating a band of experts marks the
+// others so); ids >= E are flagged and skipped; an id repeated inside a token
+// is flagged and only its lowest slot is used (the combine kernel applies the
+// same rules).
 // The inputs are read from global memory once, together (one round trip on
 // the path to the first weight copy); all else is shared memory.
 __device__ __forceinline__ void build_dispatch(DispatchSmem &s, const int32_t *ids, const float *weights, int C, int k,
@@ -150,7 +152,7 @@ __device__ __forceinline__ void build_dispatch(DispatchSmem &s, const int32_t *i
     const int e = s.ids[p];
     if ((unsigned)e < (unsigned)E)
       atomicOr(&s.bitmap[e >> 5], 1u << (e & 31));
-    else
+    else if (e >= E)                             // negative ids are absent slots, not errors
       atomicOr(flags, MOE_FLAG_BAD_EXPERT_ID);
   }
   __syncthreads();

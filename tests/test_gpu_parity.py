@@ -221,6 +221,42 @@ def test_route_forward_odd_shapes(E, k, H, I, C):
     check_layer(L, x, f"fused E{E} k{k} H{H} I{I} C{C}", fused=True)
 
 
+def _forward(h, x_bits, ids, w, canon_h, ws_tokens=8):
+    """moe_forward of a layer built from host canonical weights."""
+    packed = moe.alloc_packed(h)
+    moe.moe_pack_weights(h, to_device(canon_h), packed)
+    C, H = x_bits.shape
+    y = torch.empty((C, H), dtype=torch.float32, device=DEV)
+    ws = moe.alloc_workspace(h, ws_tokens)
+    moe.moe_forward(h, torch.from_numpy(x_bits.view(np.int16)).to(DEV), C,
+                    torch.from_numpy(np.ascontiguousarray(ids, np.int32)).to(DEV),
+                    torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(DEV), packed, y, ws)
+    assert moe.moe_get_device_status(h, ws) == 0      # absent (negative) ids raise no flag
+    return y.cpu().numpy().astype(np.float64)
+
+
+def test_band_and_slice_partials_sum_to_the_layer():
+    # the two splits of the layer over ranks (expert bands; intermediate
+    # column slices), each partial computed by the CUDA path on its own
+    # layer, summed in rank order
+    from quantized_moe_expert_router_gb300 import partition
+    E, k, H, I, C = 32, 4, 256, 192, 3
+    canon = synth.canonical_layer(0, 0, E, H, I)
+    Wr = synth.router_weights(0, 0, E, H)
+    x = gapped_tokens(0, 0, C, H, Wr, k)
+    ids, w, _ = oracle.route(oracle.router_logits(Wr, x), k)
+    y_o = oracle.moe_forward(canon, x, ids, w)
+    total = np.zeros_like(y_o)
+    for lo, hi in partition.expert_bands(E, 2):
+        total += _forward(moe.Layer(hi - lo, k, H, I, 8), x, partition.band_ids(ids, lo, hi), w,
+                          partition.band_weights(canon, lo, hi))
+    assert_close(total, y_o, "expert bands")
+    total = np.zeros_like(y_o)
+    for i0, i1 in partition.intermediate_slices(I, 2):
+        total += _forward(moe.Layer(E, k, H, i1 - i0, 8), x, ids, w, partition.slice_weights(canon, i0, i1))
+    assert_close(total, y_o, "intermediate slices")
+
+
 def test_forward_is_deterministic():
     L = GpuLayer(32, 4, 256, 192, 8)
     x = gapped_tokens(0, 0, 8, 256, L.Wr, 4)
@@ -333,6 +369,28 @@ def test_k3_decode_batch7_parity(k3_layer, k):
     x = gapped_tokens(1, 0, 7, 3584, L.Wr, k)
     check_layer(L, x, f"k3 C=7 top-{k}")
     check_layer(L, x, f"k3 C=7 top-{k} fused", fused=True)
+
+
+@pytest.mark.parametrize("C", [1, 7])
+def test_k3_zipf_routing_parity(k3_layer, C):
+    # the 8-layer workload's routing: a Zipf router bias (per-layer permutation
+    # of ranks, s = 1.1) and logit noise of std pi / sqrt(6); hot experts are
+    # shared by several tokens of a group
+    L = k3_layer
+    v = _retarget(L, L.h, 16)
+    v.Wr = synth.router_weights(0, 0, 896, 3584, synth.ZIPF_ROUTER_STD)
+    v.bias = synth.zipf_bias(0, 0, 896)
+    v.Wr_d = torch.from_numpy(v.Wr).to(DEV)
+    v.bias_d = torch.from_numpy(v.bias).to(DEV)
+    x = gapped_tokens(2, 0, C, 3584, v.Wr, 16, bias=v.bias)
+    check_layer(v, x, f"k3 zipf C={C}")
+    check_layer(v, x, f"k3 zipf C={C} one call", fused=True)
+
+
+def test_tiny_zipf_routing_parity():
+    L = GpuLayer(32, 4, 256, 192, 8, seed=4, router_std=synth.ZIPF_ROUTER_STD, zipf=True)
+    x = gapped_tokens(4, 0, 8, 256, L.Wr, 4, bias=L.bias)
+    check_layer(L, x, "tiny zipf C=8")
 
 
 def _retarget(L, h, k):
