@@ -53,6 +53,9 @@ CONFIGS = {
     "k3x8zipf": dict(E=896, k=16, H=3584, I=3072, C=1, layers=8, zipf=True,
                      workload="8 K3-shape MoE layers (133 GB resident), decode batch 1, top-16 of 896, NVFP4, "
                               "Zipf-biased routing (s = 1.1, per-layer permutation)"),
+    "prefill512": dict(E=896, k=16, H=3584, I=3072, C=512, layers=1, zipf=True,
+                       workload="K3-shape MoE layer, prefill of 512 tokens, top-16 of 896, NVFP4, "
+                                "Zipf-biased routing (s = 1.1)"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }

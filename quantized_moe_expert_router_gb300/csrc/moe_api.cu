@@ -93,7 +93,7 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
     delete L;
     return MOE_ERR_CUDA;
   }
-  if (moe::route_setup() != cudaSuccess) {
+  if (moe::route_setup() != cudaSuccess || moe::group_setup() != cudaSuccess) {
     delete L;
     return MOE_ERR_CUDA;
   }
@@ -168,7 +168,7 @@ moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_rou
   uint8_t *w = static_cast<uint8_t *>(ws);
   moe::RouteArgs a;
   a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
-  a.logits = reinterpret_cast<float *>(w + wl.logits);
+  a.logits = reinterpret_cast<float *>(w + (C <= moe::kGemvTokens ? wl.logits : wl.glogits));
   a.ticket = &reinterpret_cast<moe::WsControl *>(w)->route_ticket;
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
@@ -208,6 +208,35 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
 
   cudaError_t err = cudaSuccess;
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
+  if (C > moe::kGemvTokens) {
+    // expert-major passes of up to kGroupTokens tokens
+    moe::GroupArgs g = {};
+    g.packed = pk;
+    g.scalars = a.scalars;
+    g.gd = reinterpret_cast<int *>(w + wl.gd);
+    g.xf = reinterpret_cast<uint2 *>(w + wl.xf);
+    g.xinv = reinterpret_cast<float *>(w + wl.xinv);
+    g.hbuf = reinterpret_cast<float *>(w + wl.ghbuf);
+    g.hamax = reinterpret_cast<uint32_t *>(w + wl.ghamax);
+    g.hf = reinterpret_cast<uint2 *>(w + wl.hf);
+    g.hinv = reinterpret_cast<float *>(w + wl.hinv);
+    g.ypair = reinterpret_cast<float *>(w + wl.gypair);
+    g.flags = a.flags;
+    g.k = k; g.E = L->cfg.num_experts; g.H = H; g.I = I; g.Hp = L->Hp; g.Ip = L->Ip;
+    g.expert_bytes = L->expert_bytes;
+    for (int t0 = 0; t0 < C && err == cudaSuccess; t0 += moe::kGroupTokens) {
+      g.C = (C - t0) < moe::kGroupTokens ? (C - t0) : moe::kGroupTokens;
+      g.x = x + (size_t)t0 * H;
+      g.ids = ids + (size_t)t0 * k;
+      g.weights = weights + (size_t)t0 * k;
+      g.y = y + (size_t)t0 * H;
+      err = moe::launch_group_forward(g, L->num_sms, L->w_gu, L->w_dn, L->gu_tile_bytes, L->dn_tile_bytes,
+                                      L->dn_region_off, stream,
+                                      (L->stage_events_on && t0 == 0) ? L->stage_events[1] : nullptr);
+    }
+    if (err == cudaSuccess && L->stage_events_on) err = cudaEventRecord(L->stage_events[2], stream);
+    return cuda_status(err);
+  }
   for (int t0 = 0; t0 < C && err == cudaSuccess; t0 += moe::kGemvTokens) {
     const int Cg = (C - t0) < moe::kGemvTokens ? (C - t0) : moe::kGemvTokens;
     a.C = Cg;

@@ -18,10 +18,12 @@ namespace moe {
 constexpr int kMaxExperts = 1024;        // dispatch bitmap: 32 words of 32 bits
 constexpr int kMaxTopK = 32;             // one top-k slot per lane
 constexpr int kGemvTokens = 8;           // tokens per GEMV group (token mask bits)
+constexpr int kGroupTokens = 512;        // tokens per pass of the grouped (expert-major) path, C > 8
 constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
 constexpr int kGemvSmemBytes = 211968;   // dynamic shared memory of one expert-GEMV CTA (+ ~20 KB static)
+constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped-GEMV CTA (+ ~11 KB static)
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
 
 // Workspace control block (first 256 bytes of the workspace).
@@ -32,14 +34,26 @@ struct WsControl {
 };
 static_assert(sizeof(WsControl) == 256, "control block is 256 bytes");
 
-// Byte offsets of the workspace regions for a group of up to kGemvTokens
-// tokens (GEMV path) and C tokens of router logits.
+// Byte offsets of the workspace regions.  The decode regions (token groups of
+// at most kGemvTokens) sit at fixed offsets whatever C is; calls with C > 8
+// add the router logits of all C tokens and the grouped path's buffers for
+// passes of up to kGroupTokens tokens.
 struct WsLayout {
-  size_t logits;      // float  [C][E]
-  size_t hbuf;        // float  [kGemvTokens * k][I]  w * silu(g) * u per (token, slot), each
+  size_t logits;      // float  [kGemvTokens][E]        router logits, C <= 8
+  size_t hbuf;        // float  [kGemvTokens * k][I]    w * silu(g) * u per (token, slot), each
                       //        16-element block stored in MMA operand order (see expert_gemv.cu)
-  size_t hamax;       // uint32 [kGemvTokens * k]     max |h| per (token, slot) as float bits
-  size_t ypair;       // float  [kGemvTokens * k][H]  D_e h per (token, slot)
+  size_t hamax;       // uint32 [kGemvTokens * k]       max |h| per (token, slot) as float bits
+  size_t ypair;       // float  [kGemvTokens * k][H]    D_e h per (token, slot)
+  // C > 8 only (0 otherwise): Cg = min(C, kGroupTokens) tokens, Pg = Cg * k pairs
+  size_t glogits;     // float  [C][E]                  router logits
+  size_t gd;          // int    n, then expert [E], off [E + 1], pairs [Pg]   expert-major dispatch
+  size_t xf;          // uint2  [Cg][Hp / 16][4]        x as f16 B fragments, scaled per token
+  size_t xinv;        // float  [Cg]                    2^-s of each token's scale
+  size_t ghbuf;       // float  [Pg][I]                 h per pair, operand order
+  size_t ghamax;      // uint32 [Pg]                    max |h| per pair (zero outside a call)
+  size_t hf;          // uint2  [Pg][Ip / 16][4][2]     h as f16 hi / lo B fragments
+  size_t hinv;        // float  [Pg]                    2^-s of each pair's scale
+  size_t gypair;      // float  [Pg][H]                 D_e h per pair
   size_t total;
 };
 
@@ -69,17 +83,31 @@ namespace moe {
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline WsLayout ws_layout(const moe_layer &L, int C) {
-  WsLayout w;
+  WsLayout w = {};
+  const size_t E = L.cfg.num_experts, H = L.cfg.hidden, I = L.cfg.intermediate, k = L.cfg.top_k;
   size_t off = sizeof(WsControl);
-  w.logits = off;
-  off = align_up(off + sizeof(float) * (size_t)C * L.cfg.num_experts, 256);
-  const size_t pairs = (size_t)kGemvTokens * L.cfg.top_k;
-  w.hbuf = off;
-  off = align_up(off + sizeof(float) * pairs * L.cfg.intermediate, 256);
-  w.hamax = off;
-  off = align_up(off + sizeof(uint32_t) * pairs, 256);
-  w.ypair = off;
-  off = align_up(off + sizeof(float) * pairs * L.cfg.hidden, 256);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t pairs = (size_t)kGemvTokens * k;
+  w.logits = take(sizeof(float) * kGemvTokens * E);
+  w.hbuf = take(sizeof(float) * pairs * I);
+  w.hamax = take(sizeof(uint32_t) * pairs);
+  w.ypair = take(sizeof(float) * pairs * H);
+  if (C > kGemvTokens) {
+    const size_t Cg = C < kGroupTokens ? C : kGroupTokens, Pg = Cg * k;
+    w.glogits = take(sizeof(float) * (size_t)C * E);
+    w.gd = take(sizeof(int) * (16 + E + (E + 1) + Pg));
+    w.xf = take(8 * Cg * (size_t)L.Hp / 16 * 4);
+    w.xinv = take(sizeof(float) * Cg);
+    w.ghbuf = take(sizeof(float) * Pg * I);
+    w.ghamax = take(sizeof(uint32_t) * Pg);
+    w.hf = take(8 * Pg * (size_t)L.Ip / 16 * 4 * 2);
+    w.hinv = take(sizeof(float) * Pg);
+    w.gypair = take(sizeof(float) * Pg * H);
+  }
   w.total = off;
   return w;
 }

@@ -200,6 +200,15 @@ def test_odd_shapes_parity(E, k, H, I, C):
     check_layer(L, x, f"E{E} k{k} H{H} I{I} C{C}")
 
 
+@pytest.mark.parametrize("E,k,H,I,C", [(32, 4, 256, 192, 40), (12, 3, 64, 128, 20), (40, 8, 576, 320, 64),
+                                       (7, 7, 192, 1088, 9)])
+def test_grouped_path_parity(E, k, H, I, C):
+    # C > 8 runs expert-major: every expert's weights once for all its tokens
+    L = GpuLayer(E, k, H, I, C, seed=6)
+    x = gapped_tokens(6, 0, C, H, L.Wr, k)
+    check_layer(L, x, f"grouped E{E} k{k} H{H} I{I} C{C}")
+
+
 @pytest.mark.parametrize("C", [1, 3, 8, 11])
 def test_route_forward_equals_route_then_forward(C):
     # the one-call layer gives the separate calls' results bit for bit, call
@@ -369,6 +378,26 @@ def test_k3_decode_batch7_parity(k3_layer, k):
     x = gapped_tokens(1, 0, 7, 3584, L.Wr, k)
     check_layer(L, x, f"k3 C=7 top-{k}")
     check_layer(L, x, f"k3 C=7 top-{k} fused", fused=True)
+
+
+def test_k3_grouped_zipf_sampled_parity(k3_layer):
+    # 48 tokens of a Zipf-routed batch on the expert-major path (hot experts
+    # chosen by most of the tokens); the oracle checks a sample of the tokens
+    L = k3_layer
+    v = _retarget(L, moe.Layer(896, 16, 3584, 3072, 48), 16)
+    v.ws = moe.alloc_workspace(v.h, 48)
+    v.Wr = synth.router_weights(0, 0, 896, 3584, synth.ZIPF_ROUTER_STD)
+    v.bias = synth.zipf_bias(0, 0, 896)
+    v.Wr_d = torch.from_numpy(v.Wr).to(DEV)
+    v.bias_d = torch.from_numpy(v.bias).to(DEV)
+    x = gapped_tokens(3, 0, 48, 3584, v.Wr, 16, bias=v.bias)
+    ids, w, y = v.run(x)
+    assert moe.moe_get_device_status(v.h, v.ws) == 0
+    for t in (0, 17, 47):
+        oids, ow, gap, oy = v.oracle(x[t:t + 1])
+        assert (ids[t] == oids[0]).all()
+        np.testing.assert_allclose(w[t], ow[0], rtol=2e-5, atol=1e-7)
+        assert_close(y[t:t + 1], oy, f"k3 grouped zipf token {t}")
 
 
 @pytest.mark.parametrize("C", [1, 7])
