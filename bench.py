@@ -344,8 +344,8 @@ def main():
 
     def step(r, s):
         for li in range(NL):
-            moe.moe_route(layer, xs[r], C, Wr_ds[li], bias_ds[li], ids[r][li], wts[r][li], ws, s)
-            moe.moe_forward(layer, xs[r], C, ids[r][li], wts[r][li], packed[li], ys[r], ws, s)
+            moe.moe_route_forward(layer, xs[r], C, Wr_ds[li], bias_ds[li], packed[li], ids[r][li], wts[r][li],
+                                  ys[r], ws, s)
 
     # distinct experts each rotating input selects, summed over the layers
     # (the bytes a step streams)
@@ -476,8 +476,8 @@ def main():
             r = i % ROTATE
             x_stage.copy_(x_pin[r], non_blocking=True)
             for li in range(NL):
-                moe.moe_route(layer, x_stage, C, Wr_ds[li], bias_ds[li], ids[r][li], wts[r][li], ws, stream)
-                moe.moe_forward(layer, x_stage, C, ids[r][li], wts[r][li], packed[li], ys[r], ws, stream)
+                moe.moe_route_forward(layer, x_stage, C, Wr_ds[li], bias_ds[li], packed[li], ids[r][li],
+                                      wts[r][li], ys[r], ws, stream)
             y_pin.copy_(ys[r], non_blocking=True)
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
@@ -487,7 +487,7 @@ def main():
         e2e_s = float(tt.item())
     e2e = {"value": C * n_e2e * NL * world / e2e_s, "unit": "tok/s", "steps": n_e2e,
            "h2d_bytes_per_step": C * H * 2, "d2h_bytes_per_step": C * H * 4,
-           "path": "pinned host x -> H2D -> moe_route -> moe_forward -> D2H y, per step, host-timed"}
+           "path": "pinned host x -> H2D -> moe_route_forward -> D2H y, per step, host-timed"}
 
     flags = moe.moe_get_device_status(layer, ws, stream)
     if rank == 0:
@@ -502,7 +502,7 @@ def main():
                        "parallelism": f"replicas x{world}",
                        "l2": f"{ROTATE} rotating token sets; each step streams ~{avg_distinct * expert_bytes / 1e6:.0f} MB "
                              "of expert weights (> 129 MB L2)" if H == 3584 else "L2-resident (tiny)",
-                       "timing": "CUDA graphs of route+forward, CUDA events on the launching stream"},
+                       "timing": "CUDA graphs of moe_route_forward, CUDA events on the launching stream"},
             "us_per_layer": 1e3 * ms_per_step / NL,
             "expert_hbm_gbs": hbm_gbs, "expert_hbm_frac": hbm_gbs / world / hbm_peak,
             "distinct_experts_per_step": avg_distinct,

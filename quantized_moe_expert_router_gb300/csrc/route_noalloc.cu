@@ -74,7 +74,7 @@ extern "C" moe_status moe_route_noalloc(moe_layer_t L, const uint16_t *x, int C,
   cudaError_t err = scratch_address(L->device, &scratch);
   if (err == cudaSuccess) err = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), stream);
   if (err == cudaSuccess) {
-    moe::RouteArgs a;
+    moe::RouteArgs a = {};
     a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
     a.logits = reinterpret_cast<float *>(scratch + 256);
     a.ticket = reinterpret_cast<uint32_t *>(scratch);
