@@ -1,50 +1,100 @@
-// grouped.cu -- the routed expert FFN for C > 8 tokens, expert-major.
+// grouped.cu -- the routed expert FFN for C > 8 tokens, expert-major, on the
+// 5th-generation tensor cores (tcgen05).
 //
 // Same definition as the decode path (expert_gemv.cu, combine.cu; the
 // "MUL_MAT_ID" step of "Kimi-K3 on 2x A40 - measured findings", section "Why
 // the placement experiments all looked the same", with the routed sum of
-// "SparkInfer-K3", "How the TP module works"), organised for many tokens per
-// expert (prefill, large batches): each distinct selected expert's weights
-// are streamed once per pass of up to kGroupTokens tokens, whatever number of
-// them chose it, and each consumer warp decodes its part of a weight tile
-// into registers once and multiplies it with every token block of that
-// expert.
+// "SparkInfer-K3", "How the TP module works"), organised as one grouped GEMM
+// per projection: the rows of every distinct selected expert multiply the
+// x (or h) rows of all the (token, slot) pairs that chose it.
 //
 //   group_dispatch_kernel   ids -> distinct experts (ascending) and, per
 //                           expert, its (token, slot) pairs in ascending order
-//   group_xprep_kernel      x -> f16 B fragments, scaled by a power of two per
-//                           token (exact for bf16 input)
-//   group_gemv_kernel<0>    gate/up + SwiGLU per (expert, tile of 8 pair rows,
-//                           block of 8 pairs) -> h per pair, max |h| per pair
-//   group_hprep_kernel      h -> f16 hi/lo B fragments scaled per pair by a
-//                           power of two (h to 2^-22 of the pair's max |h|)
-//   group_gemv_kernel<1>    down per (expert, tile, block of 4 pairs) ->
-//                           per-pair partial outputs
+//   group_xprep_kernel      per token: the power of two 2^s that puts max|x|
+//                           in [2^14, 2^15) (f16 x is then exact for bf16 x)
+//   group_xgather_kernel    xg = the pairs' x rows in dispatch order, f16,
+//                           laid out k-group major (see below)
+//   group_tc_kernel<0>      gate/up + SwiGLU -> h per pair (fp32)
+//   group_hprep_kernel      per pair: 2^s from max|h|, h * 2^s split into f16
+//                           hi and lo rows (h to 2^-22 of the pair's max |h|)
+//   group_tc_kernel<1>      down -> per-pair partial outputs
 //   group_combine_kernel    y[t] = sum of t's pairs in ascending expert id
 //
-// The decode and MMA arithmetic are those of the decode path (gemv_core.cuh);
-// sums over warps and over a token's experts run in a fixed order, so results
-// are bitwise reproducible.  The work split weighs each (expert, tile) unit
-// by the streaming of the tile plus its token blocks, so hot experts (the
-// one nearly every token of a Zipf-routed prefill picks) are spread over
-// many SMs.
+// group_tc_kernel.  A unit is (expert d, m-tile mt, column chunk nc): 128
+// weight rows (8 packed tiles of 16 rows) times up to 128 B rows (gate/up:
+// 128 pairs; down: the hi and lo rows of 64 pairs) over the whole K, so every
+// unit is a complete dot product and units are independent.  Units are
+// weighted (streaming and decoding a unit's weights, plus its MMA columns)
+// and cut into one contiguous range per CTA.  One CTA per SM, 16 warps:
+//   warp 0     bulk copies of the weights, a half slice (256 k) of 8 tiles
+//              per stage, into a ring of shared-memory stages;
+//   warp 1     3-D TMA loads of the B rows, 64 k per stage: the global B
+//              buffers are [K/8][rows][8] f16, so a box of (8, R, 8) lands as
+//              eight k-groups of R rows of 16 bytes, which is the K-major,
+//              unswizzled core-matrix layout of the MMA's B operand;
+//   warp 2     owns tensor memory and issues tcgen05.mma kind::f16 (M=128,
+//              N = the unit's B rows rounded up to 16, K=16): A from tensor
+//              memory, B from shared memory, fp32 D in tensor memory (two
+//              buffers of 128 columns, so the epilogue of one unit overlaps
+//              the MMAs of the next);
+//   warps 4-11 decode: two sets of four warps (warp w reaches tensor-memory
+//              lanes 32 (w % 4) ..); a thread owns one weight row, turns 64 k
+//              of e2m1 codes into f16 (cvt.rn.f16x2.e2m1x2), multiplies by
+//              the e4m3 block scales (exact: at most 6 significant bits) and
+//              stores them into one of 8 A buffers of 32 columns
+//              (tcgen05.st); set s takes the 64-k sub-chunks s and s + 2 of
+//              every stage;
+//   warps 12-15 epilogue: read D with tcgen05.ld, apply the tensor scales,
+//              the f16 scales of x or h and (gate/up) SwiGLU and the router
+//              weight, and store per-pair rows.
+// Weight row to tensor-memory lane: lane 32 q + l (warp quadrant q, lane l)
+// holds row 8 (l & 1) + ((l >> 1) & 7) of packed tile 2 q + (l >> 4) of the
+// m-tile: rowA (gate; down row 2p) for even l, rowB (up; down row 2p + 1) for
+// odd l, so a gate row's up partner is the neighbouring lane and a warp's
+// down outputs are 32 consecutive rows.
+// Every wait is bounded (about two seconds of %globaltimer): on expiry the
+// waiting role sets MOE_FLAG_TIMEOUT and stops; the producers then wait
+// (bounded) for their copies in flight and the MMA warp for its MMAs before
+// tensor memory is released.  The sums over K run in the MMA's fixed order
+// and over a token's experts in ascending id order, so results are bitwise
+// reproducible.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "moe_internal.cuh"
 #include "kernels.h"
 #include "gemv_core.cuh"
 
 namespace moe {
 
-constexpr int kGBlkGU = 8;       // pairs per token block, gate/up: one MMA column each
-constexpr int kGBlkDN = 4;       // pairs per token block, down: hi and lo columns
-constexpr int kGRedSlots = 4;    // consumer -> epilogue reduction ring
-constexpr int kGUnitBase = 1;    // work split weight of streaming + decoding a tile ...
-constexpr int kGBlockCost = 2;   // ... and of one token block of it (measured: a block costs about twice a tile)
 constexpr int kGDispatchThreads = 1024;
+constexpr int kTcTiles = 8;                    // packed tiles of 16 rows per m-tile: M = 128
+constexpr int kTcColsGU = 64;                  // pairs per unit, gate/up (one B row each)
+constexpr int kTcColsDN = 32;                  // pairs per unit, down (hi and lo B rows)
+constexpr int kTcBRows = 64;                   // B rows per stage at most
+constexpr int kTcBoxes = 3;                    // B boxes of 16, 32 and 64 rows
+constexpr int kTcBK = 128;                     // k per B stage: sub-chunk j of it goes to issuer j
+constexpr int kTcAStageBytes = kTcTiles * (2048 + 256);   // a half slice of 8 tiles: codes, then scales
+constexpr int kTcBStageBytes = kTcBRows * kTcBK * 2;
+constexpr int kTcAStages = 6;
+constexpr int kTcBStages = 6;
+constexpr int kTcABufs = 8;                    // A buffers of 32 columns (64 k of 128 f16 rows): one issuer step
+constexpr int kTcIssuers = 2;                  // MMA warps: issuer j takes the 64-k sub-chunks of parity j
+constexpr int kTcDCol0 = 0;                    // D: [issuer][2 buffers] of 64 columns
+constexpr int kTcACol0 = 256;
+constexpr uint32_t kTcTmemCols = 512;
+constexpr int kTcUnitBase = 12;                // work weight of a unit: 12 + one per 16 B rows
+constexpr int kTcThreads = 512;
+constexpr int kTcWProdA = 0, kTcWProdB = 1, kTcWMma = 2, kTcWDec0 = 4, kTcWEpi0 = 12;   // MMA warps 2, 3
+constexpr int kTcEpiBar = 1;                   // named barrier of the 4 epilogue warps
+constexpr int kTcSmemBytes = kTcBStages * kTcBStageBytes + kTcAStages * kTcAStageBytes + 1024;
+static_assert(kTcSmemBytes <= kGroupSmemBytes, "grouped ring exceeds its shared-memory budget");
 
 // gd layout (ints): [0] n, [16, 16 + E) expert of rank d, [16 + E, 17 + 2E) off, then pairs
 __device__ __forceinline__ int *gd_expert(int *gd) { return gd + 16; }
 __device__ __forceinline__ int *gd_off(int *gd, int E) { return gd + 16 + E; }
 __device__ __forceinline__ int *gd_pairs(int *gd, int E) { return gd + 17 + 2 * E; }
+__device__ __forceinline__ const int *gd_pairs(const int *gd, int E) { return gd + 17 + 2 * E; }
 
 // Exclusive scan of v over a CTA of up to 1024 threads; `wsum` is 32 ints of
 // shared memory; returns the prefix and writes the total.
@@ -149,9 +199,8 @@ __global__ void __launch_bounds__(kGDispatchThreads) group_dispatch_kernel(const
   }
 }
 
-// ---------------------------------------------------------------- x fragments
-// One CTA per token: xf[t][s][q] = (x[16s+2q], x[16s+2q+1]) and (x[16s+2q+8],
-// x[16s+2q+9]) as f16, times 2^s_t with max|x_t| 2^s_t in [2^14, 2^15).
+// ---------------------------------------------------------------- x rows
+// One CTA per token: xinv[t] = 2^-s_t with max|x_t| 2^s_t in [2^14, 2^15).
 __global__ void __launch_bounds__(128) group_xprep_kernel(const GroupArgs a) {
   __shared__ float red[4];
   const int t = blockIdx.x, tid = threadIdx.x;
@@ -168,353 +217,586 @@ __global__ void __launch_bounds__(128) group_xprep_kernel(const GroupArgs a) {
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   if ((tid & 31) == 0) red[tid >> 5] = m;
   __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  float inv;
-  const float up = f16_range_scale(m, &inv);
-  if (tid == 0) a.xinv[t] = inv;
-  const int S = a.Hp / 16;
-  uint2 *out = a.xf + (size_t)t * S * 4;
-  for (int i = tid; i < S * 4; i += blockDim.x) {
-    const int s = i >> 2, q = i & 3, k0 = 16 * s + 2 * q;
-    uint32_t v0 = 0, v1 = 0;
-    if (k0 < a.H) {
-      v0 = *reinterpret_cast<const uint32_t *>(xr + k0);
-      v1 = *reinterpret_cast<const uint32_t *>(xr + k0 + 8);
-    }
-    out[i] = make_uint2(pack_half2(__uint_as_float(v0 << 16) * up, __uint_as_float(v0 & 0xFFFF0000u) * up),
-                        pack_half2(__uint_as_float(v1 << 16) * up, __uint_as_float(v1 & 0xFFFF0000u) * up));
+  if (tid == 0) {
+    float inv;
+    f16_range_scale(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), &inv);
+    a.xinv[t] = inv;
   }
 }
 
-// ---------------------------------------------------------------- h fragments
-// Per kept pair p (from the dispatch lists): hf[p][s][q] = hi and lo f16x2
-// pairs of h * 2^s_p (elements 2q, 2q+1 and 2q+8, 2q+9 of k-step s, read as
-// one float4 from the operand-ordered hbuf), hinv[p] = 2^-s_p; the max |h|
-// word is reset for the next call.
-__global__ void __launch_bounds__(256) group_hprep_kernel(const GroupArgs a) {
+// xg[kg][j][0..7] = x[t_j][8 kg .. 8 kg + 7] * 2^s_t as f16 (zero past H) for
+// every dispatched pair j (token t_j); rows of the buffer are the C * k pair
+// positions, of which the first `total` are written.
+__global__ void __launch_bounds__(256) group_xgather_kernel(const GroupArgs a) {
   const int n = a.gd[0];
   const int total = gd_off(a.gd, a.E)[n];
   const int *pairs = gd_pairs(a.gd, a.E);
-  const int S = a.Ip / 16;
-  for (int j = blockIdx.x; j < total; j += gridDim.x) {
-    const int p = pairs[j];
-    const float am = __uint_as_float(__ldcg(a.hamax + p));
-    float inv;
-    const float up = f16_range_scale(am, &inv);
-    const float4 *hr4 = reinterpret_cast<const float4 *>(a.hbuf + (size_t)p * a.I);
-    uint2 *out = a.hf + (size_t)p * S * 8;
-    for (int i = threadIdx.x; i < S * 4; i += blockDim.x) {
-      const int s = i >> 2;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (16 * s < a.I) v = __ldcg(hr4 + i);
-      const float x0 = v.x * up, x1 = v.y * up, x2 = v.z * up, x3 = v.w * up;
-      const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-      out[2 * i] = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
-      out[2 * i + 1] = make_uint2(pack_half2(x0 - f01.x, x1 - f01.y), pack_half2(x2 - f23.x, x3 - f23.y));
+  const int P = a.C * a.k, KG = a.Hp / 8;
+  const int items = total * KG;
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+    const int kg = it / total, j = it - kg * total;
+    const int t = __ldg(pairs + j) / a.k;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (8 * kg < a.H) {
+      const float up = __frcp_rn(__ldg(a.xinv + t));   // exact: a power of two
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + 8 * kg));
+      out.x = pack_half2(__uint_as_float(v.x << 16) * up, __uint_as_float(v.x & 0xFFFF0000u) * up);
+      out.y = pack_half2(__uint_as_float(v.y << 16) * up, __uint_as_float(v.y & 0xFFFF0000u) * up);
+      out.z = pack_half2(__uint_as_float(v.z << 16) * up, __uint_as_float(v.z & 0xFFFF0000u) * up);
+      out.w = pack_half2(__uint_as_float(v.w << 16) * up, __uint_as_float(v.w & 0xFFFF0000u) * up);
     }
-    if (threadIdx.x == 0) {
-      a.hinv[p] = inv;
-      a.hamax[p] = 0u;
-    }
+    reinterpret_cast<uint4 *>(a.xg)[(size_t)kg * P + j] = out;
   }
 }
 
-// ---------------------------------------------------------------- GEMV
-struct GroupSmem {
-  int16_t expert[kMaxExperts];
-  int off[kMaxExperts + 1];
-  int pre[kMaxExperts + 1];                        // cost prefix over experts
-  int wsum[33];
-  int n;
-  int range[4];                                    // d0, tile0, d1, tile1 of this CTA
+// ---------------------------------------------------------------- h rows
+// One CTA of 128 threads per dispatched pair j (pair p): the pair's max |h|
+// sets 2^s (max|h| 2^s in [2^14, 2^15)); hg rows 2j and 2j + 1 get the f16
+// hi part of h 2^s and the f16 rest (zero past I); hinv[p] = 2^-s.
+constexpr int kHprepThreads = 128;
+constexpr int kHprepGroups = 4;                 // k-groups of 8 per thread: Ip <= 4096
+__global__ void __launch_bounds__(kHprepThreads) group_hprep_kernel(const GroupArgs a) {
+  __shared__ float red[kHprepThreads / 32];
+  const int n = a.gd[0];
+  const int total = gd_off(a.gd, a.E)[n];
+  const int *pairs = gd_pairs(a.gd, a.E);
+  const int R2 = 2 * a.C * a.k, KG = a.Ip / 8, tid = threadIdx.x;
+  for (int j = blockIdx.x; j < total; j += gridDim.x) {
+    const int p = __ldg(pairs + j);
+    const float4 *hr = reinterpret_cast<const float4 *>(a.hbuf + (size_t)p * a.I);
+    float4 v[kHprepGroups][2];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < kHprepGroups; i++) {
+      const int kg = tid + kHprepThreads * i;
+      v[i][0] = v[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kg < KG && 8 * kg < a.I) {
+        v[i][0] = __ldcg(hr + 2 * kg);
+        v[i][1] = __ldcg(hr + 2 * kg + 1);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i][hh].x), fabsf(v[i][hh].y)), fmaxf(fabsf(v[i][hh].z), fabsf(v[i][hh].w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    float inv;
+    const float up = f16_range_scale(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), &inv);
+    __syncthreads();                               // red is reused by the next pair
+#pragma unroll
+    for (int i = 0; i < kHprepGroups; i++) {
+      const int kg = tid + kHprepThreads * i;
+      if (kg >= KG) continue;
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const float x0 = v[i][hh].x * up, x1 = v[i][hh].y * up, x2 = v[i][hh].z * up, x3 = v[i][hh].w * up;
+        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        hi[2 * hh] = *reinterpret_cast<const uint32_t *>(&h01);
+        hi[2 * hh + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+        lo[2 * hh] = pack_half2(x0 - f01.x, x1 - f01.y);
+        lo[2 * hh + 1] = pack_half2(x2 - f23.x, x3 - f23.y);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(a.hg) + (size_t)kg * R2 + 2 * j;
+      dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      dst[1] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    if (tid == 0) a.hinv[p] = inv;
+  }
+}
+
+// ---------------------------------------------------------------- tensor-core GEMM
+struct GroupTcArgs {
+  CUtensorMap bmap[kTcBoxes];   // B rows: boxes of (8, 16 << i, 16) over [K/8][rows][8] f16
+  CUtensorMap amap[2];          // weights of the region, 8-byte elements: codes (256, 1, 8, 1) and
+                                // scales (32, 1, 8, 1) boxes over [E][tiles][half slices][..]
+  const float *scalars;
+  const int *gd;
+  const float *weights;         // [C][k] router weights (gate/up)
+  const float *colscale;        // gate/up: xinv per token; down: hinv per pair
+  float *out;                   // gate/up: hbuf [C*k][I]; down: ypair [C*k][H]
+  int32_t *flags;
+  int k, E, H, I;
+  int Kp;                       // padded K of the weight rows
+  int tiles;                    // packed tiles of 16 rows per expert in this region
+  int cols;                     // pairs per unit
 };
 
-// Start (d, tile) of the first unit whose cost start is >= c (units of expert
-// d cost cost_d each and start at pre[d] + tile * cost_d).
-__device__ __forceinline__ void unit_at(const GroupSmem &s, int tiles, int blk, int c, int &d, int &tile) {
-  int lo = 0, hi = s.n;                             // largest d with pre[d] <= c
+struct TcSmem {
+  uint64_t a_full[kTcAStages], a_empty[kTcAStages];
+  uint64_t b_full[kTcBStages], b_empty[kTcBStages];
+  uint64_t a_ready[kTcABufs], a_free[kTcABufs];   // per tensor-memory A buffer
+  uint64_t d_full[2], d_free[2];
+  uint64_t drain[kTcIssuers];
+  uint32_t tmem_base;
+  int n;
+  int verdict;                  // epilogue: the D wait succeeded
+  int range[6];                 // first unit (d, mt, nc) of this CTA and the end
+  int wsum[33];
+  int colp[kTcBRows];           // epilogue: pair of each column of the unit
+  float colw[kTcBRows], cols[kTcBRows];
+  int16_t expert[kMaxExperts];
+  int off[kMaxExperts + 1];
+  int pre[kMaxExperts + 1];     // work prefix over experts
+};
+
+struct TcUnit {
+  int d, mt, nc;
+};
+__device__ __forceinline__ bool unit_before(const TcUnit &u, const TcUnit &e) {
+  return u.d != e.d ? u.d < e.d : (u.mt != e.mt ? u.mt < e.mt : u.nc < e.nc);
+}
+__device__ __forceinline__ int unit_nch(const TcSmem &s, int d, int cols) {
+  return (s.off[d + 1] - s.off[d] + cols - 1) / cols;
+}
+__device__ __forceinline__ void unit_next(const TcSmem &s, TcUnit &u, int MT, int cols) {
+  if (++u.nc == unit_nch(s, u.d, cols)) {
+    u.nc = 0;
+    if (++u.mt == MT) {
+      u.mt = 0;
+      u.d++;
+    }
+  }
+}
+// Work weight of a unit with `rows` B rows, and of one m-tile of an expert
+// with cnt pairs (its column chunks: all full but the last).
+__device__ __forceinline__ int unit_cost(int rows) { return kTcUnitBase + (rows + 15) / 16; }
+__device__ __forceinline__ int mtile_cost(int cnt, int cols, int rf, int &cfull) {
+  const int nch = (cnt + cols - 1) / cols;
+  cfull = unit_cost(cols * rf);
+  return (nch - 1) * cfull + unit_cost((cnt - (nch - 1) * cols) * rf);
+}
+// First unit whose work start is >= c.
+__device__ __forceinline__ TcUnit unit_at(const TcSmem &s, int MT, int cols, int rf, long long c) {
+  int lo = 0, hi = s.n;                            // largest d with pre[d] <= c
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (s.pre[mid] <= c) lo = mid; else hi = mid - 1;
   }
-  d = lo;
-  if (d >= s.n) { tile = 0; return; }
-  const int nb = (s.off[d + 1] - s.off[d] + blk - 1) / blk;
-  const int cost = kGUnitBase + kGBlockCost * nb;
-  tile = (c - s.pre[d] + cost - 1) / cost;
-  if (tile >= tiles) { d++; tile = 0; }
-}
-
-// Decode a warp's 16 k-steps of one tile into A fragments (f16, scaled).
-__device__ __forceinline__ void decode_half_slice(const uint8_t *codes, const uint8_t *scales, uint32_t (&A)[kWarpSteps][4]) {
-  const int lane = threadIdx.x & 31, g = lane >> 2;
-  uint4 sc = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int qg = 0; qg < kWarpSteps / 4; qg++) {
-    const uint4 cw = *reinterpret_cast<const uint4 *>(codes + ((size_t)qg * 32 + lane) * 16);
-    if ((qg & 1) == 0) sc = *reinterpret_cast<const uint4 *>(scales + ((size_t)(qg >> 1) * 8 + g) * 16);
-    const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-    const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-    for (int jj = 0; jj < 4; jj++) {
-      const int s = 4 * qg + jj;
-      const int ks = (qg & 1) * 4 + jj;
-      const uint32_t s2 = e4m3x2_to_f16x2(scs[ks >> 1] >> (16 * (ks & 1)));
-      e2m1x8_to_f16x2(cws[jj], A[s]);
-      A[s][0] = hmul2_lo(A[s][0], s2);
-      A[s][1] = hmul2_hi(A[s][1], s2);
-      A[s][2] = hmul2_lo(A[s][2], s2);
-      A[s][3] = hmul2_hi(A[s][3], s2);
-    }
+  TcUnit u = {lo, 0, 0};
+  if (lo >= s.n) return u;
+  const int cnt = s.off[lo + 1] - s.off[lo], nch = (cnt + cols - 1) / cols;
+  int cf;
+  const int cmt = mtile_cost(cnt, cols, rf, cf);
+  const int r = (int)(c - s.pre[lo]);
+  u.mt = r / cmt;
+  const int rr = r - u.mt * cmt;
+  u.nc = (rr + cf - 1) / cf;
+  if (u.nc >= nch) {
+    u.nc = 0;
+    u.mt++;
   }
+  if (u.mt >= MT) {
+    u.mt = 0;
+    u.d++;
+  }
+  return u;
 }
 
-// WIDE = 1 for tiles of 8 K-slices (18 warps): the register file is split over
-// the four SM sub-partitions, so a 5th warp on one of them caps a thread at 96
-// registers; with at most 16 warps a thread may use 128, which holds a tile's
-// decoded weights (64 registers) and a token block's B fragments (32) at once.
-template <int MODE, int WIDE>
-__global__ void __launch_bounds__(WIDE ? kMaxCtaThreads : 512, 1) group_gemv_kernel(const GroupArgs a) {
-  extern __shared__ __align__(128) uint8_t ring[];   // [S][stage_bytes] then the reduction slots
-  __shared__ GroupSmem gs;
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t red_full[kGRedSlots];
-  __shared__ __align__(8) uint64_t red_empty[kGRedSlots];
-  constexpr int BLK = MODE == 0 ? kGBlkGU : kGBlkDN;
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kTcEpiBar), "n"(128) : "memory"); }
 
-  const int NS = a.slices, W = 2 * NS, S = a.stages;
-  float4 *red = reinterpret_cast<float4 *>(ring + (size_t)S * a.stage_bytes);   // [slots][W][32]
+// 32 columns of this warp's 32 tensor-memory lanes: store / load.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+// Shared-memory descriptor of a K-major, unswizzled operand: start address,
+// byte offset between core matrices adjacent in K (leading) and in N
+// (stride), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_t, uint32_t a_t, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_t),
+      "r"(a_t), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+// Elements (0, 1) and (8, 9) of a code word's two rowA bytes (bytes 0, 2)
+// as f16x2.
+__device__ __forceinline__ void e2m1_bytes02(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b2;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+// Number of B rows, MMA N and box index of a unit with np pairs.
+__device__ __forceinline__ void unit_shape(int np, int rf, int &rows, int &N, int &bi) {
+  rows = np * rf;
+  N = (rows + 15) & ~15;
+  bi = N <= 16 ? 0 : (N <= 32 ? 1 : 2);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_constant__ GroupTcArgs a) {
+  extern __shared__ uint8_t dsm[];
+  __shared__ TcSmem s;
+  constexpr int rf = MODE == 0 ? 1 : 2;            // B rows per pair
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slice = warp >> 1, half = warp & 1;
-  const int ks0 = kSliceSteps * slice + kWarpSteps * half;
-  const int g = lane >> 2, q = lane & 3;
-  const int E = a.E;
+  const int E = a.E, cols = a.cols;
+  const int MT = (a.tiles + kTcTiles - 1) / kTcTiles;
+  const int HS = a.Kp / 256, KB = a.Kp / kTcBK;
+  uint8_t *ring_b = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);   // 1024-byte aligned
+  uint8_t *ring_a = ring_b + kTcBStages * kTcBStageBytes;
 
   if (tid == 0) {
-    for (int s = 0; s < S; s++) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], W);
+    for (int i = 0; i < kTcAStages; i++) {
+      mbar_init(&s.a_full[i], 1);
+      mbar_init(&s.a_empty[i], 8);                 // the 8 decode warps
     }
-    for (int s = 0; s < kGRedSlots; s++) {
-      mbar_init(&red_full[s], W);
-      mbar_init(&red_empty[s], 1);
+    for (int i = 0; i < kTcBStages; i++) {
+      mbar_init(&s.b_full[i], 1);
+      mbar_init(&s.b_empty[i], kTcIssuers);
     }
+    for (int i = 0; i < kTcABufs; i++) {
+      mbar_init(&s.a_ready[i], 4);                 // the 4 warps of a decode set
+      mbar_init(&s.a_free[i], 1);
+    }
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&s.d_full[i], kTcIssuers);
+      mbar_init(&s.d_free[i], 4);                  // the 4 epilogue warps
+    }
+    for (int i = 0; i < kTcIssuers; i++) mbar_init(&s.drain[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    gs.n = a.gd[0];
+    s.n = a.gd[0];
   }
+  if (warp == kTcWMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s.tmem_base)),
+                 "r"(kTcTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
   __syncthreads();
-  const int n = gs.n;
-  // experts, pair offsets and the cost prefix (every CTA computes the same)
+  tc_fence_after();
+  const int n = s.n;
   {
+    // experts, pair offsets and the work prefix (every CTA computes the same)
     int run = 0;
     for (int d0 = 0; d0 < n; d0 += blockDim.x) {
       const int d = d0 + tid;
       int cost = 0;
       if (d < n) {
-        gs.expert[d] = (int16_t)gd_expert(a.gd)[d];
-        const int o = gd_off(a.gd, E)[d], o1 = gd_off(a.gd, E)[d + 1];
-        gs.off[d] = o;
-        cost = a.tiles * (kGUnitBase + kGBlockCost * ((o1 - o + BLK - 1) / BLK));
+        s.expert[d] = (int16_t)a.gd[16 + d];
+        const int o = a.gd[16 + E + d], o1 = a.gd[17 + E + d];
+        s.off[d] = o;
+        int cf;
+        cost = MT * mtile_cost(o1 - o, cols, rf, cf);
       }
       int t1;
-      const int pre = cta_scan_excl(cost, gs.wsum, t1) + run;
-      if (d < n) gs.pre[d] = pre;
+      const int pre = cta_scan_excl(cost, s.wsum, t1) + run;
+      if (d < n) s.pre[d] = pre;
       run += t1;
     }
     if (tid == 0) {
-      gs.off[n] = gd_off(a.gd, E)[n];
-      gs.pre[n] = run;
+      s.off[n] = a.gd[16 + E + n];
+      s.pre[n] = run;
     }
     __syncthreads();
     if (tid == 0) {
-      const int total = gs.pre[n];
-      int d0, t0, d1, t1;
-      // total * grid can exceed 32 bits here (once per CTA: 64-bit is fine)
-      const int c0 = (int)((long long)total * blockIdx.x / gridDim.x);
-      const int c1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
-      unit_at(gs, a.tiles, BLK, c0, d0, t0);
-      unit_at(gs, a.tiles, BLK, c1, d1, t1);
-      gs.range[0] = d0; gs.range[1] = t0; gs.range[2] = d1; gs.range[3] = t1;
+      const long long total = s.pre[n];
+      const TcUnit u0 = unit_at(s, MT, cols, rf, total * blockIdx.x / gridDim.x);
+      const TcUnit u1 = unit_at(s, MT, cols, rf, total * (blockIdx.x + 1) / gridDim.x);
+      s.range[0] = u0.d; s.range[1] = u0.mt; s.range[2] = u0.nc;
+      s.range[3] = u1.d; s.range[4] = u1.mt; s.range[5] = u1.nc;
     }
     __syncthreads();
   }
-  const int ud0 = gs.range[0], ut0 = gs.range[1], ud1 = gs.range[2], ut1 = gs.range[3];
-  const int nunit = (ud1 - ud0) * a.tiles + (ut1 - ut0);
+  const TcUnit beg = {s.range[0], s.range[1], s.range[2]}, end = {s.range[3], s.range[4], s.range[5]};
+  const uint32_t tbase = s.tmem_base;
   const int *pairs = gd_pairs(a.gd, E);
 
-  if (warp == W) {
-    // ------------------------------------------------ producer
+  if (warp == kTcWProdA) {
+    // ------------------------------------------------ weights: half slices of 8 tiles (codes, scales)
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int i = 0;
+      int ia = 0;
       bool ok = true;
-      int d = ud0, tile = ut0;
-      for (; i < nunit; i++, tile++) {
-        if (tile == a.tiles) { tile = 0; d++; }
-        const int slot = i % S;
-        const uint32_t use = (uint32_t)(i / S);
-        if (use > 0 && !mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1u)) {
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
+        const int e = s.expert[u.d], t0 = kTcTiles * u.mt;
+        for (int hs = 0; hs < HS; hs++, ia++) {
+          const int slot = ia % kTcAStages;
+          if (ia >= kTcAStages && !mbar_wait_bounded(&s.a_empty[slot], (uint32_t)(ia / kTcAStages - 1) & 1u)) {
+            atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+            ok = false;
+            break;
+          }
+          uint8_t *dst = ring_a + (size_t)slot * kTcAStageBytes;
+          // tiles past the region's last read as zeros
+          mbar_arrive_expect_tx(&s.a_full[slot], (uint32_t)kTcAStageBytes);
+          tma_load_4d(dst, &a.amap[0], 0, hs, t0, e, &s.a_full[slot], pol);
+          tma_load_4d(dst + kTcTiles * 2048, &a.amap[1], 0, hs, t0, e, &s.a_full[slot], pol);
+        }
+      }
+      for (int j = (ia > kTcAStages ? ia - kTcAStages : 0); j < ia; j++)
+        mbar_wait_bounded(&s.a_full[j % kTcAStages], (uint32_t)(j / kTcAStages) & 1u);
+    }
+  } else if (warp == kTcWProdB) {
+    // ------------------------------------------------ B rows: 64 k per stage
+    if (lane == 0) {
+      int gc = 0;
+      bool ok = true;
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
+        const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
+        int rows, N, bi;
+        unit_shape(np, rf, rows, N, bi);
+        const int row0 = rf * (off + u.nc * cols);
+        for (int b = 0; b < KB; b++, gc++) {
+          const int slot = gc % kTcBStages;
+          if (gc >= kTcBStages && !mbar_wait_bounded(&s.b_empty[slot], (uint32_t)(gc / kTcBStages - 1) & 1u)) {
+            atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.b_full[slot], (uint32_t)((16 << bi) * kTcBK * 2));
+          tma_load_3d(ring_b + (size_t)slot * kTcBStageBytes, &a.bmap[bi], 0, row0, (kTcBK / 8) * b, &s.b_full[slot]);
+        }
+      }
+      for (int j = (gc > kTcBStages ? gc - kTcBStages : 0); j < gc; j++)
+        mbar_wait_bounded(&s.b_full[j % kTcBStages], (uint32_t)(j / kTcBStages) & 1u);
+    }
+  } else if (warp == kTcWMma || warp == kTcWMma + 1) {
+    // ------------------------------------------------ MMA issue: issuer j takes sub-chunks j, j + 2, ...
+    const int j = warp - kTcWMma;
+    if (lane == 0) {
+      const uint32_t bring = smem_u32(ring_b);
+      int gb = 0, ud = 0;                            // global B stage; this issuer's sub-chunk is 2 gb + j
+      bool ok = true;
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols), ud++) {
+        const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
+        int rows, N, bi;
+        unit_shape(np, rf, rows, N, bi);
+        const uint32_t br = 16u << bi;
+        const int db = ud & 1;
+        if (ud >= 2 && !mbar_wait_bounded(&s.d_free[db], (uint32_t)((ud >> 1) - 1) & 1u)) {
           atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-          ok = false;
           break;
         }
-        const uint8_t *src = a.packed + (size_t)gs.expert[d] * a.expert_bytes + a.region_off +
-                             (size_t)tile * a.tile_bytes;
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)a.tile_bytes);
-        bulk_copy_g2s(ring + (size_t)slot * a.stage_bytes, src, (uint32_t)a.tile_bytes, &full_bar[slot], pol);
-      }
-      if (!ok)
-        for (int j = (i > S ? i - S : 0); j < i; j++) mbar_wait_bounded(&full_bar[j % S], (uint32_t)(j / S) & 1u);
-    }
-    return;
-  }
-
-  if (warp == W + 1) {
-    // ------------------------------------------------ epilogue warp
-    int d = ud0, tile = ut0, item = 0, cur = -1;
-    float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f;
-    bool ok = true;
-    for (int i = 0; i < nunit && ok; i++, tile++) {
-      if (tile == a.tiles) { tile = 0; d++; }
-      if (d != cur) {
-        cur = d;
-        const float *sc = a.scalars + (size_t)gs.expert[d] * 6;
-        sc0 = sc[0]; sc1 = sc[2]; sc2 = sc[4];
-      }
-      const int o = gs.off[d], cnt = gs.off[d + 1] - o;
-      for (int b = 0; b * BLK < cnt; b++, item++) {
-        const int rs = item % kGRedSlots;
-        if (!mbar_wait_bounded(&red_full[rs], (uint32_t)(item / kGRedSlots) & 1u)) {
-          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-          ok = false;
-          break;
-        }
-        if constexpr (MODE == 0) {
-          const float4 *pr4 = red + (size_t)rs * W * 32 + lane;
-          float4 sum = pr4[0];
-          for (int ww = 1; ww < W; ww++) {
-            const float4 v = pr4[ww * 32];
-            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        tc_fence_after();
+        // D f32, A and B f16, both K-major, N, M = 128
+        const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((128u >> 4) << 24);
+        const uint32_t dt = tbase + (uint32_t)(kTcDCol0 + 128 * j + 64 * db);
+        const uint64_t bd_lo = smem_desc(0u, br * 16u, 128u);   // LBO / SBO fields; start added per stage
+        for (int b = 0; b < KB; b++, gb++) {
+          const int gc = 2 * gb + j, ab = gc % kTcABufs, bs = gb % kTcBStages;
+          if (!mbar_wait_bounded(&s.a_ready[ab], (uint32_t)(gc / kTcABufs) & 1u) ||
+              !mbar_wait_bounded(&s.b_full[bs], (uint32_t)(gb / kTcBStages) & 1u)) {
+            atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+            ok = false;
+            break;
           }
-          float hm0 = 0.f, hm1 = 0.f;
+          tc_fence_after();
+          // this issuer's 64 k of the stage: k-groups 8 j .. 8 j + 7
+          const uint64_t bd0 = bd_lo | (uint64_t)(((bring + (uint32_t)(bs * kTcBStageBytes) + 128u * j * br) >> 4) & 0x3FFFu);
+          const uint32_t at = tbase + (uint32_t)(kTcACol0 + 32 * ab);
 #pragma unroll
-          for (int c2 = 0; c2 < 2; c2++) {
-            const int j = b * BLK + 2 * q + c2;
-            if (j < cnt) {
-              const int p = pairs[o + j];
-              const float gg = (c2 ? sum.y : sum.x) * sc0;
-              const float uu = (c2 ? sum.w : sum.z) * sc1;
-              const float h = __ldg(a.weights + p) * silu(gg) * uu;
-              a.hbuf[(size_t)p * a.I + operand_order(tile * 8 + g)] = h;
-              if (c2) hm1 = fabsf(h); else hm0 = fabsf(h);
-            }
-          }
-          // max |h| of the block's pairs over the tile's 8 pair rows
-#pragma unroll
-          for (int sh = 4; sh < 32; sh <<= 1) {
-            hm0 = fmaxf(hm0, __shfl_xor_sync(kFull, hm0, sh));
-            hm1 = fmaxf(hm1, __shfl_xor_sync(kFull, hm1, sh));
-          }
-          if (g == 0) {
-            const int j0 = b * BLK + 2 * q;
-            if (j0 < cnt) atomicMax(a.hamax + pairs[o + j0], __float_as_uint(hm0));
-            if (j0 + 1 < cnt) atomicMax(a.hamax + pairs[o + j0 + 1], __float_as_uint(hm1));
-          }
-        } else {
-          const float2 *pr2 = reinterpret_cast<const float2 *>(red + (size_t)rs * W * 32) + lane;
-          float2 sum = pr2[0];
-          for (int ww = 1; ww < W; ww++) {
-            const float2 v = pr2[ww * 32];
-            sum.x += v.x; sum.y += v.y;
-          }
-          const int j = b * BLK + q;
-          if (j < cnt)
-            *reinterpret_cast<float2 *>(a.ypair + (size_t)pairs[o + j] * a.H + 2 * (tile * 8 + g)) =
-                make_float2(sum.x * sc2, sum.y * sc2);
+          for (int kk = 0; kk < 4; kk++)
+            tc_mma(dt, at + 8u * kk, bd0 + (uint64_t)(2u * kk * br), idesc, (uint32_t)(b | kk));
+          tc_commit(&s.a_free[ab]);
+          tc_commit(&s.b_empty[bs]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&red_empty[rs]);
+        if (ok) tc_commit(&s.d_full[db]);
       }
-    }
-    return;
-  }
-
-  // ---------------------------------------------------- consumers
-  const int HS = (MODE == 0 ? a.Hp : a.Ip) / 16;   // k-steps of this region's B rows
-  int d = ud0, tile = ut0, item = 0;
-  bool ok = true;
-  for (int i = 0; i < nunit && ok; i++, tile++) {
-    if (tile == a.tiles) { tile = 0; d++; }
-    const int slot = i % S;
-    if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
-      atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-      break;
-    }
-    uint32_t A[kWarpSteps][4];
-    {
-      const uint8_t *stg = ring + (size_t)slot * a.stage_bytes;
-      decode_half_slice(stg + (size_t)slice * 4096 + (size_t)half * 2048,
-                        stg + (size_t)NS * 4096 + (size_t)slice * 512 + (size_t)half * 256, A);
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(&s.drain[j]);
+      mbar_wait_bounded(&s.drain[j], 0u);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[slot]);   // the weights are in registers: refill the stage
-    const int o = gs.off[d], cnt = gs.off[d + 1] - o;
-    // this lane's pairs in a block: the one of its B column, and the two (or
-    // one, down) of its accumulator columns; fetched one block ahead
-    const int colj = MODE == 0 ? g : (g >> 1), accj = MODE == 0 ? 2 * q : q;
-    auto pair_at = [&](int j) { return j < cnt ? __ldg(pairs + o + j) : -1; };
-    int n_col = pair_at(colj), n_a0 = pair_at(accj), n_a1 = MODE == 0 ? pair_at(accj + 1) : -1;
-    for (int b = 0; b * BLK < cnt; b++, item++) {
-      const int p_col = n_col, p_a0 = n_a0, p_a1 = n_a1;
-      n_col = pair_at((b + 1) * BLK + colj);
-      n_a0 = pair_at((b + 1) * BLK + accj);
-      if constexpr (MODE == 0) n_a1 = pair_at((b + 1) * BLK + accj + 1);
-      const int rs = item % kGRedSlots;
-      const uint32_t ruse = (uint32_t)(item / kGRedSlots);
-      if (ruse > 0 && !mbar_wait_bounded(&red_empty[rs], (ruse - 1) & 1u)) {
-        atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-        ok = false;
-        break;
-      }
-      // B fragments of this lane's column and the 2^-s of its accumulator columns
-      const uint2 *bsrc;
-      float ci0, ci1;
-      if constexpr (MODE == 0) {
-        bsrc = p_col >= 0 ? a.xf + ((size_t)(p_col / a.k) * HS + ks0) * 4 + q : nullptr;
-        ci0 = p_a0 >= 0 ? __ldg(a.xinv + p_a0 / a.k) : 0.f;
-        ci1 = p_a1 >= 0 ? __ldg(a.xinv + p_a1 / a.k) : 0.f;
-      } else {
-        bsrc = p_col >= 0 ? a.hf + (((size_t)p_col * HS + ks0) * 4 + q) * 2 + (g & 1) : nullptr;
-        ci0 = ci1 = p_a0 >= 0 ? __ldcg(a.hinv + p_a0) : 0.f;
-      }
-      // two accumulator chains; all B loads of the block issued together
-      // (eight k-steps at a time where registers are short)
-      float acc2[2][4] = {};
-      constexpr int BB = WIDE ? 8 : 16;
-#pragma unroll
-      for (int h8 = 0; h8 < kWarpSteps / BB; h8++) {
-        uint2 bv[BB];
-#pragma unroll
-        for (int s = 0; s < BB; s++) {
-          const int ss = BB * h8 + s;
-          bv[s] = bsrc ? __ldcg(bsrc + (size_t)ss * (MODE == 0 ? 4 : 8)) : make_uint2(0u, 0u);
+  } else if (warp >= kTcWDec0 && warp < kTcWEpi0) {
+    // ------------------------------------------------ decode into tensor memory
+    const int set = (warp - kTcWDec0) >> 2, wq = warp & 3;
+    const int Tl = 2 * wq + (lane >> 4), g = (lane >> 1) & 7, hi = lane & 1;
+    const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16);
+    const uint32_t sel = hi ? 0x3232u : 0x1010u;  // this row's scale in both halves
+    int ia = 0;
+    bool ok = true;
+    for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
+      for (int hs = 0; hs < HS; hs++, ia++) {
+        const int slot = ia % kTcAStages;
+        if (!mbar_wait_bounded(&s.a_full[slot], (uint32_t)(ia / kTcAStages) & 1u)) {
+          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const uint8_t *stg = ring_a + (size_t)slot * kTcAStageBytes;
+        // this set's sub-chunks of the stage: set and set + 2
+        const int ab0 = (4 * ia + set) % kTcABufs, ab1 = (4 * ia + set + 2) % kTcABufs;
+        const int use = (4 * ia + set) / kTcABufs;     // both buffers are on the same use
+        if (use > 0 && (!mbar_wait_bounded(&s.a_free[ab0], (uint32_t)(use - 1) & 1u) ||
+                        !mbar_wait_bounded(&s.a_free[ab1], (uint32_t)(use - 1) & 1u))) {
+          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+          ok = false;
+          break;
         }
 #pragma unroll
-        for (int s = 0; s < BB; s++) mma16816(acc2[s & 1], A[BB * h8 + s], bv[s].x, bv[s].y);
-      }
-      float acc[4];
+        for (int h2 = 0; h2 < 2; h2++) {
+          const int sc = set + 2 * h2;               // 64-k sub-chunk of the stage
+          // lanes 4g + q of the sub-chunk's code group hold this row pair's
+          // words of its 4 k-steps; the scale unit of row pair g holds the
+          // (rowA, rowB) e4m3 bytes of each k-step
+          const uint8_t *cp = stg + Tl * 2048 + sc * 512 + g * 64;
+          uint4 cw[4];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; c4++) acc[c4] = acc2[0][c4] + acc2[1][c4];
-      if constexpr (MODE == 0)
-        red[((size_t)rs * W + warp) * 32 + lane] = make_float4(acc[0] * ci0, acc[1] * ci1, acc[2] * ci0, acc[3] * ci1);
-      else
-        reinterpret_cast<float2 *>(red + (size_t)rs * W * 32)[(size_t)warp * 32 + lane] =
-            make_float2((acc[0] + acc[1]) * ci0, (acc[2] + acc[3]) * ci0);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_full[rs]);
+          for (int q = 0; q < 4; q++) cw[q] = *reinterpret_cast<const uint4 *>(cp + 16 * q);
+          const uint2 sw =
+              *reinterpret_cast<const uint2 *>(stg + kTcTiles * 2048 + Tl * 256 + (sc >> 1) * 128 + g * 16 + (sc & 1) * 8);
+          uint32_t r[32];
+#pragma unroll
+          for (int jj = 0; jj < 4; jj++) {
+            const uint32_t s2 = __byte_perm(e4m3x2_to_f16x2(((jj < 2 ? sw.x : sw.y) >> (16 * (jj & 1))) & 0xFFFFu), 0u, sel);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              const uint32_t wv = (jj == 0 ? cw[q].x : jj == 1 ? cw[q].y : jj == 2 ? cw[q].z : cw[q].w) >> (8 * hi);
+              uint32_t c01, c89;
+              e2m1_bytes02(wv, c01, c89);
+              r[8 * jj + q] = hmul2_u32(c01, s2);      // elements 2q, 2q+1 of k-step jj
+              r[8 * jj + 4 + q] = hmul2_u32(c89, s2);  // elements 2q+8, 2q+9
+            }
+          }
+          tc_st32(trow + (uint32_t)(kTcACol0 + 32 * (h2 ? ab1 : ab0)), r);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s.a_ready[ab0]);
+          mbar_arrive(&s.a_ready[ab1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.a_empty[slot]);
+      }
     }
+  } else if (warp >= kTcWEpi0) {
+    // ------------------------------------------------ epilogue
+    const int wq = warp & 3, et = tid - 32 * kTcWEpi0;
+    const int Tl = 2 * wq + (lane >> 4), g = (lane >> 1) & 7, hi = lane & 1;
+    const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16);
+    int ud = 0, cur = -1;
+    float sc0 = 0.f, sc1 = 0.f;
+    for (TcUnit u = beg; unit_before(u, end); unit_next(s, u, MT, cols), ud++) {
+      const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
+      const int j0 = off + u.nc * cols;
+      const int T = kTcTiles * u.mt + Tl;            // packed tile of this lane's row
+      if (u.d != cur) {
+        cur = u.d;
+        const float *sc = a.scalars + (size_t)s.expert[u.d] * 6;
+        sc0 = MODE == 0 ? sc[0] : sc[4];
+        sc1 = sc[2];
+      }
+      epi_sync();                                    // the previous unit's column data is read
+      if (et < np) {
+        const int p = __ldg(pairs + j0 + et);
+        s.colp[et] = p;
+        if constexpr (MODE == 0) {
+          s.colw[et] = __ldg(a.weights + p);
+          s.cols[et] = __ldg(a.colscale + p / a.k);
+        } else {
+          s.cols[et] = __ldcg(a.colscale + p);
+        }
+      }
+      const int db = ud & 1;
+      if (et == 0) s.verdict = mbar_wait_bounded(&s.d_full[db], (uint32_t)(ud >> 1) & 1u) ? 1 : 0;
+      epi_sync();
+      if (!s.verdict) {
+        if (et == 0) atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = trow + (uint32_t)(kTcDCol0 + 64 * db);
+      const int ncol = np * rf;
+      for (int c0 = 0; c0 < ncol; c0 += 32) {
+        float v[32], v1[32];
+        tc_ld32(dt + (uint32_t)c0, v);                 // issuer 0: even 64-k sub-chunks
+        tc_ld32(dt + 128u + (uint32_t)c0, v1);         // issuer 1: odd ones
+#pragma unroll
+        for (int i = 0; i < 32; i++) v[i] += v1[i];
+        if (c0 + 32 >= ncol) {                       // the last read of this D buffer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.d_free[db]);
+        }
+        if constexpr (MODE == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const int nn = c0 + i;
+            if (nn >= np) break;
+            const float up = __shfl_xor_sync(kFull, v[i], 1);
+            if (!hi && T < a.tiles) {
+              const float xs = s.cols[nn];
+              const float gg = v[i] * xs * sc0, uu = up * xs * sc1;
+              a.out[(size_t)s.colp[nn] * a.I + 8 * T + g] = s.colw[nn] * silu(gg) * uu;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            const int nn = (c0 >> 1) + i;
+            if (nn >= np) break;
+            if (T < a.tiles)
+              a.out[(size_t)s.colp[nn] * a.H + 16 * T + (lane & 15)] = (v[2 * i] + v[2 * i + 1]) * s.cols[nn] * sc0;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcWMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTcTmemCols) : "memory");
   }
 }
 
@@ -555,15 +837,66 @@ __global__ void __launch_bounds__(128) group_combine_kernel(const GroupArgs a) {
 }
 
 // ------------------------------------------------------------------ host side
+using TensorMapEncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static TensorMapEncodeFn tensor_map_encoder() {
+  static const TensorMapEncodeFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<TensorMapEncodeFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor maps of a B buffer [Kp/8][rows][8] f16: boxes of 16 k-groups of
+// 16, 32 and 64 rows of 8 elements.
+static cudaError_t encode_b_maps(CUtensorMap (&maps)[kTcBoxes], const void *base, int rows, int Kp) {
+  const TensorMapEncodeFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  for (int i = 0; i < kTcBoxes; i++) {
+    const cuuint64_t dims[3] = {8, (cuuint64_t)rows, (cuuint64_t)(Kp / 8)};
+    const cuuint64_t strides[2] = {16, (cuuint64_t)rows * 16};
+    const cuuint32_t box[3] = {8, (cuuint32_t)(16 << i), kTcBK / 8};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+// Tensor maps of one weight region (gate/up or down) of every expert, in
+// 8-byte elements: the codes [E][tiles][half slices][2048 B] and the scales
+// [E][tiles][half slices][256 B] of the packed tiles; a box is one half slice
+// of 8 consecutive tiles.
+static cudaError_t encode_a_maps(CUtensorMap (&maps)[2], const uint8_t *packed, size_t region_off, int slices,
+                                 int tiles, int tile_bytes, int E, size_t expert_bytes) {
+  const TensorMapEncodeFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  for (int i = 0; i < 2; i++) {
+    const cuuint64_t inner = i == 0 ? 256 : 32;              // 2048 or 256 bytes
+    const cuuint64_t dims[4] = {inner, (cuuint64_t)(2 * slices), (cuuint64_t)tiles, (cuuint64_t)E};
+    const cuuint64_t strides[3] = {inner * 8, (cuuint64_t)tile_bytes, (cuuint64_t)expert_bytes};
+    const cuuint32_t box[4] = {(cuuint32_t)inner, 1, kTcTiles, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const uint8_t *base = packed + region_off + (i == 0 ? 0 : (size_t)slices * 4096);
+    const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<uint8_t *>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t group_setup() {
-  cudaError_t err = cudaFuncSetAttribute(group_gemv_kernel<0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGroupSmemBytes);
+  cudaError_t err =
+      cudaFuncSetAttribute(group_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(group_gemv_kernel<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmemBytes);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(group_gemv_kernel<0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmemBytes);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(group_gemv_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmemBytes);
+    err = cudaFuncSetAttribute(group_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(group_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)group_dispatch_smem(kMaxExperts));
@@ -572,47 +905,50 @@ cudaError_t group_setup() {
 
 size_t group_dispatch_smem(int E) { return (size_t)E * (kGroupTokens / 32) * 4 + 2 * (size_t)E * 4 + 33 * 4; }
 
-void group_geometry(int slices, int tile_bytes, int *stages, int *smem_bytes) {
-  const int red = kGRedSlots * 2 * slices * 32 * (int)sizeof(float4);
-  int s = (kGroupSmemBytes - red) / tile_bytes;
-  if (s > kMaxStages) s = kMaxStages;
-  if (s < 2) s = 2;
-  *stages = s;
-  *smem_bytes = s * tile_bytes + red;
-}
-
 cudaError_t launch_group_forward(GroupArgs a, int num_sms, int w_gu, int w_dn, size_t gu_tile_bytes,
                                  size_t dn_tile_bytes, size_t dn_region_off, cudaStream_t stream,
                                  cudaEvent_t after_gate_up) {
-  group_dispatch_kernel<<<1, kGDispatchThreads, group_dispatch_smem(a.E), stream>>>(a);
-  cudaError_t err = cudaGetLastError();
+  const int P = a.C * a.k;
+  GroupTcArgs t;
+  memset(&t, 0, sizeof(t));
+  cudaError_t err = encode_b_maps(t.bmap, a.xg, P, a.Hp);
   if (err != cudaSuccess) return err;
+  group_dispatch_kernel<<<1, kGDispatchThreads, group_dispatch_smem(a.E), stream>>>(a);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   group_xprep_kernel<<<a.C, 128, 0, stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  // gate/up
-  a.region_off = 0;
-  a.tiles = a.I / 8;
-  a.tile_bytes = a.stage_bytes = (int)gu_tile_bytes;
-  a.slices = w_gu;
-  group_geometry(a.slices, a.stage_bytes, &a.stages, &a.smem_bytes);
-  if (2 * w_gu + 2 > 16)
-    group_gemv_kernel<0, 1><<<num_sms, 32 * (2 * w_gu + 2), a.smem_bytes, stream>>>(a);
-  else
-    group_gemv_kernel<0, 0><<<num_sms, 32 * (2 * w_gu + 2), a.smem_bytes, stream>>>(a);
+  group_xgather_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  // gate/up + SwiGLU
+  t.scalars = a.scalars;
+  t.gd = a.gd;
+  t.weights = a.weights;
+  t.flags = a.flags;
+  t.k = a.k; t.E = a.E; t.H = a.H; t.I = a.I;
+  t.colscale = a.xinv;
+  t.out = a.hbuf;
+  t.Kp = a.Hp;
+  t.tiles = a.I / 8;
+  t.cols = kTcColsGU;
+  if ((err = encode_a_maps(t.amap, a.packed, 0, w_gu, t.tiles, (int)gu_tile_bytes, a.E, a.expert_bytes)) !=
+      cudaSuccess)
+    return err;
+  group_tc_kernel<0><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (after_gate_up && (err = cudaEventRecord(after_gate_up, stream)) != cudaSuccess) return err;
-  group_hprep_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  group_hprep_kernel<<<num_sms * 8, kHprepThreads, 0, stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // down
-  a.region_off = dn_region_off;
-  a.tiles = a.H / 16;
-  a.tile_bytes = a.stage_bytes = (int)dn_tile_bytes;
-  a.slices = w_dn;
-  group_geometry(a.slices, a.stage_bytes, &a.stages, &a.smem_bytes);
-  if (2 * w_dn + 2 > 16)
-    group_gemv_kernel<1, 1><<<num_sms, 32 * (2 * w_dn + 2), a.smem_bytes, stream>>>(a);
-  else
-    group_gemv_kernel<1, 0><<<num_sms, 32 * (2 * w_dn + 2), a.smem_bytes, stream>>>(a);
+  if ((err = encode_b_maps(t.bmap, a.hg, 2 * P, a.Ip)) != cudaSuccess) return err;
+  t.colscale = a.hinv;
+  t.out = a.ypair;
+  t.Kp = a.Ip;
+  t.tiles = a.H / 16;
+  t.cols = kTcColsDN;
+  if ((err = encode_a_maps(t.amap, a.packed, dn_region_off, w_dn, t.tiles, (int)dn_tile_bytes, a.E, a.expert_bytes)) !=
+      cudaSuccess)
+    return err;
+  group_tc_kernel<1><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   group_combine_kernel<<<a.C, 128, 0, stream>>>(a);
   return cudaGetLastError();

@@ -81,24 +81,22 @@ struct GroupArgs {
   const uint8_t *packed;
   const float *scalars;      // packed + scalars_off: float [E][6]
   int *gd;                   // expert-major dispatch: n, expert [E], off [E + 1], pairs
-  uint2 *xf;                 // [C][Hp/16][4] x B fragments
-  float *xinv;               // [C]
-  float *hbuf;               // [C*k][I] operand order
-  uint32_t *hamax;           // [C*k] (zero outside a call)
-  uint2 *hf;                 // [C*k][Ip/16][4][2] h hi/lo B fragments
-  float *hinv;               // [C*k]
+  float *xinv;               // [C]             2^-s of each token's f16 scale
+  uint16_t *xg;              // f16 [Hp/8][C*k][8]  x rows of the dispatched pairs, pair order
+  float *hbuf;               // [C*k][I]        h per pair
+  uint16_t *hg;              // f16 [Ip/8][2*C*k][8] hi / lo rows of h, pair order
+  float *hinv;               // [C*k]           2^-s of each pair's h scale
   float *ypair;              // [C*k][H]
   float *y;                  // [C][H]
   int32_t *flags;
   int C, k, E, H, I, Hp, Ip;
-  size_t expert_bytes, region_off;
-  int tiles, tile_bytes, slices, stages, stage_bytes, smem_bytes;
+  size_t expert_bytes;
 };
 // Opt-in shared memory of the grouped kernels (once per device; idempotent).
 cudaError_t group_setup();
 size_t group_dispatch_smem(int E);
 // The routed experts of one pass of up to kGroupTokens tokens, expert-major:
-// dispatch, x fragments, gate/up, h fragments, down, combine.
+// dispatch, x rows, gate/up, h rows, down, combine.
 cudaError_t launch_group_forward(GroupArgs a, int num_sms, int w_gu, int w_dn, size_t gu_tile_bytes,
                                  size_t dn_tile_bytes, size_t dn_region_off, cudaStream_t stream,
                                  cudaEvent_t after_gate_up);

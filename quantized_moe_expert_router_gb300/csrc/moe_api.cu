@@ -214,11 +214,10 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     g.packed = pk;
     g.scalars = a.scalars;
     g.gd = reinterpret_cast<int *>(w + wl.gd);
-    g.xf = reinterpret_cast<uint2 *>(w + wl.xf);
     g.xinv = reinterpret_cast<float *>(w + wl.xinv);
+    g.xg = reinterpret_cast<uint16_t *>(w + wl.xg);
     g.hbuf = reinterpret_cast<float *>(w + wl.ghbuf);
-    g.hamax = reinterpret_cast<uint32_t *>(w + wl.ghamax);
-    g.hf = reinterpret_cast<uint2 *>(w + wl.hf);
+    g.hg = reinterpret_cast<uint16_t *>(w + wl.hg);
     g.hinv = reinterpret_cast<float *>(w + wl.hinv);
     g.ypair = reinterpret_cast<float *>(w + wl.gypair);
     g.flags = a.flags;

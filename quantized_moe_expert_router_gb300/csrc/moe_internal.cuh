@@ -23,7 +23,7 @@ constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per g
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
 constexpr int kGemvSmemBytes = 211968;   // dynamic shared memory of one expert-GEMV CTA (+ ~20 KB static)
-constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped-GEMV CTA (+ ~11 KB static)
+constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped-GEMM CTA at most (+ ~12 KB static)
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
 
 // Workspace control block (first 256 bytes of the workspace).
@@ -47,12 +47,11 @@ struct WsLayout {
   // C > 8 only (0 otherwise): Cg = min(C, kGroupTokens) tokens, Pg = Cg * k pairs
   size_t glogits;     // float  [C][E]                  router logits
   size_t gd;          // int    n, then expert [E], off [E + 1], pairs [Pg]   expert-major dispatch
-  size_t xf;          // uint2  [Cg][Hp / 16][4]        x as f16 B fragments, scaled per token
-  size_t xinv;        // float  [Cg]                    2^-s of each token's scale
-  size_t ghbuf;       // float  [Pg][I]                 h per pair, operand order
-  size_t ghamax;      // uint32 [Pg]                    max |h| per pair (zero outside a call)
-  size_t hf;          // uint2  [Pg][Ip / 16][4][2]     h as f16 hi / lo B fragments
-  size_t hinv;        // float  [Pg]                    2^-s of each pair's scale
+  size_t xinv;        // float  [Cg]                    2^-s of each token's f16 scale
+  size_t xg;          // f16    [Hp / 8][Pg][8]         x rows of the pairs in dispatch order
+  size_t ghbuf;       // float  [Pg][I]                 h per pair
+  size_t hg;          // f16    [Ip / 8][2 Pg][8]       hi / lo rows of h in dispatch order
+  size_t hinv;        // float  [Pg]                    2^-s of each pair's h scale
   size_t gypair;      // float  [Pg][H]                 D_e h per pair
   size_t total;
 };
@@ -100,11 +99,10 @@ inline WsLayout ws_layout(const moe_layer &L, int C) {
     const size_t Cg = C < kGroupTokens ? C : kGroupTokens, Pg = Cg * k;
     w.glogits = take(sizeof(float) * (size_t)C * E);
     w.gd = take(sizeof(int) * (16 + E + (E + 1) + Pg));
-    w.xf = take(8 * Cg * (size_t)L.Hp / 16 * 4);
     w.xinv = take(sizeof(float) * Cg);
+    w.xg = take(2 * Pg * (size_t)L.Hp);
     w.ghbuf = take(sizeof(float) * Pg * I);
-    w.ghamax = take(sizeof(uint32_t) * Pg);
-    w.hf = take(8 * Pg * (size_t)L.Ip / 16 * 4 * 2);
+    w.hg = take(2 * 2 * Pg * (size_t)L.Ip);
     w.hinv = take(sizeof(float) * Pg);
     w.gypair = take(sizeof(float) * Pg * H);
   }
