@@ -69,19 +69,19 @@ namespace moe {
 
 constexpr int kGDispatchThreads = 1024;
 constexpr int kTcTiles = 8;                    // packed tiles of 16 rows per m-tile: M = 128
+constexpr int kTcIssuers = 2;                  // MMA warps: issuer j owns m-tile j of a unit
+constexpr int kTcUnitTiles = kTcTiles * kTcIssuers;   // packed tiles (256 weight rows) per unit
 constexpr int kTcColsGU = 64;                  // pairs per unit, gate/up (one B row each)
 constexpr int kTcColsDN = 32;                  // pairs per unit, down (hi and lo B rows)
 constexpr int kTcBRows = 64;                   // B rows per stage at most
 constexpr int kTcBoxes = 3;                    // B boxes of 16, 32 and 64 rows
-constexpr int kTcBK = 128;                     // k per B stage: sub-chunk j of it goes to issuer j
-constexpr int kTcAStageBytes = kTcTiles * (2048 + 256);   // a half slice of 8 tiles: codes, then scales
-constexpr int kTcBStageBytes = kTcBRows * kTcBK * 2;
-constexpr int kTcAStages = 6;
-constexpr int kTcBStages = 6;
-constexpr int kTcABufs = 8;                    // A buffers of 32 columns (64 k of 128 f16 rows): one issuer step
-constexpr int kTcIssuers = 2;                  // MMA warps: issuer j takes the 64-k sub-chunks of parity j
+constexpr int kTcStageK = 256;                 // k per stage (a half slice); the A and B rings advance together
+constexpr int kTcAStageBytes = kTcUnitTiles * (2048 + 256);   // codes of 16 tiles, then their scales
+constexpr int kTcBStageBytes = kTcBRows * kTcStageK * 2;
+constexpr int kTcAStages = 3;
+constexpr int kTcBStages = 3;
 constexpr int kTcDCol0 = 0;                    // D: [issuer][2 buffers] of 64 columns
-constexpr int kTcACol0 = 256;
+constexpr int kTcACol0 = 256;                  // A: [issuer][2 halves of a stage][2 sub-chunks of 64 k] of 32 columns
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcUnitBase = 12;                // work weight of a unit: 12 + one per 16 B rows
 constexpr int kTcThreads = 512;
@@ -310,9 +310,9 @@ __global__ void __launch_bounds__(kHprepThreads) group_hprep_kernel(const GroupA
 
 // ---------------------------------------------------------------- tensor-core GEMM
 struct GroupTcArgs {
-  CUtensorMap bmap[kTcBoxes];   // B rows: boxes of (8, 16 << i, 16) over [K/8][rows][8] f16
-  CUtensorMap amap[2];          // weights of the region, 8-byte elements: codes (256, 1, 8, 1) and
-                                // scales (32, 1, 8, 1) boxes over [E][tiles][half slices][..]
+  CUtensorMap bmap[kTcBoxes];   // B rows: boxes of (8, 16 << i, 32) over [K/8][rows][8] f16
+  CUtensorMap amap[2];          // weights of the region, 8-byte elements: codes (256, 1, 16, 1) and
+                                // scales (32, 1, 16, 1) boxes over [E][tiles][half slices][..]
   const float *scalars;
   const int *gd;
   const float *weights;         // [C][k] router weights (gate/up)
@@ -328,7 +328,7 @@ struct GroupTcArgs {
 struct TcSmem {
   uint64_t a_full[kTcAStages], a_empty[kTcAStages];
   uint64_t b_full[kTcBStages], b_empty[kTcBStages];
-  uint64_t a_ready[kTcABufs], a_free[kTcABufs];   // per tensor-memory A buffer
+  uint64_t a_ready[kTcIssuers][2], a_free[kTcIssuers][2];   // per issuer and half of a stage
   uint64_t d_full[2], d_free[2];
   uint64_t drain[kTcIssuers];
   uint32_t tmem_base;
@@ -487,8 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
   constexpr int rf = MODE == 0 ? 1 : 2;            // B rows per pair
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, cols = a.cols;
-  const int MT = (a.tiles + kTcTiles - 1) / kTcTiles;
-  const int HS = a.Kp / 256, KB = a.Kp / kTcBK;
+  const int MP = (a.tiles + kTcUnitTiles - 1) / kTcUnitTiles;   // m-tile pairs per expert
+  const int HS = a.Kp / kTcStageK;
   uint8_t *ring_b = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);   // 1024-byte aligned
   uint8_t *ring_a = ring_b + kTcBStages * kTcBStageBytes;
 
@@ -501,10 +501,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
       mbar_init(&s.b_full[i], 1);
       mbar_init(&s.b_empty[i], kTcIssuers);
     }
-    for (int i = 0; i < kTcABufs; i++) {
-      mbar_init(&s.a_ready[i], 4);                 // the 4 warps of a decode set
-      mbar_init(&s.a_free[i], 1);
-    }
+    for (int j = 0; j < kTcIssuers; j++)
+      for (int p = 0; p < 2; p++) {
+        mbar_init(&s.a_ready[j][p], 4);            // the 4 warps of decode set j
+        mbar_init(&s.a_free[j][p], 1);
+      }
     for (int i = 0; i < 2; i++) {
       mbar_init(&s.d_full[i], kTcIssuers);
       mbar_init(&s.d_free[i], 4);                  // the 4 epilogue warps
@@ -534,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         const int o = a.gd[16 + E + d], o1 = a.gd[17 + E + d];
         s.off[d] = o;
         int cf;
-        cost = MT * mtile_cost(o1 - o, cols, rf, cf);
+        cost = MP * mtile_cost(o1 - o, cols, rf, cf);
       }
       int t1;
       const int pre = cta_scan_excl(cost, s.wsum, t1) + run;
@@ -548,8 +549,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
     __syncthreads();
     if (tid == 0) {
       const long long total = s.pre[n];
-      const TcUnit u0 = unit_at(s, MT, cols, rf, total * blockIdx.x / gridDim.x);
-      const TcUnit u1 = unit_at(s, MT, cols, rf, total * (blockIdx.x + 1) / gridDim.x);
+      const TcUnit u0 = unit_at(s, MP, cols, rf, total * blockIdx.x / gridDim.x);
+      const TcUnit u1 = unit_at(s, MP, cols, rf, total * (blockIdx.x + 1) / gridDim.x);
       s.range[0] = u0.d; s.range[1] = u0.mt; s.range[2] = u0.nc;
       s.range[3] = u1.d; s.range[4] = u1.mt; s.range[5] = u1.nc;
     }
@@ -560,13 +561,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
   const int *pairs = gd_pairs(a.gd, E);
 
   if (warp == kTcWProdA) {
-    // ------------------------------------------------ weights: half slices of 8 tiles (codes, scales)
+    // ------------------------------------------------ weights: a half slice of 16 tiles per stage
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       int ia = 0;
       bool ok = true;
-      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
-        const int e = s.expert[u.d], t0 = kTcTiles * u.mt;
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols)) {
+        const int e = s.expert[u.d], t0 = kTcUnitTiles * u.mt;
         for (int hs = 0; hs < HS; hs++, ia++) {
           const int slot = ia % kTcAStages;
           if (ia >= kTcAStages && !mbar_wait_bounded(&s.a_empty[slot], (uint32_t)(ia / kTcAStages - 1) & 1u)) {
@@ -578,44 +579,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
           // tiles past the region's last read as zeros
           mbar_arrive_expect_tx(&s.a_full[slot], (uint32_t)kTcAStageBytes);
           tma_load_4d(dst, &a.amap[0], 0, hs, t0, e, &s.a_full[slot], pol);
-          tma_load_4d(dst + kTcTiles * 2048, &a.amap[1], 0, hs, t0, e, &s.a_full[slot], pol);
+          tma_load_4d(dst + kTcUnitTiles * 2048, &a.amap[1], 0, hs, t0, e, &s.a_full[slot], pol);
         }
       }
       for (int j = (ia > kTcAStages ? ia - kTcAStages : 0); j < ia; j++)
         mbar_wait_bounded(&s.a_full[j % kTcAStages], (uint32_t)(j / kTcAStages) & 1u);
     }
   } else if (warp == kTcWProdB) {
-    // ------------------------------------------------ B rows: 64 k per stage
+    // ------------------------------------------------ B rows: 256 k per stage
     if (lane == 0) {
-      int gc = 0;
+      int gb = 0;
       bool ok = true;
-      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols)) {
         const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
         int rows, N, bi;
         unit_shape(np, rf, rows, N, bi);
         const int row0 = rf * (off + u.nc * cols);
-        for (int b = 0; b < KB; b++, gc++) {
-          const int slot = gc % kTcBStages;
-          if (gc >= kTcBStages && !mbar_wait_bounded(&s.b_empty[slot], (uint32_t)(gc / kTcBStages - 1) & 1u)) {
+        for (int hs = 0; hs < HS; hs++, gb++) {
+          const int slot = gb % kTcBStages;
+          if (gb >= kTcBStages && !mbar_wait_bounded(&s.b_empty[slot], (uint32_t)(gb / kTcBStages - 1) & 1u)) {
             atomicOr(a.flags, MOE_FLAG_TIMEOUT);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&s.b_full[slot], (uint32_t)((16 << bi) * kTcBK * 2));
-          tma_load_3d(ring_b + (size_t)slot * kTcBStageBytes, &a.bmap[bi], 0, row0, (kTcBK / 8) * b, &s.b_full[slot]);
+          mbar_arrive_expect_tx(&s.b_full[slot], (uint32_t)((16 << bi) * kTcStageK * 2));
+          tma_load_3d(ring_b + (size_t)slot * kTcBStageBytes, &a.bmap[bi], 0, row0, (kTcStageK / 8) * hs,
+                      &s.b_full[slot]);
         }
       }
-      for (int j = (gc > kTcBStages ? gc - kTcBStages : 0); j < gc; j++)
+      for (int j = (gb > kTcBStages ? gb - kTcBStages : 0); j < gb; j++)
         mbar_wait_bounded(&s.b_full[j % kTcBStages], (uint32_t)(j / kTcBStages) & 1u);
     }
   } else if (warp == kTcWMma || warp == kTcWMma + 1) {
-    // ------------------------------------------------ MMA issue: issuer j takes sub-chunks j, j + 2, ...
+    // ------------------------------------------------ MMA issue: issuer j computes m-tile j of each unit
     const int j = warp - kTcWMma;
     if (lane == 0) {
       const uint32_t bring = smem_u32(ring_b);
-      int gb = 0, ud = 0;                            // global B stage; this issuer's sub-chunk is 2 gb + j
+      int gs = 0, ud = 0;                            // global stage, unit
       bool ok = true;
-      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols), ud++) {
+      for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols), ud++) {
         const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
         int rows, N, bi;
         unit_shape(np, rf, rows, N, bi);
@@ -629,24 +631,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         // D f32, A and B f16, both K-major, N, M = 128
         const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((128u >> 4) << 24);
         const uint32_t dt = tbase + (uint32_t)(kTcDCol0 + 128 * j + 64 * db);
-        const uint64_t bd_lo = smem_desc(0u, br * 16u, 128u);   // LBO / SBO fields; start added per stage
-        for (int b = 0; b < KB; b++, gb++) {
-          const int gc = 2 * gb + j, ab = gc % kTcABufs, bs = gb % kTcBStages;
-          if (!mbar_wait_bounded(&s.a_ready[ab], (uint32_t)(gc / kTcABufs) & 1u) ||
-              !mbar_wait_bounded(&s.b_full[bs], (uint32_t)(gb / kTcBStages) & 1u)) {
+        const uint64_t bd_lo = smem_desc(0u, br * 16u, 128u);   // LBO / SBO fields; start added per step
+        for (int hs = 0; hs < HS && ok; hs++, gs++) {
+          const int bs = gs % kTcBStages;
+          if (!mbar_wait_bounded(&s.b_full[bs], (uint32_t)(gs / kTcBStages) & 1u)) {
             atomicOr(a.flags, MOE_FLAG_TIMEOUT);
             ok = false;
             break;
           }
-          tc_fence_after();
-          // this issuer's 64 k of the stage: k-groups 8 j .. 8 j + 7
-          const uint64_t bd0 = bd_lo | (uint64_t)(((bring + (uint32_t)(bs * kTcBStageBytes) + 128u * j * br) >> 4) & 0x3FFFu);
-          const uint32_t at = tbase + (uint32_t)(kTcACol0 + 32 * ab);
+          const uint32_t bstage = bring + (uint32_t)(bs * kTcBStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            tc_mma(dt, at + 8u * kk, bd0 + (uint64_t)(2u * kk * br), idesc, (uint32_t)(b | kk));
-          tc_commit(&s.a_free[ab]);
-          tc_commit(&s.b_empty[bs]);
+          for (int p = 0; p < 2; p++) {
+            if (!mbar_wait_bounded(&s.a_ready[j][p], (uint32_t)gs & 1u)) {
+              atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+              // sub-chunk 2p + h of the stage: k-groups 8 (2p + h) ..
+              const uint64_t bd0 = bd_lo | (uint64_t)(((bstage + 128u * (2 * p + h) * br) >> 4) & 0x3FFFu);
+              const uint32_t at = tbase + (uint32_t)(kTcACol0 + 128 * j + 64 * p + 32 * h);
+#pragma unroll
+              for (int kk = 0; kk < 4; kk++)
+                tc_mma(dt, at + 8u * kk, bd0 + (uint64_t)(2u * kk * br), idesc, (uint32_t)(hs | p | h | kk));
+            }
+            tc_commit(&s.a_free[j][p]);
+          }
+          if (ok) tc_commit(&s.b_empty[bs]);
         }
         if (ok) tc_commit(&s.d_full[db]);
       }
@@ -656,64 +669,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
     }
     __syncwarp();
   } else if (warp >= kTcWDec0 && warp < kTcWEpi0) {
-    // ------------------------------------------------ decode into tensor memory
+    // ------------------------------------------------ decode into tensor memory: set j feeds issuer j
     const int set = (warp - kTcWDec0) >> 2, wq = warp & 3;
-    const int Tl = 2 * wq + (lane >> 4), g = (lane >> 1) & 7, hi = lane & 1;
-    const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16);
+    const int Tl = kTcTiles * set + 2 * wq + (lane >> 4), g = (lane >> 1) & 7, hi = lane & 1;
+    const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16) + (uint32_t)(kTcACol0 + 128 * set);
     const uint32_t sel = hi ? 0x3232u : 0x1010u;  // this row's scale in both halves
-    int ia = 0;
+    int gs = 0;
     bool ok = true;
-    for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MT, cols)) {
-      for (int hs = 0; hs < HS; hs++, ia++) {
-        const int slot = ia % kTcAStages;
-        if (!mbar_wait_bounded(&s.a_full[slot], (uint32_t)(ia / kTcAStages) & 1u)) {
+    for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols)) {
+      for (int hs = 0; hs < HS; hs++, gs++) {
+        const int slot = gs % kTcAStages;
+        if (!mbar_wait_bounded(&s.a_full[slot], (uint32_t)(gs / kTcAStages) & 1u)) {
           atomicOr(a.flags, MOE_FLAG_TIMEOUT);
           ok = false;
           break;
         }
         const uint8_t *stg = ring_a + (size_t)slot * kTcAStageBytes;
-        // this set's sub-chunks of the stage: set and set + 2
-        const int ab0 = (4 * ia + set) % kTcABufs, ab1 = (4 * ia + set + 2) % kTcABufs;
-        const int use = (4 * ia + set) / kTcABufs;     // both buffers are on the same use
-        if (use > 0 && (!mbar_wait_bounded(&s.a_free[ab0], (uint32_t)(use - 1) & 1u) ||
-                        !mbar_wait_bounded(&s.a_free[ab1], (uint32_t)(use - 1) & 1u))) {
-          atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int h2 = 0; h2 < 2; h2++) {
-          const int sc = set + 2 * h2;               // 64-k sub-chunk of the stage
-          // lanes 4g + q of the sub-chunk's code group hold this row pair's
-          // words of its 4 k-steps; the scale unit of row pair g holds the
-          // (rowA, rowB) e4m3 bytes of each k-step
-          const uint8_t *cp = stg + Tl * 2048 + sc * 512 + g * 64;
-          uint4 cw[4];
-#pragma unroll
-          for (int q = 0; q < 4; q++) cw[q] = *reinterpret_cast<const uint4 *>(cp + 16 * q);
-          const uint2 sw =
-              *reinterpret_cast<const uint2 *>(stg + kTcTiles * 2048 + Tl * 256 + (sc >> 1) * 128 + g * 16 + (sc & 1) * 8);
-          uint32_t r[32];
-#pragma unroll
-          for (int jj = 0; jj < 4; jj++) {
-            const uint32_t s2 = __byte_perm(e4m3x2_to_f16x2(((jj < 2 ? sw.x : sw.y) >> (16 * (jj & 1))) & 0xFFFFu), 0u, sel);
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-              const uint32_t wv = (jj == 0 ? cw[q].x : jj == 1 ? cw[q].y : jj == 2 ? cw[q].z : cw[q].w) >> (8 * hi);
-              uint32_t c01, c89;
-              e2m1_bytes02(wv, c01, c89);
-              r[8 * jj + q] = hmul2_u32(c01, s2);      // elements 2q, 2q+1 of k-step jj
-              r[8 * jj + 4 + q] = hmul2_u32(c89, s2);  // elements 2q+8, 2q+9
-            }
+#pragma unroll 1
+        for (int p = 0; p < 2; p++) {
+          if (gs > 0 && !mbar_wait_bounded(&s.a_free[set][p], (uint32_t)(gs - 1) & 1u)) {
+            atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+            ok = false;
+            break;
           }
-          tc_st32(trow + (uint32_t)(kTcACol0 + 32 * (h2 ? ab1 : ab0)), r);
-        }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s.a_ready[ab0]);
-          mbar_arrive(&s.a_ready[ab1]);
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int sc = 2 * p + h;                // 64-k sub-chunk of the stage
+            // lanes 4g + q of the sub-chunk's code group hold this row pair's
+            // words of its 4 k-steps; the scale unit of row pair g holds the
+            // (rowA, rowB) e4m3 bytes of each k-step
+            const uint8_t *cp = stg + Tl * 2048 + sc * 512 + g * 64;
+            uint4 cw[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) cw[q] = *reinterpret_cast<const uint4 *>(cp + 16 * q);
+            const uint2 sw = *reinterpret_cast<const uint2 *>(stg + kTcUnitTiles * 2048 + Tl * 256 + (sc >> 1) * 128 +
+                                                              g * 16 + (sc & 1) * 8);
+            uint32_t r[32];
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+              const uint32_t s2 =
+                  __byte_perm(e4m3x2_to_f16x2(((jj < 2 ? sw.x : sw.y) >> (16 * (jj & 1))) & 0xFFFFu), 0u, sel);
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                const uint32_t wv = (jj == 0 ? cw[q].x : jj == 1 ? cw[q].y : jj == 2 ? cw[q].z : cw[q].w) >> (8 * hi);
+                uint32_t c01, c89;
+                e2m1_bytes02(wv, c01, c89);
+                r[8 * jj + q] = hmul2_u32(c01, s2);      // elements 2q, 2q+1 of k-step jj
+                r[8 * jj + 4 + q] = hmul2_u32(c89, s2);  // elements 2q+8, 2q+9
+              }
+            }
+            tc_st32(trow + (uint32_t)(64 * p + 32 * h), r);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.a_ready[set][p]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.a_empty[slot]);
@@ -722,14 +732,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
   } else if (warp >= kTcWEpi0) {
     // ------------------------------------------------ epilogue
     const int wq = warp & 3, et = tid - 32 * kTcWEpi0;
-    const int Tl = 2 * wq + (lane >> 4), g = (lane >> 1) & 7, hi = lane & 1;
+    const int g = (lane >> 1) & 7, hi = lane & 1;
     const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16);
     int ud = 0, cur = -1;
     float sc0 = 0.f, sc1 = 0.f;
-    for (TcUnit u = beg; unit_before(u, end); unit_next(s, u, MT, cols), ud++) {
+    for (TcUnit u = beg; unit_before(u, end); unit_next(s, u, MP, cols), ud++) {
       const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
       const int j0 = off + u.nc * cols;
-      const int T = kTcTiles * u.mt + Tl;            // packed tile of this lane's row
       if (u.d != cur) {
         cur = u.d;
         const float *sc = a.scalars + (size_t)s.expert[u.d] * 6;
@@ -755,38 +764,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      const uint32_t dt = trow + (uint32_t)(kTcDCol0 + 64 * db);
       const int ncol = np * rf;
-      for (int c0 = 0; c0 < ncol; c0 += 32) {
-        float v[32], v1[32];
-        tc_ld32(dt + (uint32_t)c0, v);                 // issuer 0: even 64-k sub-chunks
-        tc_ld32(dt + 128u + (uint32_t)c0, v1);         // issuer 1: odd ones
-#pragma unroll
-        for (int i = 0; i < 32; i++) v[i] += v1[i];
-        if (c0 + 32 >= ncol) {                       // the last read of this D buffer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s.d_free[db]);
-        }
-        if constexpr (MODE == 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i++) {
-            const int nn = c0 + i;
-            if (nn >= np) break;
-            const float up = __shfl_xor_sync(kFull, v[i], 1);
-            if (!hi && T < a.tiles) {
-              const float xs = s.cols[nn];
-              const float gg = v[i] * xs * sc0, uu = up * xs * sc1;
-              a.out[(size_t)s.colp[nn] * a.I + 8 * T + g] = s.colw[nn] * silu(gg) * uu;
-            }
+#pragma unroll 1
+      for (int mj = 0; mj < kTcIssuers; mj++) {
+        const int T = kTcUnitTiles * u.mt + kTcTiles * mj + 2 * wq + (lane >> 4);   // packed tile of this lane's row
+        const uint32_t dt = trow + (uint32_t)(kTcDCol0 + 128 * mj + 64 * db);
+        for (int c0 = 0; c0 < ncol; c0 += 32) {
+          float v[32];
+          tc_ld32(dt + (uint32_t)c0, v);
+          if (mj == kTcIssuers - 1 && c0 + 32 >= ncol) {   // the last read of this D buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.d_free[db]);
           }
-        } else {
+          if constexpr (MODE == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; i++) {
-            const int nn = (c0 >> 1) + i;
-            if (nn >= np) break;
-            if (T < a.tiles)
-              a.out[(size_t)s.colp[nn] * a.H + 16 * T + (lane & 15)] = (v[2 * i] + v[2 * i + 1]) * s.cols[nn] * sc0;
+            for (int i = 0; i < 32; i++) {
+              const int nn = c0 + i;
+              if (nn >= np) break;
+              const float up = __shfl_xor_sync(kFull, v[i], 1);
+              if (!hi && T < a.tiles) {
+                const float xs = s.cols[nn];
+                const float gg = v[i] * xs * sc0, uu = up * xs * sc1;
+                a.out[(size_t)s.colp[nn] * a.I + 8 * T + g] = s.colw[nn] * silu(gg) * uu;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+              const int nn = (c0 >> 1) + i;
+              if (nn >= np) break;
+              if (T < a.tiles)
+                a.out[(size_t)s.colp[nn] * a.H + 16 * T + (lane & 15)] = (v[2 * i] + v[2 * i + 1]) * s.cols[nn] * sc0;
+            }
           }
         }
       }
@@ -851,7 +861,7 @@ static TensorMapEncodeFn tensor_map_encoder() {
   return fn;
 }
 
-// Tensor maps of a B buffer [Kp/8][rows][8] f16: boxes of 16 k-groups of
+// Tensor maps of a B buffer [Kp/8][rows][8] f16: boxes of 32 k-groups of
 // 16, 32 and 64 rows of 8 elements.
 static cudaError_t encode_b_maps(CUtensorMap (&maps)[kTcBoxes], const void *base, int rows, int Kp) {
   const TensorMapEncodeFn enc = tensor_map_encoder();
@@ -859,7 +869,7 @@ static cudaError_t encode_b_maps(CUtensorMap (&maps)[kTcBoxes], const void *base
   for (int i = 0; i < kTcBoxes; i++) {
     const cuuint64_t dims[3] = {8, (cuuint64_t)rows, (cuuint64_t)(Kp / 8)};
     const cuuint64_t strides[2] = {16, (cuuint64_t)rows * 16};
-    const cuuint32_t box[3] = {8, (cuuint32_t)(16 << i), kTcBK / 8};
+    const cuuint32_t box[3] = {8, (cuuint32_t)(16 << i), kTcStageK / 8};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -872,7 +882,7 @@ static cudaError_t encode_b_maps(CUtensorMap (&maps)[kTcBoxes], const void *base
 // Tensor maps of one weight region (gate/up or down) of every expert, in
 // 8-byte elements: the codes [E][tiles][half slices][2048 B] and the scales
 // [E][tiles][half slices][256 B] of the packed tiles; a box is one half slice
-// of 8 consecutive tiles.
+// of 16 consecutive tiles.
 static cudaError_t encode_a_maps(CUtensorMap (&maps)[2], const uint8_t *packed, size_t region_off, int slices,
                                  int tiles, int tile_bytes, int E, size_t expert_bytes) {
   const TensorMapEncodeFn enc = tensor_map_encoder();
@@ -881,7 +891,7 @@ static cudaError_t encode_a_maps(CUtensorMap (&maps)[2], const uint8_t *packed, 
     const cuuint64_t inner = i == 0 ? 256 : 32;              // 2048 or 256 bytes
     const cuuint64_t dims[4] = {inner, (cuuint64_t)(2 * slices), (cuuint64_t)tiles, (cuuint64_t)E};
     const cuuint64_t strides[3] = {inner * 8, (cuuint64_t)tile_bytes, (cuuint64_t)expert_bytes};
-    const cuuint32_t box[4] = {(cuuint32_t)inner, 1, kTcTiles, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)inner, 1, kTcUnitTiles, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const uint8_t *base = packed + region_off + (i == 0 ? 0 : (size_t)slices * 4096);
     const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<uint8_t *>(base), dims, strides,
