@@ -451,9 +451,16 @@ def main():
     dn_avg = float(np.mean(dn_ms))
     hbm_peak, peak_src = measured_peaks()
     achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
-    traffic_per_expert = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
-    roofline = {"kernel": f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
-                          f"{'two tiles' if C <= 2 else 'one tile'} per stage)", "bound": "hbm",
+    if C > 8:
+        # grouped path: the stage events bracket dispatch, x-row prep and the gate/up GEMM
+        traffic_per_expert = ncu_traffic("grouped.cu", f"group_tc_gu_{args.config}")
+        kernel_label = ("group_tc_kernel<0> (grouped gate/up + SwiGLU on tcgen05; the timed span also holds "
+                        "the dispatch and x-row kernels)")
+    else:
+        traffic_per_expert = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
+        kernel_label = (f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
+                        f"{'two tiles' if C <= 2 else 'one tile'} per stage)")
+    roofline = {"kernel": kernel_label, "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": peak_src,
                 "traffic": None if traffic_per_expert is None else traffic_per_expert * gu_units,

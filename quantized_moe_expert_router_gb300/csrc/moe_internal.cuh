@@ -22,6 +22,7 @@ constexpr int kGroupTokens = 512;        // tokens per pass of the grouped (expe
 constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
+constexpr int kRouteSplits = 4;          // route, C > 8: K ranges of the logits GEMM (partials summed in order)
 constexpr int kGemvSmemBytes = 211968;   // dynamic shared memory of one expert-GEMV CTA (+ ~20 KB static)
 constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped-GEMM CTA at most (+ ~12 KB static)
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
@@ -45,7 +46,7 @@ struct WsLayout {
   size_t hamax;       // uint32 [kGemvTokens * k]       max |h| per (token, slot) as float bits
   size_t ypair;       // float  [kGemvTokens * k][H]    D_e h per (token, slot)
   // C > 8 only (0 otherwise): Cg = min(C, kGroupTokens) tokens, Pg = Cg * k pairs
-  size_t glogits;     // float  [C][E]                  router logits
+  size_t glogits;     // float  [kRouteSplits][C][E]    router logit partials; logits in partial 0
   size_t gd;          // int    n, then expert [E], off [E + 1], pairs [Pg]   expert-major dispatch
   size_t xinv;        // float  [Cg]                    2^-s of each token's f16 scale
   size_t xg;          // f16    [Hp / 8][Pg][8]         x rows of the pairs in dispatch order
@@ -97,7 +98,7 @@ inline WsLayout ws_layout(const moe_layer &L, int C) {
   w.ypair = take(sizeof(float) * pairs * H);
   if (C > kGemvTokens) {
     const size_t Cg = C < kGroupTokens ? C : kGroupTokens, Pg = Cg * k;
-    w.glogits = take(sizeof(float) * (size_t)C * E);
+    w.glogits = take(sizeof(float) * kRouteSplits * (size_t)C * E);
     w.gd = take(sizeof(int) * (16 + E + (E + 1) + Pg));
     w.xinv = take(sizeof(float) * Cg);
     w.xg = take(2 * Pg * (size_t)L.Hp);

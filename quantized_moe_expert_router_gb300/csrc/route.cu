@@ -146,16 +146,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
 }
 
 // ------------------------------------------------------------ large C
-// logits[C][E] = X[C][H] Wr^T + bias.  64 tokens x 64 experts per CTA,
-// 256 threads with 4 x 4 outputs each, K tiles of 32 staged in shared memory.
+// Partial logits part[z][C][E] = X[C][K_z] Wr[E][K_z]^T over the z-th of
+// kRouteSplits contiguous ranges of 32-wide K tiles.  64 tokens x 64
+// experts per CTA, 256 threads with 4 x 4 outputs each, K tiles of 32 staged
+// in shared memory (k-major, so a thread reads its 4 tokens and 4 experts of
+// one k as two 16-byte loads).
 __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs a) {
-  __shared__ float Xs[32][64 + 4];
-  __shared__ float Ws[32][64 + 4];
+  __shared__ __align__(16) float Xs[32][64 + 4];
+  __shared__ __align__(16) float Ws[32][64 + 4];
   pdl_wait();
   const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int KT = a.H / 32;
+  const int kt0 = split_point(KT, blockIdx.z, gridDim.z), kt1 = split_point(KT, blockIdx.z + 1, gridDim.z);
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < a.H; k0 += 32) {
+  for (int kt = kt0; kt < kt1; kt++) {
+    const int k0 = 32 * kt;
     for (int i = tid; i < 64 * 32; i += 256) {
       const int r = i >> 5, c = i & 31;
       const int t = t0 + r, e = e0 + r;
@@ -165,9 +171,9 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs
     __syncthreads();
 #pragma unroll 8
     for (int c = 0; c < 32; c++) {
-      float xv[4], wv[4];
-#pragma unroll
-      for (int i = 0; i < 4; i++) { xv[i] = Xs[c][ty * 4 + i]; wv[i] = Ws[c][tx * 4 + i]; }
+      const float4 x4 = *reinterpret_cast<const float4 *>(&Xs[c][ty * 4]);
+      const float4 w4 = *reinterpret_cast<const float4 *>(&Ws[c][tx * 4]);
+      const float xv[4] = {x4.x, x4.y, x4.z, x4.w}, wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int i = 0; i < 4; i++)
 #pragma unroll
@@ -175,19 +181,29 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs
     }
     __syncthreads();
   }
+  float *part = a.logits + (size_t)blockIdx.z * a.C * a.E;
 #pragma unroll
   for (int i = 0; i < 4; i++)
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
-      if (t < a.C && e < a.E) a.logits[(size_t)t * a.E + e] = acc[i][j] + (a.bias ? a.bias[e] : 0.f);
+      if (t < a.C && e < a.E) part[(size_t)t * a.E + e] = acc[i][j];
     }
 }
 
+// One CTA per token: logits = the partials summed in split order, plus the
+// bias (written over partial 0), then the top-k of the row.
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const RouteArgs a) {
   __shared__ SelectSmem tk;
   const int t = blockIdx.x;
-  cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
+  float *lg = a.logits + (size_t)t * a.E;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    float v = lg[e];
+    for (int z = 1; z < kRouteSplits; z++) v += lg[(size_t)z * a.C * a.E + e];
+    lg[e] = v + (a.bias ? a.bias[e] : 0.f);
+  }
+  __syncthreads();
+  cta_select_topk<kRouteWarps * 32>(lg, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
 }
 
 static size_t fused_smem(int ct, int H) { (void)ct; (void)H; return kRouteSmemBytes; }
@@ -219,7 +235,7 @@ cudaError_t launch_route_fused(const RouteArgs &a, int grid, cudaStream_t stream
 }
 
 cudaError_t launch_route_batched(const RouteArgs &a, cudaStream_t stream) {
-  dim3 g1((a.E + 63) / 64, (a.C + 63) / 64);
+  dim3 g1((a.E + 63) / 64, (a.C + 63) / 64, kRouteSplits);
   route_logits_tiled_kernel<<<g1, 256, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
