@@ -159,16 +159,33 @@ __global__ void __launch_bounds__(256) route_logits_tiled_kernel(const RouteArgs
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int KT = a.H / 32;
   const int kt0 = split_point(KT, blockIdx.z, gridDim.z), kt1 = split_point(KT, blockIdx.z + 1, gridDim.z);
+  // tile loads: X row rx (8 bf16 at kx), W rows rw and rw + 32 (4 floats at kw);
+  // the next tile's loads are in flight while the current one is multiplied
+  const int rx = tid >> 2, kx = (tid & 3) * 8, rw = tid >> 3, kw = (tid & 7) * 4;
+  const bool xin = t0 + rx < a.C, win0 = e0 + rw < a.E, win1 = e0 + rw + 32 < a.E;
+  const uint16_t *xrow = a.x + (size_t)(t0 + rx) * a.H + kx;
+  const float *wrow0 = a.w_router + (size_t)(e0 + rw) * a.H + kw, *wrow1 = wrow0 + (size_t)32 * a.H;
+  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+  float4 wr0 = make_float4(0.f, 0.f, 0.f, 0.f), wr1 = wr0;
+  auto load = [&](int kt) {
+    const int k0 = 32 * kt;
+    if (xin) xr = __ldg(reinterpret_cast<const uint4 *>(xrow + k0));
+    if (win0) wr0 = __ldg(reinterpret_cast<const float4 *>(wrow0 + k0));
+    if (win1) wr1 = __ldg(reinterpret_cast<const float4 *>(wrow1 + k0));
+  };
+  if (kt0 < kt1) load(kt0);
   float acc[4][4] = {};
   for (int kt = kt0; kt < kt1; kt++) {
-    const int k0 = 32 * kt;
-    for (int i = tid; i < 64 * 32; i += 256) {
-      const int r = i >> 5, c = i & 31;
-      const int t = t0 + r, e = e0 + r;
-      Xs[c][r] = (t < a.C) ? __uint_as_float((uint32_t)a.x[(size_t)t * a.H + k0 + c] << 16) : 0.f;
-      Ws[c][r] = (e < a.E) ? a.w_router[(size_t)e * a.H + k0 + c] : 0.f;
+    const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      Xs[kx + 2 * j][rx] = __uint_as_float(xw[j] << 16);
+      Xs[kx + 2 * j + 1][rx] = __uint_as_float(xw[j] & 0xFFFF0000u);
     }
+    Ws[kw][rw] = wr0.x; Ws[kw + 1][rw] = wr0.y; Ws[kw + 2][rw] = wr0.z; Ws[kw + 3][rw] = wr0.w;
+    Ws[kw][rw + 32] = wr1.x; Ws[kw + 1][rw + 32] = wr1.y; Ws[kw + 2][rw + 32] = wr1.z; Ws[kw + 3][rw + 32] = wr1.w;
     __syncthreads();
+    if (kt + 1 < kt1) load(kt + 1);
 #pragma unroll 8
     for (int c = 0; c < 32; c++) {
       const float4 x4 = *reinterpret_cast<const float4 *>(&Xs[c][ty * 4]);
