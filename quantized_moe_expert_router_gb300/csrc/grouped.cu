@@ -444,11 +444,12 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar,
+                                            uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
@@ -563,11 +564,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
   if (warp == kTcWProdA) {
     // ------------------------------------------------ weights: a half slice of 16 tiles per stage
     if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
+      // the weights of an m-tile pair are read once per column chunk, one
+      // chunk after the other: all but the last pass leave them in L2
+      const uint64_t pol_last = l2_evict_first_policy(), pol_again = l2_evict_normal_policy();
       int ia = 0;
       bool ok = true;
       for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols)) {
         const int e = s.expert[u.d], t0 = kTcUnitTiles * u.mt;
+        const uint64_t pol = u.nc + 1 < unit_nch(s, u.d, cols) ? pol_again : pol_last;
         for (int hs = 0; hs < HS; hs++, ia++) {
           const int slot = ia % kTcAStages;
           if (ia >= kTcAStages && !mbar_wait_bounded(&s.a_empty[slot], (uint32_t)(ia / kTcAStages - 1) & 1u)) {
@@ -588,6 +592,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
   } else if (warp == kTcWProdB) {
     // ------------------------------------------------ B rows: 256 k per stage
     if (lane == 0) {
+      // every m-tile pair of an expert reads the same B rows: keep them in L2
+      const uint64_t pol = l2_evict_last_policy();
       int gb = 0;
       bool ok = true;
       for (TcUnit u = beg; ok && unit_before(u, end); unit_next(s, u, MP, cols)) {
@@ -604,7 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
           }
           mbar_arrive_expect_tx(&s.b_full[slot], (uint32_t)((16 << bi) * kTcStageK * 2));
           tma_load_3d(ring_b + (size_t)slot * kTcBStageBytes, &a.bmap[bi], 0, row0, (kTcStageK / 8) * hs,
-                      &s.b_full[slot]);
+                      &s.b_full[slot], pol);
         }
       }
       for (int j = (gb > kTcBStages ? gb - kTcBStages : 0); j < gb; j++)
@@ -786,7 +792,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
               if (!hi && T < a.tiles) {
                 const float xs = s.cols[nn];
                 const float gg = v[i] * xs * sc0, uu = up * xs * sc1;
-                a.out[(size_t)s.colp[nn] * a.I + 8 * T + g] = s.colw[nn] * silu(gg) * uu;
+                __stcs(a.out + (size_t)s.colp[nn] * a.I + 8 * T + g, s.colw[nn] * silu(gg) * uu);
               }
             }
           } else {
@@ -795,7 +801,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
               const int nn = (c0 >> 1) + i;
               if (nn >= np) break;
               if (T < a.tiles)
-                a.out[(size_t)s.colp[nn] * a.H + 16 * T + (lane & 15)] = (v[2 * i] + v[2 * i + 1]) * s.cols[nn] * sc0;
+                __stcs(a.out + (size_t)s.colp[nn] * a.H + 16 * T + (lane & 15), (v[2 * i] + v[2 * i + 1]) * s.cols[nn] * sc0);
             }
           }
         }
