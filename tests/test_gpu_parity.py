@@ -209,6 +209,16 @@ def test_grouped_path_parity(E, k, H, I, C):
     check_layer(L, x, f"grouped E{E} k{k} H{H} I{I} C{C}")
 
 
+@pytest.mark.parametrize("C", [520, 1100])
+def test_grouped_path_multi_pass_parity(C):
+    # more than 512 tokens: passes of 512 (and a ragged last one); ~65 pairs
+    # per expert, so the grouped GEMMs split experts into several column
+    # chunks (64 pairs for gate/up, 32 for down)
+    L = GpuLayer(32, 4, 256, 192, C, seed=9)
+    x = gapped_tokens(9, 0, C, 256, L.Wr, 4)
+    check_layer(L, x, f"grouped multi-pass C={C}")
+
+
 @pytest.mark.parametrize("C", [1, 3, 8, 11])
 def test_route_forward_equals_route_then_forward(C):
     # the one-call layer gives the separate calls' results bit for bit, call
