@@ -201,7 +201,7 @@ def test_odd_shapes_parity(E, k, H, I, C):
 
 
 @pytest.mark.parametrize("E,k,H,I,C", [(32, 4, 256, 192, 40), (12, 3, 64, 128, 20), (40, 8, 576, 320, 64),
-                                       (7, 7, 192, 1088, 9)])
+                                       (7, 7, 192, 1088, 9), (8, 1, 4096, 4096, 9), (16, 2, 64, 4096, 12)])
 def test_grouped_path_parity(E, k, H, I, C):
     # C > 8 runs expert-major: every expert's weights once for all its tokens
     L = GpuLayer(E, k, H, I, C, seed=6)
@@ -254,12 +254,13 @@ def _forward(h, x_bits, ids, w, canon_h, ws_tokens=8):
     return y.cpu().numpy().astype(np.float64)
 
 
-def test_band_and_slice_partials_sum_to_the_layer():
+@pytest.mark.parametrize("C", [3, 20])
+def test_band_and_slice_partials_sum_to_the_layer(C):
     # the two splits of the layer over ranks (expert bands; intermediate
     # column slices), each partial computed by the CUDA path on its own
-    # layer, summed in rank order
+    # layer, summed in rank order (C = 20 runs the grouped path)
     from quantized_moe_expert_router_gb300 import partition
-    E, k, H, I, C = 32, 4, 256, 192, 3
+    E, k, H, I = 32, 4, 256, 192
     canon = synth.canonical_layer(0, 0, E, H, I)
     Wr = synth.router_weights(0, 0, E, H)
     x = gapped_tokens(0, 0, C, H, Wr, k)
@@ -267,12 +268,13 @@ def test_band_and_slice_partials_sum_to_the_layer():
     y_o = oracle.moe_forward(canon, x, ids, w)
     total = np.zeros_like(y_o)
     for lo, hi in partition.expert_bands(E, 2):
-        total += _forward(moe.Layer(hi - lo, k, H, I, 8), x, partition.band_ids(ids, lo, hi), w,
-                          partition.band_weights(canon, lo, hi))
+        total += _forward(moe.Layer(hi - lo, k, H, I, max(C, 8)), x, partition.band_ids(ids, lo, hi), w,
+                          partition.band_weights(canon, lo, hi), ws_tokens=max(C, 8))
     assert_close(total, y_o, "expert bands")
     total = np.zeros_like(y_o)
     for i0, i1 in partition.intermediate_slices(I, 2):
-        total += _forward(moe.Layer(E, k, H, i1 - i0, 8), x, ids, w, partition.slice_weights(canon, i0, i1))
+        total += _forward(moe.Layer(E, k, H, i1 - i0, max(C, 8)), x, ids, w, partition.slice_weights(canon, i0, i1),
+                          ws_tokens=max(C, 8))
     assert_close(total, y_o, "intermediate slices")
 
 
@@ -301,6 +303,35 @@ def test_bad_and_duplicate_ids_are_flagged_and_skipped():
     y1 = oracle.moe_forward(L.host_weights(range(32)), x_bits[1:], np.array([[3, 7, 8]], np.int32),
                             np.array([[0.25, 0.25, 0.25]]))
     assert_close(y.cpu().numpy()[1:], y1, "duplicate id")
+    assert moe.moe_get_device_status(L.h, L.ws) == 0    # cleared
+
+
+def test_grouped_bad_duplicate_and_absent_ids():
+    # C > 8 (expert-major dispatch): a bad id and a repeated id are flagged
+    # and skipped, negative ids are absent slots, a token with no slot left
+    # gets a zero output
+    C, k = 12, 4
+    L = GpuLayer(32, k, 256, 192, C, seed=4)
+    x_bits = gapped_tokens(4, 0, C, 256, L.Wr, k)
+    ids_h, w_h, _ = oracle.route(oracle.router_logits(L.Wr, x_bits), k)
+    ids_h = ids_h.astype(np.int32).copy()
+    w_h = w_h.astype(np.float32).copy()
+    ids_h[0, 2] = 40                       # bad
+    ids_h[1, 3] = ids_h[1, 0]              # repeat of slot 0
+    ids_h[2, 1] = -1                       # absent
+    ids_h[3, :] = -1                       # nothing left
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV)
+    y = torch.empty((C, 256), dtype=torch.float32, device=DEV)
+    moe.moe_forward(L.h, x, C, torch.from_numpy(ids_h).to(DEV), torch.from_numpy(w_h).to(DEV), L.packed, y, L.ws)
+    flags = moe.moe_get_device_status(L.h, L.ws)
+    assert flags & moe.FLAG_BAD_EXPERT_ID and flags & moe.FLAG_DUPLICATE_ID
+    keep = (ids_h >= 0) & (ids_h < 32)
+    keep[1, 3] = False
+    y_o = oracle.moe_forward(L.host_weights(range(32)), x_bits, np.where(keep, ids_h, 0).astype(np.int32),
+                             np.where(keep, w_h, 0.0))
+    yg = y.cpu().numpy()
+    assert (yg[3] == 0).all()
+    assert_close(yg, y_o, "grouped bad / repeated / absent ids")
     assert moe.moe_get_device_status(L.h, L.ws) == 0    # cleared
 
 
