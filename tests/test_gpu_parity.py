@@ -441,6 +441,31 @@ def test_k3_grouped_zipf_sampled_parity(k3_layer):
         assert_close(y[t:t + 1], oy, f"k3 grouped zipf token {t}")
 
 
+def test_k3_prefill512_sampled_parity(k3_layer):
+    # the prefill workload as the bench runs it: 512 Zipf-routed tokens in one
+    # call (one grouped pass; hot experts split into several column chunks);
+    # every token's ids and weights are checked, the outputs of a sample
+    L = k3_layer
+    C = 512
+    v = _retarget(L, moe.Layer(896, 16, 3584, 3072, C), 16)
+    v.ws = moe.alloc_workspace(v.h, C)
+    v.Wr = synth.router_weights(0, 0, 896, 3584, synth.ZIPF_ROUTER_STD)
+    v.bias = synth.zipf_bias(0, 0, 896)
+    v.Wr_d = torch.from_numpy(v.Wr).to(DEV)
+    v.bias_d = torch.from_numpy(v.bias).to(DEV)
+    x = gapped_tokens(5, 0, C, 3584, v.Wr, 16, bias=v.bias)
+    ids, w, y = v.run_fused(x)
+    assert moe.moe_get_device_status(v.h, v.ws) == 0
+    oids, ow, gap = oracle.route(oracle.router_logits(v.Wr, x, v.bias), 16)
+    assert (ids == oids).all()
+    np.testing.assert_allclose(w, ow, rtol=2e-5, atol=1e-7)
+    counts = np.bincount(ids.ravel(), minlength=896)
+    assert counts.max() > 64                      # a gate/up unit holds 64 pairs: several chunks
+    for t in (0, 200, 511):
+        _, _, _, oy = v.oracle(x[t:t + 1])
+        assert_close(y[t:t + 1], oy, f"k3 prefill512 token {t}")
+
+
 @pytest.mark.parametrize("C", [1, 7])
 def test_k3_zipf_routing_parity(k3_layer, C):
     # the 8-layer workload's routing: a Zipf router bias (per-layer permutation
