@@ -20,33 +20,34 @@
 //   group_tc_kernel<1>      down -> per-pair partial outputs
 //   group_combine_kernel    y[t] = sum of t's pairs in ascending expert id
 //
-// group_tc_kernel.  A unit is (expert d, m-tile mt, column chunk nc): 128
-// weight rows (8 packed tiles of 16 rows) times up to 128 B rows (gate/up:
-// 128 pairs; down: the hi and lo rows of 64 pairs) over the whole K, so every
-// unit is a complete dot product and units are independent.  Units are
-// weighted (streaming and decoding a unit's weights, plus its MMA columns)
-// and cut into one contiguous range per CTA.  One CTA per SM, 16 warps:
-//   warp 0     bulk copies of the weights, a half slice (256 k) of 8 tiles
-//              per stage, into a ring of shared-memory stages;
-//   warp 1     3-D TMA loads of the B rows, 64 k per stage: the global B
-//              buffers are [K/8][rows][8] f16, so a box of (8, R, 8) lands as
-//              eight k-groups of R rows of 16 bytes, which is the K-major,
-//              unswizzled core-matrix layout of the MMA's B operand;
-//   warp 2     owns tensor memory and issues tcgen05.mma kind::f16 (M=128,
-//              N = the unit's B rows rounded up to 16, K=16): A from tensor
-//              memory, B from shared memory, fp32 D in tensor memory (two
-//              buffers of 128 columns, so the epilogue of one unit overlaps
-//              the MMAs of the next);
-//   warps 4-11 decode: two sets of four warps (warp w reaches tensor-memory
-//              lanes 32 (w % 4) ..); a thread owns one weight row, turns 64 k
-//              of e2m1 codes into f16 (cvt.rn.f16x2.e2m1x2), multiplies by
-//              the e4m3 block scales (exact: at most 6 significant bits) and
-//              stores them into one of 8 A buffers of 32 columns
-//              (tcgen05.st); set s takes the 64-k sub-chunks s and s + 2 of
-//              every stage;
-//   warps 12-15 epilogue: read D with tcgen05.ld, apply the tensor scales,
-//              the f16 scales of x or h and (gate/up) SwiGLU and the router
-//              weight, and store per-pair rows.
+// group_tc_kernel.  A unit is (expert d, pair of 128-row m-tiles, chunk of
+// the expert's pairs: 64 for gate/up, one B row each; 32 for down, their hi
+// and lo B rows) over the whole K, so every unit is a complete dot product and
+// units are independent.  Units are weighted (12 + one per 16 B rows) and cut
+// into one contiguous range per CTA.  One CTA per SM, 16 warps:
+//   warp 0      the weights: each 256-k half slice of the unit's 16 packed
+//               tiles (36 KB) by two 4-D tensor-map loads (codes, scales) into
+//               a 3-stage ring; evict-first on the last pass over an m-tile
+//               pair, normal L2 priority while later chunks will read it again;
+//   warp 1      the B rows for the same 256 k by one 3-D box into a 3-stage
+//               ring (evict-last: every m-tile pair reads them): the global B
+//               buffers are [K/8][rows][8] f16, so a box (8, R, 32) lands as
+//               32 k-groups of R rows of 16 bytes, the K-major, unswizzled
+//               core-matrix layout of the MMA's B operand;
+//   warps 2, 3  MMA issuers, one per m-tile: tcgen05.mma kind::f16 (M=128,
+//               N = the unit's B rows rounded up to 16, K=16), A from tensor
+//               memory, B from shared memory, fp32 D in tensor memory (two
+//               buffers of 64 columns per issuer, so the epilogue of a unit
+//               overlaps the MMAs of the next); warp 2 owns tensor memory;
+//   warps 4-11  decode: set j (4 warps; warp w reaches tensor-memory lanes
+//               32 (w % 4) ..) feeds m-tile j; a thread owns one weight row,
+//               turns 64 k of e2m1 codes into f16 (cvt.rn.f16x2.e2m1x2),
+//               multiplies by the e4m3 block scales (exact: at most 6
+//               significant bits) and stores them with tcgen05.st into its
+//               m-tile's A buffers (two halves of 128 k per stage);
+//   warps 12-15 epilogue: read D with tcgen05.ld, apply the tensor scale, the
+//               2^-s of x or h and (gate/up) SwiGLU and the router weight, and
+//               store per-pair rows with streaming stores.
 // Weight row to tensor-memory lane: lane 32 q + l (warp quadrant q, lane l)
 // holds row 8 (l & 1) + ((l >> 1) & 7) of packed tile 2 q + (l >> 4) of the
 // m-tile: rowA (gate; down row 2p) for even l, rowB (up; down row 2p + 1) for
@@ -54,7 +55,7 @@
 // down outputs are 32 consecutive rows.
 // Every wait is bounded (about two seconds of %globaltimer): on expiry the
 // waiting role sets MOE_FLAG_TIMEOUT and stops; the producers then wait
-// (bounded) for their copies in flight and the MMA warp for its MMAs before
+// (bounded) for their copies in flight and each MMA warp for its MMAs before
 // tensor memory is released.  The sums over K run in the MMA's fixed order
 // and over a token's experts in ascending id order, so results are bitwise
 // reproducible.
