@@ -220,7 +220,7 @@ def run_reference(args, cfg, rank):
     x_all = synth.tokens(args.seed, 0, max(1, args.steps + args.warmup), H) if args.steps + args.warmup <= 64 \
         else synth.tokens(args.seed, 0, 64, H)
     per_token = None
-    warm = min(args.warmup, 1)
+    warm = min(args.warmup, 3)                     # oracle warm-up steps, capped (each is a whole token)
     for t in range(warm):
         oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, x_all[t:t + 1])
     steps_done, elapsed = 0, 0.0
@@ -242,7 +242,9 @@ def run_reference(args, cfg, rank):
                          "sample": f"{steps_done} whole token(s) of the workload (router, top-k, "
                                    f"{k} experts), single-threaded float64 C"},
         "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": ("step count capped by a 150 s budget" if steps_done < args.steps else ""),
+        "note": "; ".join(n_ for n_ in (("step count capped by a 150 s budget" if steps_done < args.steps else ""),
+                                        (f"warm-up capped at {warm} oracle steps" if warm < args.warmup else ""))
+                          if n_),
     }
     print(json.dumps(line), flush=True)
 
