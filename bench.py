@@ -520,7 +520,10 @@ def main():
             "e2e": e2e,
             # per step: the router (one kernel, two for C > 8) and, per group of
             # 8 tokens, the gate/up, down and combine kernels
-            "gpu_launches": args.steps * NL * ((1 if C <= 8 else 2) + 3 * ((C + 7) // 8)),
+            # per layer call: C <= 8: fused router, gate/up, down, combine; C > 8: router
+            # logits and top-k, then per pass of <= 512 tokens dispatch, x prep, x rows,
+            # gate/up, h rows, down, combine
+            "gpu_launches": args.steps * NL * (4 if C <= 8 else 2 + 7 * ((C + 511) // 512)),
             "clocks": clocks,
             "host_s": t_host,
             "device_flags": flags,
