@@ -518,8 +518,6 @@ def main():
             **({"routing": zipf_stats} if zipf_stats else {}),
             "roofline": roofline,
             "e2e": e2e,
-            # per step: the router (one kernel, two for C > 8) and, per group of
-            # 8 tokens, the gate/up, down and combine kernels
             # per layer call: C <= 8: fused router, gate/up, down, combine; C > 8: router
             # logits and top-k, then per pass of <= 512 tokens dispatch, x prep, x rows,
             # gate/up, h rows, down, combine
