@@ -41,3 +41,21 @@ def test_our_arm_fails_without_a_gpu():
     r = _run("--config", "tiny", "--steps", "1", "--warmup", "3", "--no-cpu-baseline")
     assert r.returncode != 0
     assert not r.stdout.strip().startswith("{"), "our arm printed a result without a GPU"
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # N = 2 ranks on one node: rank 0 alone runs the oracle and prints; the
+    # other rank exits 0 without work
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
