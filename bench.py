@@ -12,7 +12,9 @@ batch 1.
 Timed region: K steps replayed from CUDA graphs (16 rotating token sets, so
 the routed experts change every step; the 297 MB of expert bytes a step reads
 exceed the 129 MB L2), bracketed by barrier + synchronize, timed with CUDA
-events, max over ranks.  Under torchrun each rank runs its own replica of the
+events, max over ranks.  Every graph is replayed once before timing, and the
+K steps are timed in three windows: the line reports the median window and
+the spread.  Under torchrun each rank runs its own replica of the
 layer on its own tokens (weak scaling, no collective on the data path).
 
 The JSON line also carries: the gate/up kernel's roofline (algorithmic bytes /
@@ -151,29 +153,75 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def ncu_traffic(kernel_file, tag):
-    """DRAM bytes per unit from a committed ncu summary, if the kernel source
-    is unchanged since the capture (sha256 recorded in the summary)."""
+# every source file that goes into a kernel: the .cu and the headers it includes
+KERNEL_SOURCES = {
+    "expert_gemv.cu": ("csrc/expert_gemv.cu", "csrc/gemv_core.cuh", "csrc/moe_internal.cuh", "csrc/kernels.h",
+                       "../include/moe.h"),
+    "grouped.cu": ("csrc/grouped.cu", "csrc/gemv_core.cuh", "csrc/moe_internal.cuh", "csrc/kernels.h",
+                   "../include/moe.h"),
+}
+
+
+def kernel_sources_sha256(kernel_file):
+    """sha256 over the kernel's source files (the .cu and its headers, in a
+    fixed order): the key under which an ncu summary stays valid."""
     import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel_file]:
+        with open(os.path.join(ROOT, "quantized_moe_expert_router_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel_file, tag):
+    """DRAM bytes per unit from a committed ncu summary, if none of the
+    kernel's source files has changed since the capture (their combined
+    sha256 is recorded in the summary).  Returns (bytes, source) or
+    (None, reason)."""
     prof = os.path.join(ROOT, "profiles", f"{tag}.md")
     if not os.path.exists(prof):
-        return None
+        return None, f"no ncu summary profiles/{tag}.md"
     txt = open(prof).read()
     m = re.search(r"dram_bytes_per_expert:\s*([0-9.eE+]+)", txt)
-    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    h = re.search(r"sources_sha256:\s*([0-9a-f]{64})", txt)
     if not m or not h:
-        return None
-    src = open(os.path.join(ROOT, "quantized_moe_expert_router_gb300", "csrc", kernel_file), "rb").read()
-    if hashlib.sha256(src).hexdigest() != h.group(1):
-        return None
-    return float(m.group(1))
+        return None, f"profiles/{tag}.md records no DRAM bytes or source hash"
+    if kernel_sources_sha256(kernel_file) != h.group(1):
+        return None, f"profiles/{tag}.md was captured on other kernel sources"
+    return float(m.group(1)), (f"ncu dram__bytes_read.sum + dram__bytes_write.sum per expert from "
+                               f"profiles/{tag}.md (sources sha256 {h.group(1)[:12]}), times the experts "
+                               f"of one launch")
+
+
+def host_cpu():
+    """(cores this process may use, CPU model name) of the host."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return cores, model
 
 
 # ---------------------------------------------------------------- oracle legs
 
-def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits):
-    """Time the float64 oracle (single thread) on whole tokens of the workload
-    until ``budget_s`` is used (at least one token).  Returns tokens/s."""
+def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits, threads=1):
+    """Time the float64 oracle on whole tokens of the workload, one token after
+    the other, until ``budget_s`` is used (at least one token): router logits
+    and top-k on one thread, the token's expert FFNs on ``threads`` threads
+    (oracle_moe_forward_mt spreads its (token, slot) evaluations; one thread
+    runs the plain loop).  Returns (tokens, seconds)."""
     import oracle
     done, t_total = 0, 0.0
     for t in range(x_bits.shape[0]):
@@ -186,7 +234,7 @@ def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits):
         weights = weights_for(sel)                       # input staging, not timed
         t_prep = time.perf_counter() - t_prep0
         remap = {e: i for i, e in enumerate(sel)}
-        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w)
+        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads)
         t_total += time.perf_counter() - t0 - t_prep
         done += 1
         if t_total >= budget_s:
@@ -219,15 +267,16 @@ def run_reference(args, cfg, rank):
     # whole run stays within a few minutes
     x_all = synth.tokens(args.seed, 0, max(1, args.steps + args.warmup), H) if args.steps + args.warmup <= 64 \
         else synth.tokens(args.seed, 0, 64, H)
-    per_token = None
+    threads = min(oracle.default_threads(), k)     # a step is one token: k expert FFNs at most in parallel
+    cores, model = host_cpu()
     warm = min(args.warmup, 3)                     # oracle warm-up steps, capped (each is a whole token)
     for t in range(warm):
-        oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, x_all[t:t + 1])
+        oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, x_all[t:t + 1], threads)
     steps_done, elapsed = 0, 0.0
     budget = 150.0
     for s in range(args.steps):
         xb = x_all[(warm + s) % x_all.shape[0]: (warm + s) % x_all.shape[0] + 1]
-        n, dt = oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, xb)
+        n, dt = oracle_sample(cfg, args.seed, 0, weights_for, 0.0, Wr, bias, xb, threads)
         steps_done += 1
         elapsed += dt
         if elapsed >= budget:
@@ -238,9 +287,10 @@ def run_reference(args, cfg, rank):
         "steps": steps_done, "warmup": warm, "ms_per_step": 1e3 * elapsed / steps_done,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": cfg["workload"], "tokens_per_step": 1},
-        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{steps_done} whole token(s) of the workload (router, top-k, "
-                                   f"{k} experts), single-threaded float64 C"},
+        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "host_cores": cores, "cpu_model": model,
+                         "sample": f"{steps_done} whole token(s) of the workload (router and top-k on one "
+                                   f"thread, the {k} expert FFNs on {threads} threads), float64 C oracle"},
         "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "; ".join(n_ for n_ in (("step count capped by a 150 s budget" if steps_done < args.steps else ""),
                                         (f"warm-up capped at {warm} oracle steps" if warm < args.warmup else ""))
@@ -335,10 +385,20 @@ def main():
             return {n: {f: np.stack([host_cache[e][n][f] for e in sel]) for f in ("codes", "scales", "g", "a")}
                     for n in ("gate", "up", "down")}
         cpu_sample = (sample_x, weights_for)
+        threads = min(oracle.default_threads(), k)     # one token at a time: k expert FFNs in parallel
+        cores, model = host_cpu()
+        # the threaded oracle (expert FFNs of a token over all the cores), then
+        # the plain one-thread loop on the same tokens
+        done_t, secs_t = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s / 4, Wr, bias, sample_x,
+                                       threads)
         done, secs = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s, Wr, bias, sample_x)
-        cpu_baseline = {"value": done / secs, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                        "sample": f"{done} whole token(s) of this workload (router + top-{k} + {k} expert FFNs "
-                                  f"+ combine), single-threaded float64 C oracle, {secs:.1f} s"}
+        cpu_baseline = {"value": done_t / secs_t, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                        "host_cores": cores, "cpu_model": model,
+                        "sample": f"{done_t} whole token(s) of this workload (router + top-{k} on one thread, "
+                                  f"the {k} expert FFNs on {threads} threads, combine), float64 C oracle, "
+                                  f"{secs_t:.1f} s",
+                        "single_thread": {"value": done / secs, "unit": "tok/s", "cores": 1,
+                                          "sample": f"{done} whole token(s), one thread, {secs:.1f} s"}}
     del canon
     torch.cuda.empty_cache()
 
@@ -384,11 +444,22 @@ def main():
     wrem = args.warmup % ROTATE
     g_wrem = capture(wrem, 0) if wrem else None
 
+    def run_steps():
+        for _ in range(args.steps // ROTATE):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+
+    # warm-up: the requested steps, and every graph the timed region replays
+    # at least once (its first replay uploads it)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup // ROTATE):
             g_full.replay()
         if g_wrem is not None:
             g_wrem.replay()
+        g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
     stream.synchronize()
 
     gpu_id = None
@@ -402,26 +473,33 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host0 = time.perf_counter()
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps // ROTATE):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-    ev1.record(stream)
-    stream.synchronize()
-    t_host = time.perf_counter() - t_host0
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
+    # three timed windows of exactly K steps each, every one bracketed by a
+    # barrier and a synchronize; the line reports the median window (max over
+    # ranks) and the spread of the three
+    windows = []
+    t_host = 0.0
+    for _ in range(3):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_host0 = time.perf_counter()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            run_steps()
+        ev1.record(stream)
+        stream.synchronize()
+        t_host += time.perf_counter() - t_host0
+        torch.cuda.synchronize(dev)
+        wms = ev0.elapsed_time(ev1)
+        if world > 1:
+            dist.barrier()
+            tt = torch.tensor([wms], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            wms = float(tt.item())
+        windows.append(wms)
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = float(np.median(windows))
     ms_per_step = ms / args.steps
     # one MoE layer's throughput: a step runs NL layers on the same C tokens
     tokens = C * args.steps * NL * world
@@ -455,17 +533,18 @@ def main():
     achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
     if C > 8:
         # grouped path: the stage events bracket dispatch, x-row prep and the gate/up GEMM
-        traffic_per_expert = ncu_traffic("grouped.cu", f"group_tc_gu_{args.config}")
+        traffic_per_expert, traffic_src = ncu_traffic("grouped.cu", f"group_tc_gu_{args.config}")
         kernel_label = ("group_tc_kernel<0> (grouped gate/up + SwiGLU on tcgen05; the timed span also holds "
                         "the dispatch and x-row kernels)")
     else:
-        traffic_per_expert = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
+        traffic_per_expert, traffic_src = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
         kernel_label = (f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
                         f"{'two tiles' if C <= 2 else 'one tile'} per stage)")
     roofline = {"kernel": kernel_label, "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": peak_src,
                 "traffic": None if traffic_per_expert is None else traffic_per_expert * gu_units,
+                "traffic_source": traffic_src,
                 "algorithmic_bytes_per_launch": gu_units * gu_bytes_per_expert,
                 "avg_launch_us": gu_avg * 1e3,
                 "down_kernel": {"avg_launch_us": dn_avg * 1e3,
@@ -513,6 +592,8 @@ def main():
                              "of expert weights (> 129 MB L2)" if H == 3584 else "L2-resident (tiny)",
                        "timing": "CUDA graphs of moe_route_forward, CUDA events on the launching stream"},
             "us_per_layer": 1e3 * ms_per_step / NL,
+            "windows_ms_per_step": [w_ / args.steps for w_ in windows],
+            "window_spread": (max(windows) - min(windows)) / ms,
             "expert_hbm_gbs": hbm_gbs, "expert_hbm_frac": hbm_gbs / world / hbm_peak,
             "distinct_experts_per_step": avg_distinct,
             **({"routing": zipf_stats} if zipf_stats else {}),
@@ -523,7 +604,7 @@ def main():
             # gate/up, h rows, down, combine
             "gpu_launches": args.steps * NL * (4 if C <= 8 else 2 + 7 * ((C + 511) // 512)),
             "clocks": clocks,
-            "host_s": t_host,
+            "host_s": t_host,                 # host time of the three windows
             "device_flags": flags,
         }
         if cpu_sample is not None:

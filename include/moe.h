@@ -61,7 +61,13 @@ typedef enum {
 /* Device flag bits reported by moe_get_device_status. */
 #define MOE_FLAG_BAD_EXPERT_ID 0x1   /* an id outside [0, num_experts): slot skipped */
 #define MOE_FLAG_DUPLICATE_ID 0x2    /* an expert repeated within one token: one copy dropped */
-#define MOE_FLAG_TIMEOUT 0x4         /* reserved for bounded waits */
+#define MOE_FLAG_TIMEOUT 0x4         /* a bounded device wait ran out; outputs of that call are invalid */
+
+/* moe_config.flags.  Test hook only, never set in use: every router CTA
+ * (C <= 8) waits for 16 bytes that no copy delivers, with a 20 ms limit
+ * instead of ~2 s, so the timeout path can be exercised without a GPU fault:
+ * MOE_FLAG_TIMEOUT is raised and the call's ids are all -1. */
+#define MOE_CONFIG_TEST_ROUTER_STALL 0x80000000u
 
 typedef struct {
   int32_t num_experts;   /* E, 1 .. 1024 */
@@ -69,7 +75,7 @@ typedef struct {
   int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 4096 */
   int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 4096 */
   int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
-  uint32_t flags;        /* must be 0 */
+  uint32_t flags;        /* 0 (or the test hook MOE_CONFIG_TEST_ROUTER_STALL) */
 } moe_config;
 
 typedef struct {
@@ -125,7 +131,11 @@ moe_status moe_pack_weights(moe_layer_t layer, const moe_canonical_weights *cano
  *                    = exp(l_i - l_max) / sum over kept of exp(l_j - l_max)
  * x: device bf16 bits [C][H]; w_router: device fp32 [E][H]; bias: device fp32
  * [E] or NULL; ids: device int32 [C][k]; weights: device fp32 [C][k];
- * ws: workspace of at least moe_workspace_bytes(C).  1 <= C <= max_tokens. */
+ * ws: workspace of at least moe_workspace_bytes(C).  1 <= C <= max_tokens.
+ * Failure: if a router block's bounded wait for its weight rows runs out
+ * (C <= 8), MOE_FLAG_TIMEOUT is raised and every id of the call is written as
+ * -1 (weight 0), which moe_forward treats as an absent slot; the workspace
+ * stays usable for the next call. */
 moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
                      const float *w_router, const float *bias, int32_t *ids,
                      float *weights, void *ws, size_t ws_bytes, cudaStream_t stream);
@@ -155,7 +165,8 @@ moe_status moe_route_forward(moe_layer_t layer, const uint16_t *x, int num_token
                              cudaStream_t stream);
 
 /* Synchronise `stream`, return the device flag bits accumulated in `ws` since
- * the last call (MOE_FLAG_*), and clear them. */
+ * the last call (MOE_FLAG_*), and clear them together with the router's
+ * completion counters.  No other call may be in flight on `ws`. */
 moe_status moe_get_device_status(moe_layer_t layer, void *ws, cudaStream_t stream,
                                  int32_t *flags);
 
@@ -178,7 +189,11 @@ moe_status moe_set_stage_events(moe_layer_t layer, cudaEvent_t *events, int n_ev
  * C * num_experts <= 8192, otherwise MOE_ERR_WORKSPACE_TOO_SMALL and nothing
  * is queued.  The first call on a device looks up the array's address; make
  * it outside any stream capture.  All calls share the array, so calls that
- * overlap on the GPU race: serialise them on one stream.  Allocates nothing. */
+ * overlap on the GPU race: serialise them on one stream.  Allocates nothing.
+ * This entry point reports no device flags (it has no workspace to hold
+ * them): a call whose bounded router wait ran out writes every id as -1 and
+ * every weight as 0, which the caller can test.  The cached address of the
+ * array is per device and becomes invalid after cudaDeviceReset. */
 moe_status moe_route_noalloc(moe_layer_t layer, const uint16_t *x, int num_tokens,
                              const float *w_router, const float *bias, int32_t *ids,
                              float *weights, cudaStream_t stream);

@@ -3,7 +3,8 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The product
 package never imports it and has no CPU fallback.  The arithmetic lives in
-``moe_oracle.c`` (plain C, float64, single thread); this module only compiles it
+``moe_oracle.c`` (plain C, float64; one thread, or the (token, slot) expert
+evaluations spread over POSIX threads with bit-identical results); this module only compiles it
 with gcc and marshals numpy arrays through ctypes.
 
 Each function names the passage it follows in ``moe_oracle.c``.  Parity pins
@@ -38,7 +39,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC",
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-pthread",
                            "-shared", "-o", tmp, _SRC, "-lm"])
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -69,6 +70,8 @@ def _load():
             lib.oracle_expert_ffn.restype = i32
             lib.oracle_moe_forward.argtypes = [i32] * 5 + [P, P, P] * 3 + [P, P, P, P]
             lib.oracle_moe_forward.restype = i32
+            lib.oracle_moe_forward_mt.argtypes = [i32] * 6 + [P, P, P] * 3 + [P, P, P, P]
+            lib.oracle_moe_forward_mt.restype = i32
             _lib = lib
     return _lib
 
@@ -150,12 +153,23 @@ def expert_ffn(H, I, gate, up, down, x):
     return y
 
 
-def moe_forward(weights, x_bf16, ids, w):
+def default_threads() -> int:
+    """Host cores this process may use (the threaded oracle's default)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def moe_forward(weights, x_bf16, ids, w, threads=1):
     """Routed MoE output.
 
     weights: dict with 'gate', 'up', 'down', each a dict of 'codes' [E][rows][K/2],
     'scales' [E][rows][K/16], 'g' [E] (canonical NVFP4).  x_bf16 uint16 [C][H],
-    ids int32 [C][k], w float64 [C][k] -> y float64 [C][H].
+    ids int32 [C][k], w float64 [C][k] -> y float64 [C][H].  ``threads`` > 1
+    spreads the (token, slot) expert evaluations over that many POSIX threads
+    (oracle_moe_forward_mt) and sums them in slot order as the one-thread
+    code does, so the result is bit-for-bit the same.
     """
     gate, up, down = weights["gate"], weights["up"], weights["down"]
     E, I, Hh = gate["codes"].shape
@@ -171,7 +185,10 @@ def moe_forward(weights, x_bf16, ids, w):
         keep.append((c, s, g))
         args += [_ptr(c), _ptr(s), _ptr(g)]
     y = np.empty((C, H), np.float64)
-    rc = _load().oracle_moe_forward(C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
+    if threads > 1:
+        rc = _load().oracle_moe_forward_mt(int(threads), C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
+    else:
+        rc = _load().oracle_moe_forward(C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
     if rc != OK:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return y

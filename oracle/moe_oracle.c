@@ -44,6 +44,7 @@
  * whether the host compiler fuses multiply-adds.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -281,6 +282,48 @@ int oracle_expert_ffn(int H, int I,
   return ORACLE_OK;
 }
 
+/* Everything one token needs: the arguments of oracle_moe_forward. */
+typedef struct {
+  int C, E, k, H, I;
+  const uint8_t *gate_codes, *gate_scales;
+  const float *gate_g;
+  const uint8_t *up_codes, *up_scales;
+  const float *up_g;
+  const uint8_t *down_codes, *down_scales;
+  const float *down_g;
+  const uint16_t *x;
+  const int32_t *ids;
+  const double *w;
+  double *y;
+} forward_args;
+
+/* y[t] of one token, with the scratch vectors xt[H] and ye[H]. */
+static int forward_token(const forward_args *a, int t, double *xt, double *ye) {
+  const int H = a->H, I = a->I, k = a->k;
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  for (int j = 0; j < H; j++) xt[j] = oracle_bf16_value(a->x[(int64_t)t * H + j]);
+  for (int j = 0; j < H; j++) a->y[(int64_t)t * H + j] = 0.0;
+  for (int i = 0; i < k; i++) {
+    int e = a->ids[(int64_t)t * k + i];
+    if (e < 0 || e >= a->E) return ORACLE_ERR_BAD_ID;
+    int rc = oracle_expert_ffn(H, I,
+                               a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
+                               a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
+                               a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
+                               xt, ye);
+    if (rc != ORACLE_OK) return rc;
+    double wi = a->w[(int64_t)t * k + i];
+    for (int j = 0; j < H; j++) a->y[(int64_t)t * H + j] += wi * ye[j];
+  }
+  return ORACLE_OK;
+}
+
+static int forward_args_ok(const forward_args *a) {
+  return !(a->C < 0 || a->E <= 0 || a->k <= 0 || a->H <= 0 || a->I <= 0 || a->H % 16 || a->I % 16 ||
+           !a->x || !a->ids || !a->w || !a->y);
+}
+
 /* The routed MoE output of C tokens given their selections:
  *   y[t] = sum_i w[t][i] * FFN_{ids[t][i]}(x[t])
  * Canonical weights are arrays over E experts:
@@ -295,11 +338,9 @@ int oracle_moe_forward(int C, int E, int k, int H, int I,
                        const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
                        const uint16_t *x, const int32_t *ids, const double *w,
                        double *y) {
-  if (C < 0 || E <= 0 || k <= 0 || H <= 0 || I <= 0 || H % 16 || I % 16 || !x ||
-      !ids || !w || !y)
-    return ORACLE_ERR_ARG;
-  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
-  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  forward_args a = {C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+                    down_codes, down_scales, down_g, x, ids, w, y};
+  if (!forward_args_ok(&a)) return ORACLE_ERR_ARG;
   double *xt = (double *)malloc(sizeof(double) * (size_t)H);
   double *ye = (double *)malloc(sizeof(double) * (size_t)H);
   if (!xt || !ye) {
@@ -308,26 +349,100 @@ int oracle_moe_forward(int C, int E, int k, int H, int I,
     return ORACLE_ERR_ARG;
   }
   int rc = ORACLE_OK;
-  for (int t = 0; t < C && rc == ORACLE_OK; t++) {
-    for (int j = 0; j < H; j++) xt[j] = oracle_bf16_value(x[(int64_t)t * H + j]);
-    for (int j = 0; j < H; j++) y[(int64_t)t * H + j] = 0.0;
-    for (int i = 0; i < k; i++) {
-      int e = ids[(int64_t)t * k + i];
-      if (e < 0 || e >= E) {
-        rc = ORACLE_ERR_BAD_ID;
-        break;
-      }
-      rc = oracle_expert_ffn(H, I,
-                             gate_codes + e * gu_codes, gate_scales + e * gu_scales, gate_g[e],
-                             up_codes + e * gu_codes, up_scales + e * gu_scales, up_g[e],
-                             down_codes + e * dn_codes, down_scales + e * dn_scales, down_g[e],
-                             xt, ye);
-      if (rc != ORACLE_OK) break;
-      double wi = w[(int64_t)t * k + i];
-      for (int j = 0; j < H; j++) y[(int64_t)t * H + j] += wi * ye[j];
-    }
-  }
+  for (int t = 0; t < C && rc == ORACLE_OK; t++) rc = forward_token(&a, t, xt, ye);
   free(xt);
   free(ye);
+  return rc;
+}
+
+/* The same result computed by `nthreads` POSIX threads.  The (token, slot)
+ * pairs are dealt out to the threads (pair p = thread, thread + nthreads,
+ * ...); each thread runs oracle_expert_ffn for its pairs into a buffer of
+ * their outputs, and the calling thread then forms every y[t] exactly as
+ * oracle_moe_forward does: from 0, adding w[t][i] * (expert output of slot i)
+ * for i = 0, 1, ... .  Same values, same order: the output is bit-for-bit
+ * the single-threaded one; the threads only change which core computes which
+ * expert output. */
+typedef struct {
+  const forward_args *a;
+  double *ye_all;                      /* [C * k][H] expert outputs of every pair */
+  int first, step;
+  int rc;
+} forward_job;
+
+static void *forward_worker(void *p) {
+  forward_job *j = (forward_job *)p;
+  const forward_args *a = j->a;
+  const int H = a->H, I = a->I, k = a->k;
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+  j->rc = xt ? ORACLE_OK : ORACLE_ERR_ARG;
+  for (int64_t pr = j->first; pr < (int64_t)a->C * k && j->rc == ORACLE_OK; pr += j->step) {
+    const int64_t t = pr / k;
+    const int e = a->ids[pr];
+    if (e < 0 || e >= a->E) {
+      j->rc = ORACLE_ERR_BAD_ID;
+      break;
+    }
+    for (int q = 0; q < H; q++) xt[q] = oracle_bf16_value(a->x[t * H + q]);
+    j->rc = oracle_expert_ffn(H, I,
+                              a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
+                              a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
+                              a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
+                              xt, j->ye_all + pr * H);
+  }
+  free(xt);
+  return NULL;
+}
+
+int oracle_moe_forward_mt(int nthreads, int C, int E, int k, int H, int I,
+                          const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                          const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                          const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                          const uint16_t *x, const int32_t *ids, const double *w,
+                          double *y) {
+  forward_args a = {C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+                    down_codes, down_scales, down_g, x, ids, w, y};
+  if (!forward_args_ok(&a) || nthreads < 1) return ORACLE_ERR_ARG;
+  init_tables();                       /* fill the shared tables before any thread reads them */
+  const int64_t npairs = (int64_t)C * k;
+  if (nthreads > npairs) nthreads = npairs > 0 ? (int)npairs : 1;
+  double *ye_all = (double *)malloc(sizeof(double) * (size_t)(npairs > 0 ? npairs : 1) * (size_t)H);
+  pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  forward_job *jobs = (forward_job *)malloc(sizeof(forward_job) * (size_t)nthreads);
+  if (!ye_all || !tids || !jobs) {
+    free(ye_all);
+    free(tids);
+    free(jobs);
+    return ORACLE_ERR_ARG;
+  }
+  int started = 0;
+  for (int i = 0; i < nthreads; i++) {
+    jobs[i].a = &a;
+    jobs[i].ye_all = ye_all;
+    jobs[i].first = i;
+    jobs[i].step = nthreads;
+    jobs[i].rc = ORACLE_OK;
+    if (pthread_create(&tids[i], NULL, forward_worker, &jobs[i]) != 0) break;
+    started++;
+  }
+  for (int i = started; i < nthreads; i++) forward_worker(&jobs[i]);   /* no thread: run it here */
+  int rc = ORACLE_OK;
+  for (int i = 0; i < nthreads; i++) {
+    if (i < started) pthread_join(tids[i], NULL);
+    if (jobs[i].rc != ORACLE_OK && rc == ORACLE_OK) rc = jobs[i].rc;
+  }
+  for (int t = 0; t < C && rc == ORACLE_OK; t++) {
+    for (int q = 0; q < H; q++) y[(int64_t)t * H + q] = 0.0;
+    for (int i = 0; i < k; i++) {
+      const double wi = w[(int64_t)t * k + i];
+      const double *ye = ye_all + ((int64_t)t * k + i) * H;
+      for (int q = 0; q < H; q++) y[(int64_t)t * H + q] += wi * ye[q];
+    }
+  }
+  free(ye_all);
+  free(tids);
+  free(jobs);
   return rc;
 }

@@ -24,8 +24,11 @@ struct RouteArgs {
   float *weights;        // [C][k]
   float *logits;         // workspace [C][E]
   uint32_t *ticket;      // workspace counter (0 between calls)
+  uint32_t *timeouts;    // workspace counter of router CTAs whose wait ran out (0 between calls)
   int32_t *flags;        // workspace flag word (MOE_FLAG_TIMEOUT)
   int C, E, H, k;
+  uint32_t stall_tx;     // test hook: extra bytes every CTA waits for and no copy delivers (0 = off)
+  unsigned long long wait_ns;   // limit of a bounded wait
 };
 // Router GEMV fused with top-k (C <= 8): grid is fixed per layer.
 cudaError_t launch_route_fused(const RouteArgs &a, int grid, cudaStream_t stream);
@@ -33,6 +36,8 @@ cudaError_t launch_route_fused(const RouteArgs &a, int grid, cudaStream_t stream
 cudaError_t launch_route_batched(const RouteArgs &a, cudaStream_t stream);
 // Opt-in shared memory for the fused router (once per device; idempotent).
 cudaError_t route_setup();
+// Wait limit and test stall of the router from the layer's config flags.
+void route_wait_policy(uint32_t config_flags, RouteArgs *a);
 
 struct GemvArgs {
   const uint8_t *packed;

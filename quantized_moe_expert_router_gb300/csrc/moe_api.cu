@@ -60,7 +60,7 @@ const char *moe_status_string(moe_status s) {
 moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out) {
   if (!cfg || !out) return MOE_ERR_INVALID_ARG;
   const moe_config c = *cfg;
-  if (c.flags != 0 || c.max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~(uint32_t)MOE_CONFIG_TEST_ROUTER_STALL) != 0 || c.max_tokens < 1) return MOE_ERR_INVALID_ARG;
   if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.top_k < 1 || c.top_k > moe::kMaxTopK || c.top_k > c.num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.hidden < 64 || c.hidden % 64 || c.hidden > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -170,8 +170,10 @@ moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_rou
   a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
   a.logits = reinterpret_cast<float *>(w + (C <= moe::kGemvTokens ? wl.logits : wl.glogits));
   a.ticket = &reinterpret_cast<moe::WsControl *>(w)->route_ticket;
+  a.timeouts = &reinterpret_cast<moe::WsControl *>(w)->route_timeouts;
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
+  moe::route_wait_policy(L->cfg.flags, &a);
   cudaError_t err;
   if (C <= moe::kRouteFusedTokens) {
     const int grid = a.E < L->num_sms ? a.E : L->num_sms;   // router rows dealt round-robin
@@ -182,9 +184,20 @@ moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_rou
   return cuda_status(err);
 }
 
-moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *ids,
-                       const float *weights, const void *packed, float *y, void *ws,
-                       size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// moe_forward's work.  `after_router`: the fused router kernel was queued
+// right before on `stream` (moe_route_forward), so the gate/up kernel may be
+// launched as its programmatic dependent.  That kernel reads x before it
+// waits for the preceding grid; x is then already visible, because the router
+// (a normal launch) could only start once everything queued before it had
+// finished.  A standalone call has no such guarantee for x written by the
+// caller's last kernel, so there the gate/up kernel is a normal launch.
+moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *ids, const float *weights,
+                        const void *packed, float *y, void *ws, size_t ws_bytes, cudaStream_t stream,
+                        bool after_router) {
   if (!L || !x || !ids || !weights || !packed || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (C < 1 || C > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(packed) || !aligned16(y) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
@@ -255,7 +268,8 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
     a.stage_bytes = a.tile_bytes;
     a.red_stage_f4 = gu_pairs ? 2 * wq * 8 : wq * 32;
     moe::gemv_geometry(a.stage_bytes, a.red_stage_f4 * 16, &a.stages, &a.smem_bytes);
-    err = moe::launch_expert_gemv(gu_pairs ? 2 : 0, a, gemv_grid(*L, max_pairs * a.tiles), true, stream);
+    err = moe::launch_expert_gemv(gu_pairs ? 2 : 0, a, gemv_grid(*L, max_pairs * a.tiles), after_router && t0 == 0,
+                                  stream);
     if (err != cudaSuccess) break;
     if (L->stage_events_on && t0 == 0) err = cudaEventRecord(L->stage_events[1], stream);
     if (err != cudaSuccess) break;
@@ -280,6 +294,15 @@ moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *i
   return cuda_status(err);
 }
 
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(moe_layer_t L, const uint16_t *x, int C, const int32_t *ids, const float *weights,
+                       const void *packed, float *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+  return forward_impl(L, x, C, ids, weights, packed, y, ws, ws_bytes, stream, false);
+}
+
 moe_status moe_route_forward(moe_layer_t L, const uint16_t *x, int C, const float *w_router,
                              const float *bias, const void *packed, int32_t *ids, float *weights, float *y,
                              void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -288,17 +311,21 @@ moe_status moe_route_forward(moe_layer_t L, const uint16_t *x, int C, const floa
   if (!aligned16(packed) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   const moe_status st = moe_route(L, x, C, w_router, bias, ids, weights, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  return moe_forward(L, x, C, ids, weights, packed, y, ws, ws_bytes, stream);
+  return forward_impl(L, x, C, ids, weights, packed, y, ws, ws_bytes, stream,
+                      C <= moe::kRouteFusedTokens && !L->stage_events_on);
 }
 
 moe_status moe_get_device_status(moe_layer_t L, void *ws, cudaStream_t stream, int32_t *flags) {
   if (!L || !ws || !flags) return MOE_ERR_INVALID_ARG;
   DeviceGuard guard(L->device);
   if (!guard.ok) return MOE_ERR_CUDA;
-  int32_t *f = &static_cast<moe::WsControl *>(ws)->flags;
+  moe::WsControl *ctl = static_cast<moe::WsControl *>(ws);
   cudaError_t err = cudaStreamSynchronize(stream);
-  if (err == cudaSuccess) err = cudaMemcpy(flags, f, sizeof(int32_t), cudaMemcpyDeviceToHost);
-  if (err == cudaSuccess) err = cudaMemsetAsync(f, 0, sizeof(int32_t), stream);
+  if (err == cudaSuccess) err = cudaMemcpy(flags, &ctl->flags, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  // flags, router ticket and router failure count back to zero: a router grid
+  // that stopped early leaves the workspace as good as new
+  static_assert(offsetof(moe::WsControl, route_timeouts) == 8, "control words 0..11");
+  if (err == cudaSuccess) err = cudaMemsetAsync(ctl, 0, 12, stream);
   if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
   return cuda_status(err);
 }

@@ -31,6 +31,22 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Bounded wait for phase `parity` of the rows barrier; false when `limit_ns`
+// of %globaltimer pass first.
+__device__ __forceinline__ bool rows_wait(uint64_t *bar, uint32_t parity, unsigned long long limit_ns) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; it++) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    if (done) return true;
+    unsigned long long now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    if (it == 0) t0 = now;
+    else if (now - t0 > limit_ns) return false;
+  }
+}
+
 template <int CT>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const RouteArgs a) {
   extern __shared__ __align__(128) float4 xs4[];   // [CT][H/4] then [rows][H/4]
@@ -54,11 +70,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   }
   __syncthreads();
   bool ok = true;
-  for (int rb = r0, round = 0; rb < r1; rb += max_rows, round++) {
+  int round = 0;
+  for (int rb = r0; rb < r1; rb += max_rows, round++) {
     const int nr = (r1 - rb) < max_rows ? (r1 - rb) : max_rows;
     if (threadIdx.x == 0) {
+      // (a.stall_tx: test hook, bytes that no copy delivers, so the wait below runs out)
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rows_bar)),
-                   "r"((uint32_t)(nr * row_bytes)) : "memory");
+                   "r"((uint32_t)(nr * row_bytes) + (round == 0 ? a.stall_tx : 0u)) : "memory");
       for (int r = 0; r < nr; r++)
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
@@ -81,22 +99,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
       }
       __syncthreads();
     }
-    // bounded wait for the round's rows (about two seconds of %globaltimer)
-    {
-      uint32_t done = 0;
-      unsigned long long t0 = 0;
-      for (uint32_t it = 0;; it++) {
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(smem_addr(&rows_bar)), "r"((uint32_t)(round & 1)) : "memory");
-        if (done) break;
-        unsigned long long now;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
-        if (it == 0) t0 = now;
-        else if (now - t0 > 2000000000ull) break;
-      }
-      ok = __syncthreads_and(done != 0) != 0;    // one decision for the whole CTA
-      if (!ok && threadIdx.x == 0) atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-    }
+    // bounded wait for the round's rows (a.wait_ns of %globaltimer, about two seconds)
+    ok = __syncthreads_and(rows_wait(&rows_bar, (uint32_t)(round & 1), a.wait_ns)) != 0;   // one decision for the CTA
     if (!ok) break;
     // dot products: warp w takes rows w, w + 8, ... of the round
     for (int r = warp; r < nr; r += kRouteWarps) {
@@ -129,8 +133,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
     }
     __syncthreads();                       // the rows buffer is refilled by the next round
   }
-  if (!ok) return;                         // the flag is set; no copy of this CTA is left in flight
-  // the last CTA to finish runs the top-k
+  if (!ok && threadIdx.x == 0) {
+    // The round's rows did not arrive in time: flag it, count this CTA as
+    // failed for the current call, and give the copies one more bounded wait
+    // so that none is left in flight when the CTA exits.
+    atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+    atomicAdd(a.timeouts, 1u);
+    rows_wait(&rows_bar, (uint32_t)(round & 1), a.wait_ns);
+  }
+  // Every CTA takes a ticket, failed or not, so the last one always resets
+  // the counters for the next call.  The last CTA runs the top-k; if any CTA
+  // failed, the logits are incomplete and it writes ids -1 (an absent slot
+  // for moe_forward) and weights 0 instead.
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -140,9 +154,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int t = 0; t < a.C; t++)
-    cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k, a.weights + (size_t)t * a.k, tk);
-  if (threadIdx.x == 0) *a.ticket = 0u;
+  const bool failed = *reinterpret_cast<volatile uint32_t *>(a.timeouts) != 0u;
+  if (failed) {
+    for (int i = threadIdx.x; i < a.C * a.k; i += blockDim.x) {
+      a.ids[i] = -1;
+      a.weights[i] = 0.f;
+    }
+  } else {
+    for (int t = 0; t < a.C; t++)
+      cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k,
+                                        a.weights + (size_t)t * a.k, tk);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *a.ticket = 0u;
+    *a.timeouts = 0u;
+  }
 }
 
 // ------------------------------------------------------------ large C
@@ -237,6 +264,12 @@ cudaError_t route_setup() {
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(route_fused_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem(8, kMaxHidden));
   return err;
+}
+
+void route_wait_policy(uint32_t config_flags, RouteArgs *a) {
+  const bool stall = (config_flags & MOE_CONFIG_TEST_ROUTER_STALL) != 0;
+  a->stall_tx = stall ? 16u : 0u;
+  a->wait_ns = stall ? 20000000ull : 2000000000ull;   // 20 ms under the test hook, else ~2 s
 }
 
 cudaError_t launch_route_fused(const RouteArgs &a, int grid, cudaStream_t stream) {

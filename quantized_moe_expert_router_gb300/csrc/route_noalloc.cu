@@ -21,8 +21,12 @@
 //   - Every call shares the one array: calls whose work overlaps on the GPU
 //     (different streams, or different host threads) race on it.  Serialise
 //     them on one stream.
-//   - Each call clears the completion counter before its kernel, so the
+//   - Each call clears the completion counters before its kernel, so the
 //     contents a previous call left behind do not matter.
+//   - No device flags reach the caller (the flag word lives in the array and
+//     no entry point reads it); a call whose bounded router wait ran out
+//     writes every id as -1 and every weight as 0 instead.
+//   - The cached device address is invalid after cudaDeviceReset.
 #include <mutex>
 
 #include "kernels.h"
@@ -34,7 +38,8 @@ constexpr int kNoAllocTokens = 8;
 constexpr int kNoAllocLogits = 8192;                 // floats: C * E limit
 constexpr size_t kNoAllocBytes = 256 + sizeof(float) * kNoAllocLogits;
 
-// [0, 256): uint32 completion counter (+ padding); [256, ...): logits.
+// [0, 256): uint32 completion counter, flag word, failure counter (+ padding);
+// [256, ...): logits.
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -72,14 +77,16 @@ extern "C" moe_status moe_route_noalloc(moe_layer_t L, const uint16_t *x, int C,
   if (prev != L->device && cudaSetDevice(L->device) != cudaSuccess) return MOE_ERR_CUDA;
   unsigned char *scratch = nullptr;
   cudaError_t err = scratch_address(L->device, &scratch);
-  if (err == cudaSuccess) err = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), stream);
+  if (err == cudaSuccess) err = cudaMemsetAsync(scratch, 0, 3 * sizeof(uint32_t), stream);
   if (err == cudaSuccess) {
     moe::RouteArgs a = {};
     a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
     a.logits = reinterpret_cast<float *>(scratch + 256);
     a.ticket = reinterpret_cast<uint32_t *>(scratch);
     a.flags = reinterpret_cast<int32_t *>(scratch + sizeof(uint32_t));
+    a.timeouts = reinterpret_cast<uint32_t *>(scratch + 2 * sizeof(uint32_t));
     a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
+    moe::route_wait_policy(L->cfg.flags, &a);
     const int grid = a.E < L->num_sms ? a.E : L->num_sms;
     err = moe::launch_route_fused(a, grid, stream);
   }

@@ -26,6 +26,7 @@ STATUS_NAMES = {
 FLAG_BAD_EXPERT_ID = 0x1
 FLAG_DUPLICATE_ID = 0x2
 FLAG_TIMEOUT = 0x4
+CONFIG_TEST_ROUTER_STALL = 0x80000000   # test hook: the router's bounded wait runs out
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",
@@ -110,9 +111,9 @@ def _stream(stream):
 class Layer:
     """Owns one ``moe_layer_t`` handle (host memory only)."""
 
-    def __init__(self, num_experts, top_k, hidden, intermediate, max_tokens, device=0):
+    def __init__(self, num_experts, top_k, hidden, intermediate, max_tokens, device=0, flags=0):
         lib = load_library()
-        self.cfg = moe_config(num_experts, top_k, hidden, intermediate, max_tokens, 0)
+        self.cfg = moe_config(num_experts, top_k, hidden, intermediate, max_tokens, flags)
         self.device = device
         h = ctypes.c_void_p()
         _check("moe_layer_create", lib.moe_layer_create(ctypes.byref(self.cfg), device, ctypes.byref(h)))

@@ -29,6 +29,7 @@ def test_reference_arm_prints_the_contract_line():
     assert "workload" in d["config"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["host_cores"] >= cb["cores"] and cb["cpu_model"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -160,3 +160,20 @@ def test_bad_expert_id_is_an_error():
     x = synth.tokens(0, 0, 1, 64)
     with pytest.raises(ValueError):
         oracle.moe_forward(L, x, np.array([[4]]), np.array([[1.0]]))
+
+
+@pytest.mark.parametrize("C,threads", [(1, 3), (4, 2), (9, 7), (5, 64)])
+def test_threaded_oracle_is_bitwise_the_single_threaded_one(C, threads):
+    # the threaded forward only moves (token, slot) expert evaluations to other
+    # cores and sums them in the same slot order
+    E, k, H, I = 16, 3, 64, 96
+    cw = synth.canonical_layer(2, 0, E, H, I)
+    x = synth.tokens(2, 0, C, H)
+    ids, w, _ = oracle.route(oracle.router_logits(synth.router_weights(2, 0, E, H), x), k)
+    y1 = oracle.moe_forward(cw, x, ids, w)
+    y2 = oracle.moe_forward(cw, x, ids, w, threads=threads)
+    assert (y1 == y2).all()
+    bad = ids.copy()
+    bad[C - 1, 0] = E
+    with pytest.raises(ValueError):
+        oracle.moe_forward(cw, x, bad, w, threads=threads)
