@@ -58,6 +58,12 @@ CONFIGS = {
     "prefill512": dict(E=896, k=16, H=3584, I=3072, C=512, layers=1, zipf=True,
                        workload="K3-shape MoE layer, prefill of 512 tokens, top-16 of 896, NVFP4, "
                                 "Zipf-biased routing (s = 1.1)"),
+    "k3verify4": dict(E=896, k=16, H=3584, I=3072, C=4, layers=1, zipf=False, draft_rho=0.95,
+                      workload="K3-shape MoE layer, multi-row verify pass: 4 draft rows of one stream "
+                               "(pairwise correlation 0.95), top-16 of 896, NVFP4"),
+    "k3verify8": dict(E=896, k=16, H=3584, I=3072, C=8, layers=1, zipf=False, draft_rho=0.95,
+                      workload="K3-shape MoE layer, multi-row verify pass: 8 draft rows of one stream "
+                               "(pairwise correlation 0.95), top-16 of 896, NVFP4"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -361,7 +367,10 @@ def main():
             Wr, bias = Wl, bl
 
     # rotating token sets, distinct per rank
-    x_host = [synth.tokens(args.seed + 1000 * rank, r, C, H) for r in range(ROTATE)]
+    if cfg.get("draft_rho") is not None:
+        x_host = [synth.draft_rows(args.seed + 1000 * rank, r, C, H, cfg["draft_rho"]) for r in range(ROTATE)]
+    else:
+        x_host = [synth.tokens(args.seed + 1000 * rank, r, C, H) for r in range(ROTATE)]
     xs = [torch.from_numpy(xh.view(np.int16)).to(dev) for xh in x_host]
     ids = [[torch.empty((C, k), dtype=torch.int32, device=dev) for _ in range(NL)] for _ in range(ROTATE)]
     wts = [[torch.empty((C, k), dtype=torch.float32, device=dev) for _ in range(NL)] for _ in range(ROTATE)]

@@ -30,6 +30,8 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_ARG, ERR_NAN_SCALE, ERR_BAD_ID = 0, 1, 2, 3
+FMT_NVFP4, FMT_MXFP4 = 0, 1
+_FMT = {"nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4}
 
 
 def build(force: bool = False) -> str:
@@ -56,6 +58,16 @@ def _load():
             lib.oracle_e2m1_value.restype = ctypes.c_double
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_value.restype = ctypes.c_double
+            lib.oracle_dequant_fmt.argtypes = [i32, P, P, ctypes.c_float, i64, i64, P]
+            lib.oracle_dequant_fmt.restype = i32
+            lib.oracle_expert_ffn_fmt.argtypes = [i32, i32, i32] + [P, P, ctypes.c_float] * 3 + [P, P]
+            lib.oracle_expert_ffn_fmt.restype = i32
+            lib.oracle_moe_forward_fmt.argtypes = [i32] * 6 + [P, P, P] * 3 + [P, P, P, P]
+            lib.oracle_moe_forward_fmt.restype = i32
+            lib.oracle_moe_forward_mt_fmt.argtypes = [i32] * 7 + [P, P, P] * 3 + [P, P, P, P]
+            lib.oracle_moe_forward_mt_fmt.restype = i32
             lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_value.restype = ctypes.c_double
             lib.oracle_expert_bytes.argtypes = [i64, i64]
@@ -92,6 +104,10 @@ def e4m3_value(byte: int) -> float:
     return _load().oracle_e4m3_value(byte)
 
 
+def e8m0_value(byte: int) -> float:
+    return _load().oracle_e8m0_value(byte)
+
+
 def bf16_value(bits: int) -> float:
     return _load().oracle_bf16_value(bits)
 
@@ -100,11 +116,11 @@ def expert_bytes(hidden: int, inter: int) -> int:
     return int(_load().oracle_expert_bytes(hidden, inter))
 
 
-def dequant(codes, scales, g, rows, K):
+def dequant(codes, scales, g, rows, K, fmt="nvfp4"):
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.uint8)
     out = np.empty((rows, K), np.float64)
-    rc = _load().oracle_dequant(_ptr(codes), _ptr(scales), float(g), rows, K, _ptr(out))
+    rc = _load().oracle_dequant_fmt(_FMT[fmt], _ptr(codes), _ptr(scales), float(g), rows, K, _ptr(out))
     if rc != OK:
         raise ValueError(f"oracle_dequant failed ({rc})")
     return out
@@ -137,7 +153,7 @@ def route(logits, k):
     return ids, w, gap
 
 
-def expert_ffn(H, I, gate, up, down, x):
+def expert_ffn(H, I, gate, up, down, x, fmt="nvfp4"):
     """gate/up/down = (codes, scales, g) of one expert; x float64 [H] -> y float64 [H]."""
     x = _c(x, np.float64)
     y = np.empty((H,), np.float64)
@@ -147,7 +163,7 @@ def expert_ffn(H, I, gate, up, down, x):
         c, s = _c(m[0], np.uint8), _c(m[1], np.uint8)
         mats.append((c, s))
         args += [_ptr(c), _ptr(s), float(m[2])]
-    rc = _load().oracle_expert_ffn(H, I, *args, _ptr(x), _ptr(y))
+    rc = _load().oracle_expert_ffn_fmt(_FMT[fmt], H, I, *args, _ptr(x), _ptr(y))
     if rc != OK:
         raise ValueError(f"oracle_expert_ffn failed ({rc})")
     return y
@@ -161,7 +177,7 @@ def default_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
-def moe_forward(weights, x_bf16, ids, w, threads=1):
+def moe_forward(weights, x_bf16, ids, w, threads=1, fmt=None):
     """Routed MoE output.
 
     weights: dict with 'gate', 'up', 'down', each a dict of 'codes' [E][rows][K/2],
@@ -169,8 +185,10 @@ def moe_forward(weights, x_bf16, ids, w, threads=1):
     ids int32 [C][k], w float64 [C][k] -> y float64 [C][H].  ``threads`` > 1
     spreads the (token, slot) expert evaluations over that many POSIX threads
     (oracle_moe_forward_mt) and sums them in slot order as the one-thread
-    code does, so the result is bit-for-bit the same.
+    code does, so the result is bit-for-bit the same.  ``fmt`` names the
+    weight format, "nvfp4" (default) or "mxfp4".
     """
+    fmt = _FMT[fmt or "nvfp4"]
     gate, up, down = weights["gate"], weights["up"], weights["down"]
     E, I, Hh = gate["codes"].shape
     H = Hh * 2
@@ -186,17 +204,18 @@ def moe_forward(weights, x_bf16, ids, w, threads=1):
         args += [_ptr(c), _ptr(s), _ptr(g)]
     y = np.empty((C, H), np.float64)
     if threads > 1:
-        rc = _load().oracle_moe_forward_mt(int(threads), C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
+        rc = _load().oracle_moe_forward_mt_fmt(fmt, int(threads), C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w),
+                                               _ptr(y))
     else:
-        rc = _load().oracle_moe_forward(C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
+        rc = _load().oracle_moe_forward_fmt(fmt, C, E, k, H, I, *args, _ptr(x), _ptr(ids), _ptr(w), _ptr(y))
     if rc != OK:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return y
 
 
-def full_layer(weights, Wr, x_bf16, k, bias=None):
+def full_layer(weights, Wr, x_bf16, k, bias=None, fmt="nvfp4"):
     """Router + top-k + routed FFN for C tokens: returns (ids, w, gap, y)."""
     logits = router_logits(Wr, x_bf16, bias)
     ids, w, gap = route(logits, k)
-    y = moe_forward(weights, x_bf16, ids, w)
+    y = moe_forward(weights, x_bf16, ids, w, fmt=fmt)
     return ids, w, gap, y

@@ -88,6 +88,13 @@ double oracle_e4m3_value(uint8_t byte) {
   return sign ? -mag : mag;
 }
 
+/* e8m0 (the MX scale type, OCP Microscaling Formats spec): an unsigned
+ * biased exponent, value = 2^(byte - 127); byte 0xFF is NaN. */
+double oracle_e8m0_value(uint8_t byte) {
+  if (byte == 0xFF) return NAN;
+  return ldexp(1.0, (int)byte - 127);
+}
+
 /* bfloat16: the upper 16 bits of an IEEE binary32. */
 double oracle_bf16_value(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -120,31 +127,62 @@ static void init_tables(void) {
   tables_ready = 1;
 }
 
-/* Weight (r, k) of one NVFP4 matrix [rows][K]:
- *   code  = nibble k%2 (low nibble for even k) of codes[r*K/2 + k/2]
- *   scale = scales[r*K/16 + k/16]
- *   w     = e2m1(code) * e4m3(scale) * g                                      */
-static double nvfp4_weight(const uint8_t *codes, const uint8_t *scales, float g,
-                           int64_t K, int64_t r, int64_t k) {
-  uint8_t byte = codes[r * (K / 2) + k / 2];
-  uint8_t nibble = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
-  uint8_t sbyte = scales[r * (K / 16) + k / 16];
-  return e2m1_table[nibble] * e4m3_table[sbyte] * (double)g;
+/* The two 4-bit weight formats.  Both store one e2m1 code per element, two
+ * per byte, the low nibble holding the even element, and multiply the whole
+ * matrix by the fp32 tensor scale g:
+ *   NVFP4: one e4m3 scale per 16 consecutive elements along K
+ *          (scales [rows][K/16]);
+ *   MXFP4: one e8m0 scale per 32 consecutive elements along K
+ *          (scales [rows][K/32]; OCP MX, the format of the ggml microbench in
+ *          "Kimi-K3 on 2x A40 - measured findings", section "Why the
+ *          placement experiments all looked the same"). */
+#define ORACLE_FMT_NVFP4 0
+#define ORACLE_FMT_MXFP4 1
+
+static int fmt_block(int fmt) { return fmt == ORACLE_FMT_MXFP4 ? 32 : 16; }
+
+static double fmt_scale(int fmt, uint8_t b) {
+  return fmt == ORACLE_FMT_MXFP4 ? oracle_e8m0_value(b) : e4m3_table[b];
 }
 
-/* Dense float64 copy of one NVFP4 matrix: out[rows][K].  Returns
+/* Weight (r, k) of one matrix [rows][K]:
+ *   code  = nibble k%2 (low nibble for even k) of codes[r*K/2 + k/2]
+ *   scale = scales[r*K/B + k/B]   (B = 16 for NVFP4, 32 for MXFP4)
+ *   w     = e2m1(code) * scale * g                                           */
+static double fp4_weight(int fmt, const uint8_t *codes, const uint8_t *scales, float g,
+                         int64_t K, int64_t r, int64_t k) {
+  const int B = fmt_block(fmt);
+  uint8_t byte = codes[r * (K / 2) + k / 2];
+  uint8_t nibble = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+  uint8_t sbyte = scales[r * (K / B) + k / B];
+  return e2m1_table[nibble] * fmt_scale(fmt, sbyte) * (double)g;
+}
+
+/* 1 if any of the n scale bytes is a NaN of the format. */
+static int fmt_has_nan(int fmt, const uint8_t *scales, int64_t n) {
+  for (int64_t i = 0; i < n; i++)
+    if (isnan(fmt_scale(fmt, scales[i]))) return 1;
+  return 0;
+}
+
+/* Dense float64 copy of one matrix: out[rows][K].  Returns
  * ORACLE_ERR_NAN_SCALE if any scale byte is NaN. */
-int oracle_dequant(const uint8_t *codes, const uint8_t *scales, float g,
-                   int64_t rows, int64_t K, double *out) {
-  if (!codes || !scales || !out || rows < 0 || K <= 0 || K % 16 != 0)
+int oracle_dequant_fmt(int fmt, const uint8_t *codes, const uint8_t *scales, float g,
+                       int64_t rows, int64_t K, double *out) {
+  if ((fmt != ORACLE_FMT_NVFP4 && fmt != ORACLE_FMT_MXFP4) || !codes || !scales || !out || rows < 0 || K <= 0 ||
+      K % fmt_block(fmt) != 0)
     return ORACLE_ERR_ARG;
   init_tables();
-  for (int64_t i = 0; i < rows * (K / 16); i++)
-    if (isnan(oracle_e4m3_value(scales[i]))) return ORACLE_ERR_NAN_SCALE;
+  if (fmt_has_nan(fmt, scales, rows * (K / fmt_block(fmt)))) return ORACLE_ERR_NAN_SCALE;
   for (int64_t r = 0; r < rows; r++)
     for (int64_t k = 0; k < K; k++)
-      out[r * K + k] = nvfp4_weight(codes, scales, g, K, r, k);
+      out[r * K + k] = fp4_weight(fmt, codes, scales, g, K, r, k);
   return ORACLE_OK;
+}
+
+int oracle_dequant(const uint8_t *codes, const uint8_t *scales, float g,
+                   int64_t rows, int64_t K, double *out) {
+  return oracle_dequant_fmt(ORACLE_FMT_NVFP4, codes, scales, g, rows, K, out);
 }
 
 /* ---------------------------------------------------------------- router */
@@ -245,45 +283,56 @@ int oracle_route(int C, int E, int k, const double *logits, int32_t *ids,
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 
 /* One expert's SwiGLU FFN on a float64 input vector x[H]:
- *   g = G x, u = U x         (G, U: NVFP4 [I][H])
+ *   g = G x, u = U x         (G, U: [I][H])
  *   a = silu(g) * u
- *   y = D a                  (D: NVFP4 [H][I])
- * Shapes from "SparkInfer-K3", "The model": the expert reads and writes the
- * 3584-wide latent space and is 3072 wide inside. */
-int oracle_expert_ffn(int H, int I,
-                      const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
-                      const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
-                      const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
-                      const double *x, double *y) {
-  if (H <= 0 || I <= 0 || H % 16 || I % 16 || !x || !y) return ORACLE_ERR_ARG;
+ *   y = D a                  (D: [H][I])
+ * with the matrices in format `fmt`.  Shapes from "SparkInfer-K3", "The
+ * model": the expert reads and writes the 3584-wide latent space and is 3072
+ * wide inside. */
+int oracle_expert_ffn_fmt(int fmt, int H, int I,
+                          const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
+                          const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
+                          const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
+                          const double *x, double *y) {
+  if (fmt != ORACLE_FMT_NVFP4 && fmt != ORACLE_FMT_MXFP4) return ORACLE_ERR_ARG;
+  const int B = fmt_block(fmt);
+  if (H <= 0 || I <= 0 || H % B || I % B || !x || !y) return ORACLE_ERR_ARG;
   init_tables();
-  for (int64_t i = 0; i < (int64_t)I * (H / 16); i++)
-    if (isnan(oracle_e4m3_value(gate_scales[i])) || isnan(oracle_e4m3_value(up_scales[i])))
-      return ORACLE_ERR_NAN_SCALE;
-  for (int64_t i = 0; i < (int64_t)H * (I / 16); i++)
-    if (isnan(oracle_e4m3_value(down_scales[i]))) return ORACLE_ERR_NAN_SCALE;
+  if (fmt_has_nan(fmt, gate_scales, (int64_t)I * (H / B)) || fmt_has_nan(fmt, up_scales, (int64_t)I * (H / B)) ||
+      fmt_has_nan(fmt, down_scales, (int64_t)H * (I / B)))
+    return ORACLE_ERR_NAN_SCALE;
   double *a = (double *)malloc(sizeof(double) * (size_t)I);
   if (!a) return ORACLE_ERR_ARG;
   for (int r = 0; r < I; r++) {
     double g = 0.0, u = 0.0;
     for (int k = 0; k < H; k++) {
-      g += nvfp4_weight(gate_codes, gate_scales, gate_g, H, r, k) * x[k];
-      u += nvfp4_weight(up_codes, up_scales, up_g, H, r, k) * x[k];
+      g += fp4_weight(fmt, gate_codes, gate_scales, gate_g, H, r, k) * x[k];
+      u += fp4_weight(fmt, up_codes, up_scales, up_g, H, r, k) * x[k];
     }
     a[r] = silu(g) * u;
   }
   for (int r = 0; r < H; r++) {
     double s = 0.0;
     for (int k = 0; k < I; k++)
-      s += nvfp4_weight(down_codes, down_scales, down_g, I, r, k) * a[k];
+      s += fp4_weight(fmt, down_codes, down_scales, down_g, I, r, k) * a[k];
     y[r] = s;
   }
   free(a);
   return ORACLE_OK;
 }
 
+int oracle_expert_ffn(int H, int I,
+                      const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
+                      const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
+                      const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
+                      const double *x, double *y) {
+  return oracle_expert_ffn_fmt(ORACLE_FMT_NVFP4, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+                               down_codes, down_scales, down_g, x, y);
+}
+
 /* Everything one token needs: the arguments of oracle_moe_forward. */
 typedef struct {
+  int fmt;
   int C, E, k, H, I;
   const uint8_t *gate_codes, *gate_scales;
   const float *gate_g;
@@ -299,15 +348,15 @@ typedef struct {
 
 /* y[t] of one token, with the scratch vectors xt[H] and ye[H]. */
 static int forward_token(const forward_args *a, int t, double *xt, double *ye) {
-  const int H = a->H, I = a->I, k = a->k;
-  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
-  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  const int H = a->H, I = a->I, k = a->k, B = fmt_block(a->fmt);
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / B;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / B;
   for (int j = 0; j < H; j++) xt[j] = oracle_bf16_value(a->x[(int64_t)t * H + j]);
   for (int j = 0; j < H; j++) a->y[(int64_t)t * H + j] = 0.0;
   for (int i = 0; i < k; i++) {
     int e = a->ids[(int64_t)t * k + i];
     if (e < 0 || e >= a->E) return ORACLE_ERR_BAD_ID;
-    int rc = oracle_expert_ffn(H, I,
+    int rc = oracle_expert_ffn_fmt(a->fmt, H, I,
                                a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
                                a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
                                a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
@@ -320,7 +369,9 @@ static int forward_token(const forward_args *a, int t, double *xt, double *ye) {
 }
 
 static int forward_args_ok(const forward_args *a) {
-  return !(a->C < 0 || a->E <= 0 || a->k <= 0 || a->H <= 0 || a->I <= 0 || a->H % 16 || a->I % 16 ||
+  if (a->fmt != ORACLE_FMT_NVFP4 && a->fmt != ORACLE_FMT_MXFP4) return 0;
+  const int B = fmt_block(a->fmt);
+  return !(a->C < 0 || a->E <= 0 || a->k <= 0 || a->H <= 0 || a->I <= 0 || a->H % B || a->I % B ||
            !a->x || !a->ids || !a->w || !a->y);
 }
 
@@ -332,13 +383,13 @@ static int forward_args_ok(const forward_args *a) {
  * order the ids are given.  An id outside [0, E) is an error.  The partial
  * sums over disjoint subsets of the selected experts add up to this result
  * ("SparkInfer-K3", "How the TP module works"). */
-int oracle_moe_forward(int C, int E, int k, int H, int I,
-                       const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
-                       const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
-                       const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
-                       const uint16_t *x, const int32_t *ids, const double *w,
-                       double *y) {
-  forward_args a = {C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+int oracle_moe_forward_fmt(int fmt, int C, int E, int k, int H, int I,
+                           const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                           const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                           const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                           const uint16_t *x, const int32_t *ids, const double *w,
+                           double *y) {
+  forward_args a = {fmt, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
                     down_codes, down_scales, down_g, x, ids, w, y};
   if (!forward_args_ok(&a)) return ORACLE_ERR_ARG;
   double *xt = (double *)malloc(sizeof(double) * (size_t)H);
@@ -353,6 +404,16 @@ int oracle_moe_forward(int C, int E, int k, int H, int I,
   free(xt);
   free(ye);
   return rc;
+}
+
+int oracle_moe_forward(int C, int E, int k, int H, int I,
+                       const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                       const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                       const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                       const uint16_t *x, const int32_t *ids, const double *w,
+                       double *y) {
+  return oracle_moe_forward_fmt(ORACLE_FMT_NVFP4, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes,
+                                up_scales, up_g, down_codes, down_scales, down_g, x, ids, w, y);
 }
 
 /* The same result computed by `nthreads` POSIX threads.  The (token, slot)
@@ -373,9 +434,9 @@ typedef struct {
 static void *forward_worker(void *p) {
   forward_job *j = (forward_job *)p;
   const forward_args *a = j->a;
-  const int H = a->H, I = a->I, k = a->k;
-  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / 16;
-  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / 16;
+  const int H = a->H, I = a->I, k = a->k, B = fmt_block(a->fmt);
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / B;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / B;
   double *xt = (double *)malloc(sizeof(double) * (size_t)H);
   j->rc = xt ? ORACLE_OK : ORACLE_ERR_ARG;
   for (int64_t pr = j->first; pr < (int64_t)a->C * k && j->rc == ORACLE_OK; pr += j->step) {
@@ -386,7 +447,7 @@ static void *forward_worker(void *p) {
       break;
     }
     for (int q = 0; q < H; q++) xt[q] = oracle_bf16_value(a->x[t * H + q]);
-    j->rc = oracle_expert_ffn(H, I,
+    j->rc = oracle_expert_ffn_fmt(a->fmt, H, I,
                               a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
                               a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
                               a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
@@ -396,13 +457,13 @@ static void *forward_worker(void *p) {
   return NULL;
 }
 
-int oracle_moe_forward_mt(int nthreads, int C, int E, int k, int H, int I,
-                          const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
-                          const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
-                          const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
-                          const uint16_t *x, const int32_t *ids, const double *w,
-                          double *y) {
-  forward_args a = {C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+int oracle_moe_forward_mt_fmt(int fmt, int nthreads, int C, int E, int k, int H, int I,
+                              const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                              const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                              const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                              const uint16_t *x, const int32_t *ids, const double *w,
+                              double *y) {
+  forward_args a = {fmt, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
                     down_codes, down_scales, down_g, x, ids, w, y};
   if (!forward_args_ok(&a) || nthreads < 1) return ORACLE_ERR_ARG;
   init_tables();                       /* fill the shared tables before any thread reads them */
@@ -445,4 +506,14 @@ int oracle_moe_forward_mt(int nthreads, int C, int E, int k, int H, int I,
   free(tids);
   free(jobs);
   return rc;
+}
+
+int oracle_moe_forward_mt(int nthreads, int C, int E, int k, int H, int I,
+                          const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                          const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                          const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                          const uint16_t *x, const int32_t *ids, const double *w,
+                          double *y) {
+  return oracle_moe_forward_mt_fmt(ORACLE_FMT_NVFP4, nthreads, C, E, k, H, I, gate_codes, gate_scales, gate_g,
+                                   up_codes, up_scales, up_g, down_codes, down_scales, down_g, x, ids, w, y);
 }

@@ -53,6 +53,7 @@ KIND_ROUTER = 2
 KIND_X = 3
 KIND_BIAS_PERM = 4
 KIND_GSCALE = 5
+KIND_DRAFT = 6
 
 MAT_GATE, MAT_UP, MAT_DOWN = 0, 1, 2
 
@@ -171,6 +172,26 @@ def quantize_nvfp4(w: np.ndarray, g: float):
     return packed, scode
 
 
+def quantize_mxfp4(w: np.ndarray):
+    """Encode float64 weights [rows][K] into canonical MXFP4 (OCP MX): per
+    32-element block along K a shared e8m0 scale 2^e with e = floor(log2 amax)
+    - 2 (the spec's rule: the exponent of amax minus e2m1's largest exponent,
+    clamped to [-127, 127]; an all-zero block gets e = -127), and codes = the
+    e2m1 value nearest to w / 2^e (ties to even, saturating at 6).  Returns
+    codes uint8 [rows][K/2] (low nibble = even k) and scales uint8 [rows][K/32]
+    (byte = e + 127)."""
+    rows, K = w.shape
+    blk = w.reshape(rows, K // 32, 32)
+    amax = np.abs(blk).max(axis=2)
+    _, ex = np.frexp(amax)                        # amax = m 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = np.where(amax > 0.0, ex.astype(np.int64) - 1 - 2, -127)
+    e = np.clip(e, -127, 127)
+    sc = np.ldexp(1.0, e)[:, :, None]
+    codes = e2m1_encode(blk, sc).reshape(rows, K)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
 # ------------------------------------------------------------ layer inputs
 
 def global_scales(seed: int, layer: int, E: int):
@@ -189,27 +210,34 @@ def weight_key(seed: int, layer: int, expert: int, mat: int) -> int:
     return key(seed, KIND_WEIGHT, layer, expert, mat)
 
 
-def expert_matrix(seed: int, layer: int, expert: int, mat: int, rows: int, K: int, g: float):
-    """Canonical NVFP4 (codes, scales) of one matrix of one expert."""
+def expert_matrix(seed: int, layer: int, expert: int, mat: int, rows: int, K: int, g: float, fmt="nvfp4"):
+    """Canonical (codes, scales) of one matrix of one expert: NVFP4 with
+    global scale g, or MXFP4 (no global scale; the weights are the same draws)."""
     k = weight_key(seed, layer, expert, mat)
     w = (_ih8_sum(k, rows * K).astype(np.float64) - IH8_CENTER) * W_COEF
+    if fmt == "mxfp4":
+        return quantize_mxfp4(w.reshape(rows, K))
     return quantize_nvfp4(w.reshape(rows, K), g)
 
 
-def canonical_layer(seed: int, layer: int, E: int, H: int, I: int, experts=None):
-    """Host-generated canonical NVFP4 layer.
+def canonical_layer(seed: int, layer: int, E: int, H: int, I: int, experts=None, fmt="nvfp4"):
+    """Host-generated canonical layer, NVFP4 or MXFP4.
 
     Returns dict gate/up/down -> {'codes', 'scales', 'g', 'a'} with codes
-    [n][rows][K/2], scales [n][rows][K/16], g/a [n] for the experts listed (all
-    E by default), in that order."""
+    [n][rows][K/2], scales [n][rows][K/16] (NVFP4) or [n][rows][K/32] (MXFP4),
+    g/a [n] for the experts listed (all E by default), in that order.  MXFP4
+    matrices carry the tensor scale g = 1."""
     experts = list(range(E)) if experts is None else list(experts)
     g, a = global_scales(seed, layer, E)
+    if fmt == "mxfp4":
+        g = np.ones_like(g)
+    blk = 32 if fmt == "mxfp4" else 16
     out = {}
     for mat, name, rows, K in ((MAT_GATE, "gate", I, H), (MAT_UP, "up", I, H), (MAT_DOWN, "down", H, I)):
         codes = np.empty((len(experts), rows, K // 2), np.uint8)
-        scales = np.empty((len(experts), rows, K // 16), np.uint8)
+        scales = np.empty((len(experts), rows, K // blk), np.uint8)
         for j, e in enumerate(experts):
-            codes[j], scales[j] = expert_matrix(seed, layer, e, mat, rows, K, float(g[mat][e]))
+            codes[j], scales[j] = expert_matrix(seed, layer, e, mat, rows, K, float(g[mat][e]), fmt)
         out[name] = {"codes": codes, "scales": scales,
                      "g": g[mat][experts].copy(), "a": a[mat][experts].copy()}
     return out
@@ -235,6 +263,21 @@ def tokens(seed: int, layer: int, C: int, H: int, attempts=None) -> np.ndarray:
     x = np.empty((C, H), np.uint16)
     for t in range(C):
         x[t] = f64_to_bf16_bits(normals(key(seed, KIND_X, layer, t, attempts[t]), H))
+    return x
+
+
+def draft_rows(seed: int, layer: int, r: int, H: int, rho: float = 0.95, attempts=None) -> np.ndarray:
+    """x bf16 bits [r][H] of r draft rows of one stream: row j is
+    sqrt(rho) b + sqrt(1 - rho) z_j with b and z_j N(0,1) vectors (b shared by
+    the rows, stream (seed, DRAFT, layer, 0); z_j from stream (seed, DRAFT,
+    layer, 1 + j, attempts[j])), so the rows are N(0,1) with pairwise
+    correlation rho and their top-k expert sets overlap."""
+    attempts = [0] * r if attempts is None else attempts
+    b = normals(key(seed, KIND_DRAFT, layer, 0), H)
+    x = np.empty((r, H), np.uint16)
+    for j in range(r):
+        z = normals(key(seed, KIND_DRAFT, layer, 1 + j, attempts[j]), H)
+        x[j] = f64_to_bf16_bits(math.sqrt(rho) * b + math.sqrt(1.0 - rho) * z)
     return x
 
 

@@ -28,11 +28,18 @@ def assert_close(y, y_ref, label=""):
     return err / max(scale, 1e-300), l2
 
 
-def gapped_tokens(seed, layer, C, H, Wr, k, bias=None, min_gap=MIN_GAP, max_attempts=200):
+def gapped_tokens(seed, layer, C, H, Wr, k, bias=None, min_gap=MIN_GAP, max_attempts=200, draft_rho=None):
     """x (bf16 bits [C][H]) whose oracle top-k boundary gap is >= min_gap for
-    every token: a token that misses it is redrawn from its next attempt."""
+    every token: a token that misses it is redrawn from its next attempt.
+    With ``draft_rho`` the rows are draft rows of one stream
+    (``synth.draft_rows``, pairwise correlation draft_rho)."""
     attempts = [0] * C
-    x = synth.tokens(seed, layer, C, H, attempts)
+
+    def draw():
+        if draft_rho is None:
+            return synth.tokens(seed, layer, C, H, attempts)
+        return synth.draft_rows(seed, layer, C, H, draft_rho, attempts)
+    x = draw()
     for _ in range(max_attempts):
         _, _, gap = oracle.route(oracle.router_logits(Wr, x, bias), k)
         bad = [t for t in range(C) if gap[t] < min_gap]
@@ -40,7 +47,7 @@ def gapped_tokens(seed, layer, C, H, Wr, k, bias=None, min_gap=MIN_GAP, max_atte
             return x
         for t in bad:
             attempts[t] += 1
-        x = synth.tokens(seed, layer, C, H, attempts)
+        x = draw()
     raise RuntimeError("could not draw tokens with the required logit gap")
 
 

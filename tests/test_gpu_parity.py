@@ -550,6 +550,29 @@ def test_k3_zipf_routing_parity(k3_layer, C):
     check_layer(v, x, f"k3 zipf C={C} one call", fused=True)
 
 
+@pytest.mark.parametrize("r", [2, 4, 8])
+def test_k3_verify_pass_parity(k3_layer, r):
+    # the multi-row verify pass: r draft rows of one stream (pairwise
+    # correlation 0.95) in one call; the rows share most of their experts, so
+    # many experts carry several rows (the down kernel's second pass of four
+    # token slots runs for experts that more than four rows chose)
+    L = k3_layer
+    x = gapped_tokens(4, 0, r, 3584, L.Wr, 16, draft_rho=0.95)
+    ids, _, _ = L.run(x)
+    assert len(set(ids.ravel().tolist())) < 16 * r
+    counts = np.bincount(ids.ravel(), minlength=896)
+    if r == 8:
+        assert counts.max() > 4                  # an expert chosen by more than four rows
+    check_layer(L, x, f"k3 verify pass r={r}")
+    check_layer(L, x, f"k3 verify pass r={r} one call", fused=True)
+
+
+def test_tiny_verify_pass_parity():
+    L = GpuLayer(32, 4, 256, 192, 8, seed=8)
+    x = gapped_tokens(8, 0, 8, 256, L.Wr, 4, draft_rho=0.95)
+    check_layer(L, x, "tiny verify pass r=8")
+
+
 def test_tiny_zipf_routing_parity():
     L = GpuLayer(32, 4, 256, 192, 8, seed=4, router_std=synth.ZIPF_ROUTER_STD, zipf=True)
     x = gapped_tokens(4, 0, 8, 256, L.Wr, 4, bias=L.bias)

@@ -91,3 +91,30 @@ def test_zipf_bias_hot_set():
     top = np.sort(p)[::-1]
     assert abs(top[:104].sum() - 0.78) < 0.03
     assert not (np.argsort(b) == np.argsort(synth.zipf_bias(0, 1, E))).all()
+
+
+def test_draft_rows_correlation_and_limits():
+    # draft rows of one stream: N(0,1) rows with pairwise correlation rho;
+    # rho = 1 gives identical rows, and a row's attempt number redraws that
+    # row alone
+    H = 4096
+    x = synth.bf16_bits_to_f32(synth.draft_rows(3, 0, 4, H, 0.95)).astype(np.float64)
+    assert np.abs(x.std(axis=1) - 1.0).max() < 0.05
+    c = np.corrcoef(x)
+    assert np.abs(c[np.triu_indices(4, 1)] - 0.95).max() < 0.02
+    same = synth.draft_rows(3, 0, 3, H, 1.0)
+    assert (same[0] == same[1]).all() and (same[1] == same[2]).all()
+    a = synth.draft_rows(3, 0, 3, H, 0.9)
+    b = synth.draft_rows(3, 0, 3, H, 0.9, attempts=[0, 1, 0])
+    assert (a[0] == b[0]).all() and (a[2] == b[2]).all() and not (a[1] == b[1]).all()
+
+
+def test_draft_rows_share_most_experts():
+    # the verify pass's routing: with rho = 0.95 the 8 rows of a pass touch
+    # far fewer distinct experts than 8 independent tokens would (16 each)
+    E, H, k = 896, 3584, 16
+    Wr = synth.router_weights(0, 0, E, H)
+    for seed in range(3):
+        ids, _, _ = oracle.route(oracle.router_logits(Wr, synth.draft_rows(seed, 0, 8, H, 0.95)), k)
+        ind, _, _ = oracle.route(oracle.router_logits(Wr, synth.tokens(seed, 0, 8, H)), k)
+        assert len(set(ids.ravel().tolist())) < 48 < len(set(ind.ravel().tolist()))
