@@ -64,6 +64,12 @@ CONFIGS = {
     "k3verify8": dict(E=896, k=16, H=3584, I=3072, C=8, layers=1, zipf=False, draft_rho=0.95,
                       workload="K3-shape MoE layer, multi-row verify pass: 8 draft rows of one stream "
                                "(pairwise correlation 0.95), top-16 of 896, NVFP4"),
+    "k3b1mx": dict(E=896, k=16, H=3584, I=3072, C=1, layers=1, zipf=False, fmt="mxfp4",
+                   workload="K3-shape MoE layer, decode batch 1, top-16 of 896, MXFP4 (e8m0 scale per 32), "
+                            "uniform routing"),
+    "k3c7mx": dict(E=896, k=16, H=3584, I=3072, C=7, layers=1, zipf=False, fmt="mxfp4",
+                   workload="K3-shape MoE layer, decode batch 7, top-16 of 896, MXFP4 (e8m0 scale per 32), "
+                            "uniform routing"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -240,7 +246,8 @@ def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits, 
         weights = weights_for(sel)                       # input staging, not timed
         t_prep = time.perf_counter() - t_prep0
         remap = {e: i for i, e in enumerate(sel)}
-        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads)
+        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads,
+                           fmt=cfg.get("fmt", "nvfp4"))
         t_total += time.perf_counter() - t0 - t_prep
         done += 1
         if t_total >= budget_s:
@@ -263,7 +270,7 @@ def run_reference(args, cfg, rank):
     def weights_for(sel):
         need = [e for e in sel if e not in cache]
         if need:
-            part = synth.canonical_layer(args.seed, 0, E, H, I, experts=need)
+            part = synth.canonical_layer(args.seed, 0, E, H, I, experts=need, fmt=cfg.get("fmt", "nvfp4"))
             for j, e in enumerate(need):
                 cache[e] = {n: {f: m[f][j] for f in ("codes", "scales", "g", "a")} for n, m in part.items()}
         return {n: {f: np.stack([cache[e][n][f] for e in sel]) for f in ("codes", "scales", "g", "a")}
@@ -344,12 +351,13 @@ def main():
 
     # one handle serves every layer (it holds the shapes only); per layer its
     # packed weights, router and (Zipf) router bias
-    layer = moe.Layer(E, k, H, I, C, device=local)
+    fmt = cfg.get("fmt", "nvfp4")
+    layer = moe.Layer(E, k, H, I, C, device=local, flags=moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0)
     router_std = synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0
     packed, Wr_ds, bias_ds, biases = [], [], [], []
     canon = None
     for li in range(NL):
-        cl = synth_dev.canonical_layer_device(args.seed, li, E, H, I, dev)
+        cl = synth_dev.canonical_layer_device(args.seed, li, E, H, I, dev, fmt=fmt)
         pk = moe.alloc_packed(layer, dev)
         moe.moe_pack_weights(layer, cl, pk)
         packed.append(pk)
@@ -514,7 +522,10 @@ def main():
     tokens = C * args.steps * NL * world
     tok_s = tokens / (ms / 1e3)
     avg_distinct = sum(distinct[(i % ROTATE)] for i in range(args.steps)) / args.steps
-    expert_bytes = E and (EXPERT_BYTES_K3 if (H, I) == (3584, 3072) else 3 * (I * H // 2 + I * H // 16 + 8))
+    if fmt == "mxfp4":
+        expert_bytes = 3 * (I * H // 2 + I * H // 32 + 8)
+    else:
+        expert_bytes = EXPERT_BYTES_K3 if (H, I) == (3584, 3072) else 3 * (I * H // 2 + I * H // 16 + 8)
     hbm_gbs = avg_distinct * expert_bytes * world / (ms_per_step * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (gate/up), per-stage CUDA events
@@ -534,7 +545,7 @@ def main():
     stream.synchronize()
     gu_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof)]
     dn_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_prof)]
-    gu_bytes_per_expert = 2 * (I * H // 2 + I * H // 16)
+    gu_bytes_per_expert = 2 * (I * H // 2 + I * H // (32 if fmt == "mxfp4" else 16))
     gu_units = sum(len(set(ids[i % ROTATE][0].cpu().numpy().ravel().tolist())) for i in range(n_prof)) / n_prof
     gu_avg = float(np.mean(gu_ms))
     dn_avg = float(np.mean(dn_ms))

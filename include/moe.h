@@ -69,18 +69,28 @@ typedef enum {
  * MOE_FLAG_TIMEOUT is raised and the call's ids are all -1. */
 #define MOE_CONFIG_TEST_ROUTER_STALL 0x80000000u
 
+/* moe_config.flags: the layer's weights are MXFP4 (OCP Microscaling: e2m1
+ * codes as in NVFP4, one e8m0 scale byte per 32 elements along K, value
+ * 2^(byte - 127), 0xFF = NaN), the format of the ggml MUL_MAT_ID microbench in
+ * "Kimi-K3 on 2x A40 - measured findings" (section "Why the placement
+ * experiments all looked the same").  moe_fp4_tensor.scales is then
+ * [E][rows][K/32] and global_scale still multiplies the matrix (pass 1.0 for
+ * plain MXFP4).  Every C runs on the decode kernels (groups of 8 tokens, each
+ * expert read once per group); the tcgen05 grouped path is NVFP4 only. */
+#define MOE_CONFIG_MXFP4 0x1u
+
 typedef struct {
   int32_t num_experts;   /* E, 1 .. 1024 */
   int32_t top_k;         /* k, 1 .. min(32, E) */
   int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 4096 */
   int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 4096 */
   int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
-  uint32_t flags;        /* 0 (or the test hook MOE_CONFIG_TEST_ROUTER_STALL) */
+  uint32_t flags;        /* 0, MOE_CONFIG_MXFP4, or the test hook MOE_CONFIG_TEST_ROUTER_STALL */
 } moe_config;
 
 typedef struct {
   const uint8_t *codes;        /* device, [E][rows][K/2] */
-  const uint8_t *scales;       /* device, [E][rows][K/16] */
+  const uint8_t *scales;       /* device, [E][rows][K/16] e4m3 (NVFP4) or [E][rows][K/32] e8m0 (MXFP4) */
   const float *global_scale;   /* device, [E] */
   const float *input_scale;    /* device, [E] (copied into the packed buffer, unused) */
 } moe_fp4_tensor;
@@ -102,8 +112,9 @@ moe_status moe_layer_destroy(moe_layer_t layer);
 
 /* Bytes of the packed weight buffer moe_pack_weights writes.  For H and I
  * multiples of 512 it equals E * (bytes of one canonical expert) + 16: the
- * packer reorders bytes and adds nothing but a 16-byte status trailer.
- * Smaller shapes are padded along K to a multiple of 512 with zero codes. */
+ * packer reorders bytes and adds nothing but a 16-byte status trailer (the
+ * same holds for MXFP4 layers).  Smaller shapes are padded along K to a
+ * multiple of 512 with zero codes. */
 moe_status moe_packed_bytes(moe_layer_t layer, size_t *bytes);
 
 /* Bytes of workspace route/forward need for up to `num_tokens` tokens.  The
@@ -111,13 +122,13 @@ moe_status moe_packed_bytes(moe_layer_t layer, size_t *bytes);
  * before its first use; route and forward leave it in a reusable state. */
 moe_status moe_workspace_bytes(moe_layer_t layer, int num_tokens, size_t *bytes);
 
-/* Reorder canonical NVFP4 weights (all E experts) into the packed layout the
+/* Reorder canonical NVFP4 (or MXFP4) weights (all E experts) into the packed layout the
  * kernels stream: per expert, I "gate/up pair rows" (gate row r and up row r
  * interleaved per 16-element block) then H/2 "down pair rows" (down rows 2p
  * and 2p+1 interleaved), each pair row holding its codes and then its scale
  * bytes; the 6 fp32 scalars of all experts follow.  Offline, once per layer:
  * this call synchronises `stream` and returns MOE_ERR_INVALID_VALUE if any
- * scale byte is an e4m3 NaN (0x7F or 0xFF).  `packed` (device,
+ * scale byte is a NaN (e4m3 0x7F or 0xFF; e8m0 0xFF).  `packed` (device,
  * moe_packed_bytes long) must not overlap the canonical buffers. */
 moe_status moe_pack_weights(moe_layer_t layer, const moe_canonical_weights *canon,
                             void *packed, cudaStream_t stream);

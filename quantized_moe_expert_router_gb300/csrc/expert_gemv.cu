@@ -67,9 +67,10 @@ constexpr int kDnTilesPerStage = 2;             // down projection: two tiles of
 // (decode groups of at most 2 tokens: their partials are 1/4 of a warp's
 // accumulators, so a stage's reduction slots stay small); MODE 1: down, two
 // tiles per stage.
-template <int MODE>
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
   constexpr bool GU = MODE != 1;
+  constexpr bool MX = FMT == kFmtMxfp4;
   extern __shared__ __align__(128) uint8_t ring[];   // [S][stage_bytes] then the reduction slots
   __shared__ DispatchSmem ds;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -276,9 +277,12 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
       atomicOr(a.flags, MOE_FLAG_TIMEOUT);
       break;
     }
+    // scale units: NVFP4 256 B per half slice (8 rows x 8 k-steps x 2 rows x 2
+    // groups), MXFP4 128 B (8 rows x 8 k-step pairs x 2 rows)
+    constexpr int kHalfScaleBytes = MX ? 128 : 256;
     const uint8_t *codes = ring + (size_t)slot * a.stage_bytes + (size_t)slice * 4096 + (size_t)half * 2048;
-    const uint8_t *scales =
-        ring + (size_t)slot * a.stage_bytes + (size_t)NS * 4096 + (size_t)slice * 512 + (size_t)half * 256;
+    const uint8_t *scales = ring + (size_t)slot * a.stage_bytes + (size_t)NS * 4096 +
+                            (size_t)(2 * slice + half) * kHalfScaleBytes;
 
     for (int pass = 0; pass < npass; pass++, item++) {
       const int rs = slot * NP + pass;
@@ -293,14 +297,16 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
 
       if constexpr (MODE == 0) {
         float acc[4];
-        mma_half_slice(codes, scales, bf, acc);
+        if constexpr (MX) mma_half_slice_mx(codes, scales, bf, acc);
+        else mma_half_slice(codes, scales, bf, acc);
         red[(size_t)rs * red_slot_f4 + (size_t)warp * 32 + lane] =
             make_float4(acc[0] * colinv0, acc[1] * colinv1, acc[2] * colinv0, acc[3] * colinv1);
       } else if constexpr (MODE == 2) {
         // two tiles per stage; lanes q = 0 hold the columns of tokens 0 and 1
         const int tb = a.tile_bytes / 2;
         float accA[4], accB[4];
-        mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        if constexpr (MX) mma_half_slice_x2_mx(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        else mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
         if (q == 0) {
           float4 *r4 = red + (size_t)rs * red_slot_f4;
           r4[(size_t)warp * 8 + g] = make_float4(accA[0] * colinv0, accA[1] * colinv1, accA[2] * colinv0, accA[3] * colinv1);
@@ -312,7 +318,8 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         // (both carry the slot's 2^-s), so a partial is one float2 per tile
         const int tb = a.tile_bytes / kDnTilesPerStage;
         float accA[4], accB[4];
-        mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        if constexpr (MX) mma_half_slice_x2_mx(codes, scales, codes + tb, scales + tb, bf, accA, accB);
+        else mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
         float2 *r2 = reinterpret_cast<float2 *>(red + (size_t)rs * red_slot_f4);
         r2[(size_t)warp * 32 + lane] = make_float2((accA[0] + accA[1]) * colinv0, (accA[2] + accA[3]) * colinv0);
         r2[(size_t)(W + warp) * 32 + lane] = make_float2((accB[0] + accB[1]) * colinv0, (accB[2] + accB[3]) * colinv0);
@@ -334,7 +341,7 @@ void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_
   *smem_bytes = s * (stage_bytes + red_stage_bytes);
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -346,23 +353,35 @@ static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE>, a);
+  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE, FMT>, a);
+}
+
+template <int FMT>
+static cudaError_t launch_fmt(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
+  return mode == 0 ? launch_one<0, FMT>(a, grid, pdl, stream)
+                   : mode == 2 ? launch_one<2, FMT>(a, grid, pdl, stream) : launch_one<1, FMT>(a, grid, pdl, stream);
 }
 
 cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
-  return mode == 0 ? launch_one<0>(a, grid, pdl, stream)
-                   : mode == 2 ? launch_one<2>(a, grid, pdl, stream) : launch_one<1>(a, grid, pdl, stream);
+  return a.fmt == kFmtMxfp4 ? launch_fmt<kFmtMxfp4>(mode, a, grid, pdl, stream)
+                            : launch_fmt<kFmtNvfp4>(mode, a, grid, pdl, stream);
+}
+
+template <int MODE, int FMT>
+static cudaError_t allow_smem(int smem) {
+  return cudaFuncSetAttribute(expert_gemv_kernel<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 cudaError_t gemv_setup() {
   // the largest dynamic shared memory any geometry requests (the attribute is
   // per kernel and device, so it must not depend on the layer that sets it)
   const int smem = kGemvSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(expert_gemv_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(expert_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(expert_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = allow_smem<0, kFmtNvfp4>(smem);
+  if (err == cudaSuccess) err = allow_smem<1, kFmtNvfp4>(smem);
+  if (err == cudaSuccess) err = allow_smem<2, kFmtNvfp4>(smem);
+  if (err == cudaSuccess) err = allow_smem<0, kFmtMxfp4>(smem);
+  if (err == cudaSuccess) err = allow_smem<1, kFmtMxfp4>(smem);
+  if (err == cudaSuccess) err = allow_smem<2, kFmtMxfp4>(smem);
   return err;
 }
 

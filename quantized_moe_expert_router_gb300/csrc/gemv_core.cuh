@@ -358,4 +358,78 @@ __device__ __forceinline__ void mma_half_slice_x2(const uint8_t *codesA, const u
   }
 }
 
+// ---------------------------------------------------------------- MXFP4
+// e8m0 scale byte -> fp32 2^(b - 127) (b = 0 gives the subnormal 2^-127; the
+// packer rejects the NaN byte 0xFF).
+__device__ __forceinline__ float e8m0_to_float(uint32_t b) { return __uint_as_float(b ? (b << 23) : 0x00400000u); }
+
+// The MXFP4 forms of the two steps above.  A block scale covers 32 elements
+// (two k-steps), a power of two that f16 cannot always hold, so it is applied
+// in fp32 after the MMA: the two k-steps of a pair are multiplied with the
+// raw e2m1 codes (exact in f16) into a fresh accumulator, which is then
+// scaled by the rowA / rowB e8m0 values and added to the running sum.  The
+// scale unit of row pair g for the warp's 16 k-steps is 16 bytes: the (rowA,
+// rowB) bytes of its 8 k-step pairs.
+__device__ __forceinline__ void mx_pair_step(const uint32_t cw0, const uint32_t cw1, const uint32_t (&b0)[2],
+                                             const uint32_t (&b1)[2], uint32_t sab, float (&c)[4]) {
+  float t[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t A[4];
+  e2m1x8_to_f16x2(cw0, A);
+  mma16816(t, A, b0[0], b0[1]);
+  e2m1x8_to_f16x2(cw1, A);
+  mma16816(t, A, b1[0], b1[1]);
+  const float fa = e8m0_to_float(sab & 0xFFu), fb = e8m0_to_float((sab >> 8) & 0xFFu);
+  c[0] = fmaf(t[0], fa, c[0]);
+  c[1] = fmaf(t[1], fa, c[1]);
+  c[2] = fmaf(t[2], fb, c[2]);
+  c[3] = fmaf(t[3], fb, c[3]);
+}
+
+__device__ __forceinline__ void mma_half_slice_mx(const uint8_t *codes, const uint8_t *scales,
+                                                  const uint32_t (&bf)[kWarpSteps][2], float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  const uint4 sc = *reinterpret_cast<const uint4 *>(scales + g * 16);
+  const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
+  float c2[2][4] = {};
+#pragma unroll
+  for (int qg = 0; qg < kWarpSteps / 4; qg++) {
+    const uint4 cw = *reinterpret_cast<const uint4 *>(codes + ((size_t)qg * 32 + lane) * 16);
+    const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int pp = 0; pp < 2; pp++) {
+      const int P = 2 * qg + pp;                       // k-step pair of the warp's 8
+      mx_pair_step(cws[2 * pp], cws[2 * pp + 1], bf[2 * P], bf[2 * P + 1], scs[P >> 1] >> (16 * (P & 1)), c2[pp]);
+    }
+  }
+#pragma unroll
+  for (int c4 = 0; c4 < 4; c4++) acc[c4] = c2[0][c4] + c2[1][c4];
+}
+
+__device__ __forceinline__ void mma_half_slice_x2_mx(const uint8_t *codesA, const uint8_t *scalesA, const uint8_t *codesB,
+                                                     const uint8_t *scalesB, const uint32_t (&bf)[kWarpSteps][2],
+                                                     float (&accA)[4], float (&accB)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  const uint4 sa = *reinterpret_cast<const uint4 *>(scalesA + g * 16);
+  const uint4 sb = *reinterpret_cast<const uint4 *>(scalesB + g * 16);
+  const uint32_t sas[4] = {sa.x, sa.y, sa.z, sa.w}, sbs[4] = {sb.x, sb.y, sb.z, sb.w};
+  float ca[4] = {}, cb[4] = {};
+#pragma unroll
+  for (int qg = 0; qg < kWarpSteps / 4; qg++) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(codesA + ((size_t)qg * 32 + lane) * 16);
+    const uint4 wb = *reinterpret_cast<const uint4 *>(codesB + ((size_t)qg * 32 + lane) * 16);
+    const uint32_t was[4] = {wa.x, wa.y, wa.z, wa.w}, wbs[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int pp = 0; pp < 2; pp++) {
+      const int P = 2 * qg + pp;
+      mx_pair_step(was[2 * pp], was[2 * pp + 1], bf[2 * P], bf[2 * P + 1], sas[P >> 1] >> (16 * (P & 1)), ca);
+      mx_pair_step(wbs[2 * pp], wbs[2 * pp + 1], bf[2 * P], bf[2 * P + 1], sbs[P >> 1] >> (16 * (P & 1)), cb);
+    }
+  }
+#pragma unroll
+  for (int c4 = 0; c4 < 4; c4++) {
+    accA[c4] = ca[c4];
+    accB[c4] = cb[c4];
+  }
+}
+
 }  // namespace moe

@@ -12,6 +12,7 @@ struct PackArgs {
   uint8_t *packed;
   int32_t *status;   // in the packed trailer
   int E, H, I, w_gu, w_dn;
+  int fmt;           // kFmtNvfp4: e4m3 scales per 16 elements; kFmtMxfp4: e8m0 per 32
   size_t dn_region_off, expert_bytes, scalars_off;
 };
 cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream);
@@ -60,6 +61,7 @@ struct GemvArgs {
   int stage_bytes;           // bytes of one ring stage (one stage unit)
   int red_stage_f4;          // reduction slots of one stage, in float4
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
+  int fmt;                   // kFmtNvfp4 or kFmtMxfp4 (scale unit layout and decode)
 };
 // Ring geometry and dynamic shared memory of one kernel.
 void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_bytes);

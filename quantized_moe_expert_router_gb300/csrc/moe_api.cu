@@ -60,7 +60,8 @@ const char *moe_status_string(moe_status s) {
 moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out) {
   if (!cfg || !out) return MOE_ERR_INVALID_ARG;
   const moe_config c = *cfg;
-  if ((c.flags & ~(uint32_t)MOE_CONFIG_TEST_ROUTER_STALL) != 0 || c.max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~(uint32_t)(MOE_CONFIG_TEST_ROUTER_STALL | MOE_CONFIG_MXFP4)) != 0 || c.max_tokens < 1)
+    return MOE_ERR_INVALID_ARG;
   if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.top_k < 1 || c.top_k > moe::kMaxTopK || c.top_k > c.num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.hidden < 64 || c.hidden % 64 || c.hidden > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -75,14 +76,16 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   moe_layer *L = new (std::nothrow) moe_layer();
   if (!L) return MOE_ERR_OUT_OF_MEMORY;
   L->cfg = c;
+  L->fmt = (c.flags & MOE_CONFIG_MXFP4) ? moe::kFmtMxfp4 : moe::kFmtNvfp4;
   L->device = device;
   L->num_sms = sms;
   L->Hp = (int)align_up(c.hidden, moe::kKAlign);
   L->Ip = (int)align_up(c.intermediate, moe::kKAlign);
   L->w_gu = L->Hp / moe::kKAlign;
   L->w_dn = L->Ip / moe::kKAlign;
-  L->gu_tile_bytes = (size_t)L->w_gu * moe::kTileSliceBytes;
-  L->dn_tile_bytes = (size_t)L->w_dn * moe::kTileSliceBytes;
+  const size_t slice_bytes = L->fmt == moe::kFmtMxfp4 ? moe::kTileSliceBytesMx : moe::kTileSliceBytes;
+  L->gu_tile_bytes = (size_t)L->w_gu * slice_bytes;
+  L->dn_tile_bytes = (size_t)L->w_dn * slice_bytes;
   L->dn_region_off = (size_t)(c.intermediate / 8) * L->gu_tile_bytes;
   L->expert_bytes = L->dn_region_off + (size_t)(c.hidden / 16) * L->dn_tile_bytes;
   L->scalars_off = (size_t)c.num_experts * L->expert_bytes;
@@ -144,6 +147,7 @@ moe_status moe_pack_weights(moe_layer_t L, const moe_canonical_weights *cw, void
   a.status = status;
   a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.I = L->cfg.intermediate;
   a.w_gu = L->w_gu; a.w_dn = L->w_dn;
+  a.fmt = L->fmt;
   a.dn_region_off = L->dn_region_off; a.expert_bytes = L->expert_bytes;
   a.scalars_off = L->scalars_off;
   err = moe::launch_pack(a, L->num_sms, stream);
@@ -218,10 +222,13 @@ moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.k = k; a.E = L->cfg.num_experts; a.H = H; a.I = I;
   a.expert_bytes = L->expert_bytes;
+  a.fmt = L->fmt;
 
   cudaError_t err = cudaSuccess;
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
-  if (C > moe::kGemvTokens) {
+  // C > 8: the grouped tcgen05 path (NVFP4); MXFP4 layers run every C on the
+  // decode kernels, in groups of 8 tokens
+  if (C > moe::kGemvTokens && L->fmt == moe::kFmtNvfp4) {
     // expert-major passes of up to kGroupTokens tokens
     moe::GroupArgs g = {};
     g.packed = pk;

@@ -26,6 +26,8 @@ constexpr int kRouteSplits = 4;          // route, C > 8: K ranges of the logits
 constexpr int kGemvSmemBytes = 211968;   // dynamic shared memory of one expert-GEMV CTA (+ ~20 KB static)
 constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped-GEMM CTA at most (+ ~12 KB static)
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
+constexpr int kTileSliceBytesMx = 4352;  // the same for MXFP4: 4096 code + 256 scale bytes (one per 32 elements)
+constexpr int kFmtNvfp4 = 0, kFmtMxfp4 = 1;
 
 // Workspace control block (first 256 bytes of the workspace).
 struct WsControl {
@@ -64,12 +66,13 @@ struct WsLayout {
 // stage-event hook.
 struct moe_layer {
   moe_config cfg;
+  int fmt;                    // kFmtNvfp4 or kFmtMxfp4 (MOE_CONFIG_MXFP4)
   int device;
   int num_sms;
   int Hp, Ip;                 // K of gate/up and of down, padded to kKAlign
   int w_gu, w_dn;             // 512-element K-slices (= consumer warps of a group)
-  size_t gu_tile_bytes;       // w_gu * kTileSliceBytes: 8 gate/up pair rows
-  size_t dn_tile_bytes;       // w_dn * kTileSliceBytes: 8 down pair rows
+  size_t gu_tile_bytes;       // w_gu * slice bytes (kTileSliceBytes or kTileSliceBytesMx): 8 gate/up pair rows
+  size_t dn_tile_bytes;       // w_dn * slice bytes: 8 down pair rows
   size_t dn_region_off;       // offset of the down tiles inside an expert
   size_t expert_bytes;        // packed bytes of one expert (without scalars)
   size_t scalars_off;         // float [E][6] : g_gate a_gate g_up a_up g_down a_down

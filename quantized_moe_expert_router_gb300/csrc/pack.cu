@@ -1,4 +1,4 @@
-// pack.cu -- canonical NVFP4 expert weights -> the packed "tile" layout the
+// pack.cu -- canonical NVFP4 / MXFP4 expert weights -> the packed "tile" layout the
 // expert kernels stream (byte moves only; no value changes).
 //
 // A pair row is two matrix rows that share K: gate row r with up row r
@@ -18,6 +18,10 @@
 // rowB), so a warp loads a 16x16 weight block per k-step with one 4-byte
 // share of a 16-byte shared-memory load.  The scale unit of row g holds, for
 // 8 k-steps, the two e4m3 bytes (rowA scale, rowB scale) of each k-step.
+//
+// MXFP4 (one e8m0 scale per 32 elements) keeps the code units and halves the
+// scale region of a slice: [2 units of 8 k-step pairs][8 rows g][16 bytes],
+// the (rowA, rowB) bytes of each pair (W * 256 bytes); a NaN is the byte 0xFF.
 //
 // Packed expert e (at e * expert_bytes): I/8 gate/up tiles, then H/16 down
 // tiles.  After all experts: float [E][6] = g_gate a_gate g_up a_up g_down
@@ -58,18 +62,20 @@ __global__ void pack_kernel(const PackArgs a) {
     const int64_t e = et / tiles, tile = et % tiles;
     const int K = gu ? a.H : a.I;                        // real K of the rows
     const int64_t p = tile * 8 + g;                      // pair row
+    const bool mx = a.fmt == kFmtMxfp4;
+    const int SB = mx ? 32 : 16;                         // elements per scale byte
     const uint8_t *ca, *cb, *sa, *sb;
     if (gu) {
       const int64_t row = e * a.I + p;
       ca = a.gate_codes + row * (K / 2); cb = a.up_codes + row * (K / 2);
-      sa = a.gate_scales + row * (K / 16); sb = a.up_scales + row * (K / 16);
+      sa = a.gate_scales + row * (K / SB); sb = a.up_scales + row * (K / SB);
     } else {
       const int64_t row = e * a.H + 2 * p;
       ca = a.down_codes + row * (K / 2); cb = ca + K / 2;
-      sa = a.down_scales + row * (K / 16); sb = sa + K / 16;
+      sa = a.down_scales + row * (K / SB); sb = sa + K / SB;
     }
     uint8_t *tb = a.packed + e * a.expert_bytes + (gu ? 0 : a.dn_region_off) +
-                  tile * (size_t)W * kTileSliceBytes;
+                  tile * (size_t)W * (mx ? kTileSliceBytesMx : kTileSliceBytes);
     // code bytes of this slice (k-steps 32w .. 32w+31), zero past K
     const int kstep0 = 32 * w, ksteps = K / 16;
 #pragma unroll 1
@@ -98,6 +104,35 @@ __global__ void pack_kernel(const PackArgs a) {
       }
     }
     uint8_t *sbase = tb + (size_t)W * 4096;
+    if (mx) {
+      // MXFP4: per slice 2 units (k-steps 16u .. 16u + 15 = k-step pairs
+      // 8u .. 8u + 7) of [8 rows g][16 bytes]: (rowA, rowB) e8m0 bytes of
+      // each pair
+      const int pair0 = kstep0 / 2, npairs = K / 32;
+#pragma unroll 1
+      for (int u = 0; u < 2; u++) {
+        uint32_t sw[4];
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int i2 = 0; i2 < 2; i2++) {
+            const int P = pair0 + 8 * u + 2 * h + i2;
+            uint32_t xa = 0, xb = 0;
+            if (P < npairs) {
+              xa = sa[P];
+              xb = sb[P];
+              nan_seen |= (xa == 0xFFu) | (xb == 0xFFu);
+            }
+            v |= (xa | (xb << 8)) << (16 * i2);
+          }
+          sw[h] = v;
+        }
+        *reinterpret_cast<uint4 *>(sbase + (size_t)w * 256 + ((size_t)u * 8 + g) * 16) =
+            make_uint4(sw[0], sw[1], sw[2], sw[3]);
+      }
+      continue;
+    }
 #pragma unroll 1
     for (int q8 = 0; q8 < 4; q8++) {
       uint32_t sw[4];

@@ -32,17 +32,24 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             lib.synth_generate_matrices.restype = ctypes.c_int
+            lib.synth_generate_matrices_mx.argtypes = [
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.synth_generate_matrices_mx.restype = ctypes.c_int
             _lib = lib
     return _lib
 
 
 def canonical_layer_device(seed: int, layer: int, E: int, H: int, I: int, device="cuda:0",
-                           stream=None):
-    """Canonical NVFP4 layer on the device: dict gate/up/down -> {'codes',
-    'scales', 'g', 'a'} torch tensors ([E][rows][K/2] uint8, [E][rows][K/16]
-    uint8, [E] float32, [E] float32)."""
+                           stream=None, fmt="nvfp4"):
+    """Canonical NVFP4 (or MXFP4) layer on the device: dict gate/up/down ->
+    {'codes', 'scales', 'g', 'a'} torch tensors ([E][rows][K/2] uint8,
+    [E][rows][K/16] (NVFP4) or [E][rows][K/32] (MXFP4) uint8, [E] float32,
+    [E] float32; MXFP4 matrices have g = 1)."""
     lib = _load()
     g, a = global_scales(seed, layer, E)
+    if fmt == "mxfp4":
+        g = np.ones_like(g)
     stream = stream or torch.cuda.current_stream(device)
     out = {}
     for mat, name, rows, K in ((MAT_GATE, "gate", I, H), (MAT_UP, "up", I, H), (MAT_DOWN, "down", H, I)):
@@ -51,10 +58,15 @@ def canonical_layer_device(seed: int, layer: int, E: int, H: int, I: int, device
         g_d = torch.from_numpy(g[mat].copy()).to(device)
         a_d = torch.from_numpy(a[mat].copy()).to(device)
         codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
-        scales = torch.empty((E, rows, K // 16), dtype=torch.uint8, device=device)
-        rc = lib.synth_generate_matrices(keys_d.data_ptr(), g_d.data_ptr(), E, rows, K, W_COEF,
-                                         codes.data_ptr(), scales.data_ptr(),
-                                         ctypes.c_void_p(stream.cuda_stream))
+        if fmt == "mxfp4":
+            scales = torch.empty((E, rows, K // 32), dtype=torch.uint8, device=device)
+            rc = lib.synth_generate_matrices_mx(keys_d.data_ptr(), E, rows, K, W_COEF, codes.data_ptr(),
+                                                scales.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+        else:
+            scales = torch.empty((E, rows, K // 16), dtype=torch.uint8, device=device)
+            rc = lib.synth_generate_matrices(keys_d.data_ptr(), g_d.data_ptr(), E, rows, K, W_COEF,
+                                             codes.data_ptr(), scales.data_ptr(),
+                                             ctypes.c_void_p(stream.cuda_stream))
         if rc != 0:
             raise RuntimeError(f"synth_generate_matrices failed with cudaError {rc}")
         out[name] = {"codes": codes, "scales": scales, "g": g_d, "a": a_d, "_keys": keys_d}

@@ -1,8 +1,8 @@
 // synth.cu -- device twin of the host weight generator in synth/__init__.py.
 //
-// Generates canonical NVFP4 expert matrices (codes, scales) from the same
+// Generates canonical NVFP4 and MXFP4 expert matrices (codes, scales) from the same
 // SplitMix64 counter streams, the same Irwin-Hall(8) normal deviates and the
-// same NVFP4 encoder, bit for bit: every step is an integer operation, a
+// same NVFP4 / MXFP4 encoders, bit for bit: every step is an integer operation, a
 // comparison, or one correctly rounded float64 operation (built with
 // -fmad=false so no multiply-add is fused).  Input generation only: nothing
 // here decodes weights or computes any part of the MoE layer.
@@ -97,9 +97,59 @@ __global__ void gen_matrix_kernel(const uint64_t *keys, const float *g, int n, i
   }
 }
 
+// One thread per 32-element block (MXFP4, OCP MX): shared exponent
+// e = floor(log2 amax) - 2 clamped to [-127, 127] (-127 for an all-zero
+// block), scale byte e + 127, codes = nearest e2m1 of w / 2^e.
+__global__ void gen_matrix_mx_kernel(const uint64_t *keys, int n, int rows, int K, double w_coef, uint8_t *codes,
+                                     uint8_t *scales) {
+  const int64_t blocks_per_row = K / 32;
+  const int64_t per_expert = (int64_t)rows * blocks_per_row;
+  const int64_t total = per_expert * n;
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = blk / per_expert, rb = blk % per_expert;
+    const int64_t r = rb / blocks_per_row, bb = rb % blocks_per_row;
+    const uint64_t key = keys[e];
+    const uint64_t i0 = (uint64_t)(r * K + bb * 32);
+    double w[32];
+    double amax = 0.0;
+    for (int j = 0; j < 32; j++) {
+      w[j] = ((double)ih8_sum(key, i0 + j) - 262140.0) * w_coef;
+      amax = fmax(amax, fabs(w[j]));
+    }
+    int ex = 0;
+    if (amax > 0.0) frexp(amax, &ex);
+    int sh = amax > 0.0 ? ex - 1 - 2 : -127;
+    sh = sh < -127 ? -127 : (sh > 127 ? 127 : sh);
+    const double sc = ldexp(1.0, sh);
+    uint32_t c[32];
+    for (int j = 0; j < 32; j++) c[j] = e2m1_encode(w[j], sc);
+    uint32_t out[4];
+    for (int q = 0; q < 4; q++) {
+      out[q] = 0;
+      for (int j = 0; j < 8; j++) out[q] |= c[8 * q + j] << (4 * j);
+    }
+    *reinterpret_cast<uint4 *>(codes + e * (per_expert * 16) + rb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+    scales[e * per_expert + rb] = (uint8_t)(sh + 127);
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+// Canonical MXFP4 [n][rows][K/2] codes and [n][rows][K/32] e8m0 scales of one
+// matrix kind for n experts (the same weight draws as the NVFP4 generator).
+int synth_generate_matrices_mx(const uint64_t *keys, int n, int rows, int K, double w_coef, uint8_t *codes,
+                               uint8_t *scales, cudaStream_t stream) {
+  if (n <= 0 || rows <= 0 || K <= 0 || K % 32) return (int)cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  gen_matrix_mx_kernel<<<sms * 8, 256, 0, stream>>>(keys, n, rows, K, w_coef, codes, scales);
+  return (int)cudaGetLastError();
+}
+
 
 // Canonical NVFP4 [n][rows][K/2] codes and [n][rows][K/16] scales of one
 // matrix kind for n experts; keys[n] (device) are the per-expert stream keys,

@@ -29,14 +29,14 @@ def to_device(canon_h):
 
 class GpuLayer:
     def __init__(self, E, k, H, I, max_tokens, seed=0, layer=0, device_gen=False, router_std=1.0,
-                 zipf=False):
+                 zipf=False, fmt="nvfp4"):
         self.E, self.k, self.H, self.I = E, k, H, I
-        self.seed, self.layer_id = seed, layer
-        self.h = moe.Layer(E, k, H, I, max_tokens)
+        self.seed, self.layer_id, self.fmt = seed, layer, fmt
+        self.h = moe.Layer(E, k, H, I, max_tokens, flags=moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0)
         if device_gen:
-            self.canon = synth_dev.canonical_layer_device(seed, layer, E, H, I, DEV)
+            self.canon = synth_dev.canonical_layer_device(seed, layer, E, H, I, DEV, fmt=fmt)
         else:
-            self.canon_h = synth.canonical_layer(seed, layer, E, H, I)
+            self.canon_h = synth.canonical_layer(seed, layer, E, H, I, fmt=fmt)
             self.canon = to_device(self.canon_h)
         self.packed = moe.alloc_packed(self.h)
         moe.moe_pack_weights(self.h, self.canon, self.packed)
@@ -81,7 +81,7 @@ class GpuLayer:
         sel = sorted(set(int(e) for e in ids.ravel()))
         remap = {e: i for i, e in enumerate(sel)}
         y = oracle.moe_forward(self.host_weights(sel), x_bits, np.vectorize(remap.get)(ids).astype(np.int32), w,
-                               threads=threads)
+                               threads=threads, fmt=getattr(self, "fmt", "nvfp4"))
         return ids, w, gap, y
 
 
@@ -592,3 +592,96 @@ def _retarget(L, h, k):
     v.oracle = GpuLayer.oracle.__get__(v)
     v.host_weights = GpuLayer.host_weights.__get__(v)
     return v
+
+
+# ------------------------------------------------------------------ MXFP4 weights
+
+def test_device_generator_matches_host_mxfp4():
+    E, H, I = 3, 256, 192
+    d = synth_dev.canonical_layer_device(0, 5, E, H, I, DEV, fmt="mxfp4")
+    h = synth.canonical_layer(0, 5, E, H, I, fmt="mxfp4")
+    for n in ("gate", "up", "down"):
+        for f in ("codes", "scales", "g"):
+            assert (d[n][f].cpu().numpy() == h[n][f]).all(), (n, f)
+
+
+def _unpack_tiles_mx(buf, ntiles, W, K):
+    """MXFP4 tiles -> (rowA codes, rowB codes, rowA scales, rowB scales)."""
+    tb = W * 4352
+    t = buf[: ntiles * tb].reshape(ntiles, tb)
+    codes = t[:, : W * 4096].reshape(ntiles, W, 8, 8, 4, 4, 4).transpose(0, 3, 1, 2, 5, 4, 6)
+    S = W * 32
+    c = codes.reshape(ntiles, 8, S, 4, 4)
+    A = np.empty((ntiles, 8, S, 8), np.uint8)
+    B = np.empty((ntiles, 8, S, 8), np.uint8)
+    A[..., :4], A[..., 4:] = c[..., 0], c[..., 2]
+    B[..., :4], B[..., 4:] = c[..., 1], c[..., 3]
+    sc = t[:, W * 4096:].reshape(ntiles, W, 2, 8, 8, 2).transpose(0, 3, 1, 2, 4, 5).reshape(ntiles, 8, W * 16, 2)
+    rows = ntiles * 8
+    return (A.reshape(rows, S * 8)[:, : K // 2], B.reshape(rows, S * 8)[:, : K // 2],
+            sc[..., 0].reshape(rows, W * 16)[:, : K // 32], sc[..., 1].reshape(rows, W * 16)[:, : K // 32])
+
+
+@pytest.mark.parametrize("E,H,I", [(5, 256, 192), (2, 1024, 576)])
+def test_pack_layout_roundtrip_mxfp4(E, H, I):
+    L = GpuLayer(E, 2, H, I, 1, fmt="mxfp4")
+    packed = L.packed.cpu().numpy()
+    assert packed.size == moe.moe_packed_bytes(L.h)
+    Wg, Wd = -(-H // 512), -(-I // 512)
+    gu_bytes = (I // 8) * Wg * 4352
+    ebytes = gu_bytes + (H // 16) * Wd * 4352
+    for e in range(E):
+        base = e * ebytes
+        ga, ub, gs, us = _unpack_tiles_mx(packed[base: base + gu_bytes], I // 8, Wg, H)
+        assert (ga == L.canon_h["gate"]["codes"][e]).all() and (ub == L.canon_h["up"]["codes"][e]).all()
+        assert (gs == L.canon_h["gate"]["scales"][e]).all() and (us == L.canon_h["up"]["scales"][e]).all()
+        da, db, das, dbs = _unpack_tiles_mx(packed[base + gu_bytes: base + ebytes], H // 16, Wd, I)
+        assert (da == L.canon_h["down"]["codes"][e][0::2]).all() and (db == L.canon_h["down"]["codes"][e][1::2]).all()
+        assert (das == L.canon_h["down"]["scales"][e][0::2]).all()
+        assert (dbs == L.canon_h["down"]["scales"][e][1::2]).all()
+
+
+def test_packed_bytes_mxfp4_k3_shape():
+    h = moe.Layer(896, 16, 3584, 3072, 1, flags=moe.CONFIG_MXFP4)
+    assert moe.moe_packed_bytes(h) == 896 * (3 * 3072 * 3584 * 17 // 32 + 24) + 16
+
+
+def test_pack_rejects_nan_scale_mxfp4():
+    L = GpuLayer(4, 2, 256, 192, 1, fmt="mxfp4")
+    L.canon["up"]["scales"][1, 7, 3] = 0xFF
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_pack_weights(L.h, L.canon, L.packed)
+    assert ei.value.status == 3
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 8, 11, 20])
+def test_mxfp4_tiny_parity(C):
+    # C > 8 runs in groups of 8 tokens on the decode kernels
+    L = GpuLayer(32, 4, 256, 192, 24, fmt="mxfp4")
+    x = gapped_tokens(0, 0, C, 256, L.Wr, 4)
+    check_layer(L, x, f"mxfp4 tiny C={C}")
+
+
+@pytest.mark.parametrize("E,k,H,I,C", [(12, 3, 64, 128, 5), (40, 8, 576, 320, 2), (7, 7, 192, 1088, 1),
+                                       (9, 2, 4096, 4096, 3)])
+def test_mxfp4_odd_shapes_parity(E, k, H, I, C):
+    L = GpuLayer(E, k, H, I, C, seed=3, fmt="mxfp4")
+    x = gapped_tokens(3, 0, C, H, L.Wr, k)
+    check_layer(L, x, f"mxfp4 E{E} k{k} H{H} I{I} C{C}")
+
+
+@pytest.fixture(scope="module")
+def k3_layer_mx():
+    L = GpuLayer(896, 16, 3584, 3072, 8, seed=0, device_gen=True, fmt="mxfp4")
+    yield L
+    del L.canon
+
+
+@pytest.mark.parametrize("C,k", [(1, 16), (1, 8), (7, 16), (7, 8)])
+def test_k3_mxfp4_parity(k3_layer_mx, C, k):
+    # the ggml microbench's shapes: 8 or 16 of the K3-shape experts at C = 1
+    # and C = 7, MXFP4
+    L = k3_layer_mx if k == 16 else _retarget(k3_layer_mx, moe.Layer(896, k, 3584, 3072, 8, flags=moe.CONFIG_MXFP4), k)
+    x = gapped_tokens(6, 0, C, 3584, L.Wr, k)
+    check_layer(L, x, f"k3 mxfp4 C={C} top-{k}")
+    check_layer(L, x, f"k3 mxfp4 C={C} top-{k} one call", fused=True)
