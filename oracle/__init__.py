@@ -68,6 +68,12 @@ def _load():
             lib.oracle_moe_forward_fmt.restype = i32
             lib.oracle_moe_forward_mt_fmt.argtypes = [i32] * 7 + [P, P, P] * 3 + [P, P, P, P]
             lib.oracle_moe_forward_mt_fmt.restype = i32
+            lib.oracle_dense_gemv.argtypes = [i32, i32, i32, P, P, ctypes.c_float, i32, P, P]
+            lib.oracle_dense_gemv.restype = i32
+            lib.oracle_rms_norm.argtypes = [i32, i32, P, P, ctypes.c_double, P]
+            lib.oracle_rms_norm.restype = i32
+            lib.oracle_bf16_round.argtypes = [ctypes.c_double]
+            lib.oracle_bf16_round.restype = ctypes.c_uint16
             lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_value.restype = ctypes.c_double
             lib.oracle_expert_bytes.argtypes = [i64, i64]
@@ -219,3 +225,79 @@ def full_layer(weights, Wr, x_bf16, k, bias=None, fmt="nvfp4"):
     ids, w, gap = route(logits, k)
     y = moe_forward(weights, x_bf16, ids, w, fmt=fmt)
     return ids, w, gap, y
+
+
+# ------------------------------------------------- around the routed sum
+
+def dense_gemv(codes, scales, g, x, fmt="nvfp4"):
+    """y [C][M] = W x for W [M][K] 4-bit (codes [M][K/2], scales, tensor
+    scale g) and x float64 [C][K] (oracle_dense_gemv)."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    x = _c(np.atleast_2d(x), np.float64)
+    M, K = codes.shape[0], codes.shape[1] * 2
+    C = x.shape[0]
+    y = np.empty((C, M), np.float64)
+    rc = _load().oracle_dense_gemv(_FMT[fmt], M, K, _ptr(codes), _ptr(scales), float(g), C, _ptr(x), _ptr(y))
+    if rc != OK:
+        raise ValueError(f"oracle_dense_gemv failed ({rc})")
+    return y
+
+
+def rms_norm(y, gamma, eps):
+    """RMS norm of the rows of y (oracle_rms_norm)."""
+    y = _c(np.atleast_2d(y), np.float64)
+    gamma = _c(gamma, np.float32)
+    out = np.empty_like(y)
+    rc = _load().oracle_rms_norm(y.shape[0], y.shape[1], _ptr(y), _ptr(gamma), float(eps), _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_rms_norm failed ({rc})")
+    return out
+
+
+def bf16_round(v):
+    """float64 array -> bfloat16 bits (nearest, ties to even)."""
+    v = np.asarray(v, np.float64)
+    f = _load().oracle_bf16_round
+    return np.array([f(float(a)) for a in v.ravel()], np.uint16).reshape(v.shape)
+
+
+def bf16_to_f64(bits):
+    return np.array([bf16_value(int(b)) for b in np.asarray(bits).ravel()], np.float64).reshape(np.shape(bits))
+
+
+def ffn_layer(ffn, routed, Wr, u_bf16, k, bias=None, threads=1, fmt="nvfp4", ids_w=None):
+    """The MoE FFN of a Kimi-K3-class layer around the routed sum
+    ("SparkInfer-K3", "How the TP module works" and "The model"):
+
+      x   = routed_down u           (u: bf16 hidden [C][Hd]; x rounded to bf16)
+      ids, w = top-k of the router on x;  y_r = routed sum of the experts on x
+      n   = routed_norm(y_r)         (RMS norm with gamma, eps)
+      out = routed_up n + sum over the shared experts s of FFN_s(u)
+
+    ffn: dict with 'routed_down' and 'routed_up' ({'codes','scales','g'}),
+    'shared' (gate/up/down dicts over the shared experts, as the routed
+    weights), 'gamma' float32 [latent], 'eps'.  Returns (ids, w, gap, x_bf16,
+    y_r, out).  ``ids_w``: use these (ids, w) instead of the router's."""
+    u = np.asarray(u_bf16, np.uint16)
+    C = u.shape[0]
+    uf = bf16_to_f64(u)
+    rd = ffn["routed_down"]
+    x_f = dense_gemv(rd["codes"], rd["scales"], rd["g"], uf, fmt)
+    x_bf16 = bf16_round(x_f)
+    if ids_w is None:
+        ids, w, gap = route(router_logits(Wr, x_bf16, bias), k)
+    else:
+        (ids, w), gap = ids_w, None
+    y_r = moe_forward(routed, x_bf16, ids, w, threads=threads, fmt=fmt)
+    n = rms_norm(y_r, ffn["gamma"], ffn["eps"])
+    ru = ffn["routed_up"]
+    out = dense_gemv(ru["codes"], ru["scales"], ru["g"], n, fmt)
+    sh = ffn["shared"]
+    Hd = u.shape[1]
+    Is = sh["gate"]["codes"].shape[1]
+    for s in range(sh["gate"]["codes"].shape[0]):
+        mats = [(sh[m]["codes"][s], sh[m]["scales"][s], float(sh[m]["g"][s])) for m in ("gate", "up", "down")]
+        for t in range(C):
+            out[t] += expert_ffn(Hd, Is, *mats, uf[t], fmt=fmt)
+    return ids, w, gap, x_bf16, y_r, out

@@ -517,3 +517,63 @@ int oracle_moe_forward_mt(int nthreads, int C, int E, int k, int H, int I,
   return oracle_moe_forward_mt_fmt(ORACLE_FMT_NVFP4, nthreads, C, E, k, H, I, gate_codes, gate_scales, gate_g,
                                    up_codes, up_scales, up_g, down_codes, down_scales, down_g, x, ids, w, y);
 }
+
+/* ------------------------------------------------- around the routed sum */
+
+/* Dense 4-bit GEMV of C vectors: y[t][m] = sum_k W[m][k] x[t][k] in float64,
+ * W [M][K] in format `fmt` (codes [M][K/2], scales [M][K/B], tensor scale g).
+ * The latent projections routed_down (7168 -> 3584) and routed_up
+ * (3584 -> 7168) of "SparkInfer-K3", section "How the TP module works"
+ * (FfnPartial: router -> routed_down -> experts; FfnFinish: routed_norm ->
+ * routed_up -> shared experts), are of this form. */
+int oracle_dense_gemv(int fmt, int M, int K, const uint8_t *codes, const uint8_t *scales, float g, int C,
+                      const double *x, double *y) {
+  if ((fmt != ORACLE_FMT_NVFP4 && fmt != ORACLE_FMT_MXFP4) || M <= 0 || K <= 0 || C < 0 ||
+      K % fmt_block(fmt) || !codes || !scales || !x || !y)
+    return ORACLE_ERR_ARG;
+  init_tables();
+  if (fmt_has_nan(fmt, scales, (int64_t)M * (K / fmt_block(fmt)))) return ORACLE_ERR_NAN_SCALE;
+  for (int t = 0; t < C; t++)
+    for (int m = 0; m < M; m++) {
+      double s = 0.0;
+      for (int k = 0; k < K; k++) s += fp4_weight(fmt, codes, scales, g, K, m, k) * x[(int64_t)t * K + k];
+      y[(int64_t)t * M + m] = s;
+    }
+  return ORACLE_OK;
+}
+
+/* RMS norm of C vectors of length n (routed_norm, "SparkInfer-K3", "How the
+ * TP module works": it follows the complete routed sum, because
+ * rms_norm(sum of partials) != sum of rms_norm(partials)):
+ *   out[t][i] = y[t][i] / sqrt(mean_j y[t][j]^2 + eps) * gamma[i]. */
+int oracle_rms_norm(int C, int n, const double *y, const float *gamma, double eps, double *out) {
+  if (C < 0 || n <= 0 || !y || !gamma || !out || !(eps >= 0.0)) return ORACLE_ERR_ARG;
+  for (int t = 0; t < C; t++) {
+    double ss = 0.0;
+    for (int i = 0; i < n; i++) ss += y[(int64_t)t * n + i] * y[(int64_t)t * n + i];
+    const double r = 1.0 / sqrt(ss / (double)n + eps);
+    for (int i = 0; i < n; i++) out[(int64_t)t * n + i] = y[(int64_t)t * n + i] * r * (double)gamma[i];
+  }
+  return ORACLE_OK;
+}
+
+/* float64 -> bfloat16 bits, round to nearest, ties to even (finite inputs). */
+uint16_t oracle_bf16_round(double v) {
+  if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+  const int neg = v < 0.0;
+  double a = fabs(v);
+  int e;
+  frexp(a, &e);                          /* a = m 2^e, m in [0.5, 1) */
+  int eb = e - 1;                        /* a in [2^eb, 2^(eb+1)) */
+  if (eb < -126) eb = -126;              /* subnormal range: fixed spacing 2^-133 */
+  const double ulp = ldexp(1.0, eb - 7);
+  double q = a / ulp;                    /* exact: a power-of-two division */
+  double r = floor(q);
+  const double frac = q - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  const double rv = r * ulp;             /* the rounded magnitude */
+  float f = (float)rv;                   /* exact: 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)((u >> 16) | (neg ? 0x8000u : 0u));
+}

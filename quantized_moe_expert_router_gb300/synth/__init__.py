@@ -54,6 +54,9 @@ KIND_X = 3
 KIND_BIAS_PERM = 4
 KIND_GSCALE = 5
 KIND_DRAFT = 6
+KIND_FFN = 7            # the weights around the routed sum (latent projections, shared experts, norm)
+
+FFN_ROUTED_DOWN, FFN_ROUTED_UP, FFN_SHARED, FFN_GAMMA = 0, 1, 2, 3
 
 MAT_GATE, MAT_UP, MAT_DOWN = 0, 1, 2
 
@@ -240,6 +243,44 @@ def canonical_layer(seed: int, layer: int, E: int, H: int, I: int, experts=None,
             codes[j], scales[j] = expert_matrix(seed, layer, e, mat, rows, K, float(g[mat][e]), fmt)
         out[name] = {"codes": codes, "scales": scales,
                      "g": g[mat][experts].copy(), "a": a[mat][experts].copy()}
+    return out
+
+
+def ffn_matrix(seed: int, layer: int, part: int, idx: int, rows: int, K: int, fmt="nvfp4"):
+    """One N(0, 0.02) matrix [rows][K] of the FFN around the routed sum,
+    quantized like the expert weights: (codes, scales, g).  NVFP4 gets a
+    global scale g that keeps block scales unsaturated; MXFP4 g = 1."""
+    k = key(seed, KIND_FFN, layer, part, idx)
+    w = ((_ih8_sum(k, rows * K).astype(np.float64) - IH8_CENTER) * W_COEF).reshape(rows, K)
+    if fmt == "mxfp4":
+        c, sc = quantize_mxfp4(w)
+        return c, sc, np.float32(1.0)
+    g = np.float32(W_ABS_MAX / (6.0 * _E4M3_MAX) * (1.0 + 0.25 * (idx % 3)))
+    c, sc = quantize_nvfp4(w, float(g))
+    return c, sc, g
+
+
+def ffn_weights(seed: int, layer: int, hidden: int, latent: int, shared: int, shared_inter: int,
+                fmt="nvfp4", eps: float = 1e-6) -> dict:
+    """Host-generated weights around the routed sum of one layer:
+    routed_down [latent][hidden], routed_up [hidden][latent] (each
+    {'codes','scales','g','a'}), 'shared' = gate/up [S][Is][hidden] and down
+    [S][hidden][Is] in the routed experts' dict form, 'gamma' float32 [latent]
+    = 1 + 0.1 z, and 'eps'."""
+    def mat(part, idx, rows, K):
+        c, sc, g = ffn_matrix(seed, layer, part, idx, rows, K, fmt)
+        return {"codes": c, "scales": sc, "g": np.float32(g), "a": np.float32(1.0)}
+    out = {"routed_down": mat(FFN_ROUTED_DOWN, 0, latent, hidden),
+           "routed_up": mat(FFN_ROUTED_UP, 0, hidden, latent)}
+    sh = {}
+    for m, name, rows, K in ((0, "gate", shared_inter, hidden), (1, "up", shared_inter, hidden),
+                             (2, "down", hidden, shared_inter)):
+        ms = [mat(FFN_SHARED, 3 * s + m, rows, K) for s in range(shared)]
+        sh[name] = {f: np.stack([q[f] for q in ms]) for f in ("codes", "scales", "g", "a")}
+    out["shared"] = sh
+    z = normals(key(seed, KIND_FFN, layer, FFN_GAMMA, 0), latent)
+    out["gamma"] = (1.0 + 0.1 * z).astype(np.float32)
+    out["eps"] = eps
     return out
 
 
