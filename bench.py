@@ -70,6 +70,11 @@ CONFIGS = {
     "k3c7mx": dict(E=896, k=16, H=3584, I=3072, C=7, layers=1, zipf=False, fmt="mxfp4",
                    workload="K3-shape MoE layer, decode batch 7, top-16 of 896, MXFP4 (e8m0 scale per 32), "
                             "uniform routing"),
+    "k3ffnb1": dict(E=896, k=16, H=3584, I=3072, C=1, layers=1, zipf=False,
+                    ffn=dict(hidden=7168, shared=2, shared_inter=3072),
+                    workload="K3-shape MoE FFN at decode batch 1: routed_down 7168->3584, router + top-16 of 896 "
+                             "experts, routed_norm, routed_up 3584->7168, 2 shared experts (7168->3072->7168), "
+                             "NVFP4"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -374,8 +379,22 @@ def main():
         if li == 0:
             Wr, bias = Wl, bl
 
+    FFN = cfg.get("ffn")
+    if FFN:
+        # the FFN around the routed sum (one layer): its weights on the device
+        Hd = FFN["hidden"]
+        fw = synth_dev.ffn_weights_device(args.seed, 0, Hd, H, FFN["shared"], FFN["shared_inter"], dev)
+        ffn = moe.Ffn(layer, Hd, FFN["shared"], FFN["shared_inter"], eps=fw["eps"])
+        fpacked = moe.alloc_ffn_packed(ffn, dev)
+        moe.moe_ffn_pack_weights(ffn, fw, fpacked)
+        ffn_ws = moe.alloc_ffn_workspace(ffn, C, dev)
+        ffn_bytes = sum(m["codes"].numel() + m["scales"].numel() + 8 * m["g"].numel()
+                        for m in [fw["routed_down"], fw["routed_up"]] + list(fw["shared"].values()))
     # rotating token sets, distinct per rank
-    if cfg.get("draft_rho") is not None:
+    if FFN:
+        x_host = [synth.tokens(args.seed + 1000 * rank, r, C, FFN["hidden"]) for r in range(ROTATE)]
+        outs = [torch.empty((C, FFN["hidden"]), dtype=torch.float32, device=dev) for _ in range(ROTATE)]
+    elif cfg.get("draft_rho") is not None:
         x_host = [synth.draft_rows(args.seed + 1000 * rank, r, C, H, cfg["draft_rho"]) for r in range(ROTATE)]
     else:
         x_host = [synth.tokens(args.seed + 1000 * rank, r, C, H) for r in range(ROTATE)]
@@ -404,27 +423,68 @@ def main():
         cpu_sample = (sample_x, weights_for)
         threads = min(oracle.default_threads(), k)     # one token at a time: k expert FFNs in parallel
         cores, model = host_cpu()
+        if FFN:
+            fw_host = {"routed_down": {f: (fw["routed_down"][f].cpu().numpy() if f in ("codes", "scales")
+                                           else float(fw["routed_down"][f][0])) for f in ("codes", "scales", "g")},
+                       "routed_up": {f: (fw["routed_up"][f].cpu().numpy() if f in ("codes", "scales")
+                                         else float(fw["routed_up"][f][0])) for f in ("codes", "scales", "g")},
+                       "shared": {n: {f: m[f].cpu().numpy() for f in ("codes", "scales", "g", "a")}
+                                  for n, m in fw["shared"].items()},
+                       "gamma": fw["gamma"].cpu().numpy(), "eps": fw["eps"]}
+
+            def ffn_sample(budget_s, th):
+                done_, tt_, fetch = 0, 0.0, [0.0]
+
+                def fetch_w(sel):
+                    f0 = time.perf_counter()
+                    r_ = weights_for(sel)
+                    fetch[0] += time.perf_counter() - f0
+                    return r_
+                for t in range(sample_x.shape[0]):
+                    fetch[0] = 0.0
+                    t0_ = time.perf_counter()
+                    oracle.ffn_layer(fw_host, fetch_w, Wr, sample_x[t:t + 1], k, bias, threads=th)
+                    tt_ += time.perf_counter() - t0_ - fetch[0]
+                    done_ += 1
+                    if tt_ >= budget_s:
+                        break
+                return done_, tt_
+            done_t, secs_t = ffn_sample(args.cpu_budget_s / 4, threads)
+            done, secs = ffn_sample(args.cpu_budget_s, 1)
+            cpu_baseline = {"value": done_t / secs_t, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                            "host_cores": cores, "cpu_model": model,
+                            "sample": f"{done_t} whole token(s) of this workload (routed_down, router + top-{k}, "
+                                      f"routed_norm, routed_up and the shared experts on one thread, the {k} routed "
+                                      f"expert FFNs on {threads} threads), float64 C oracle, {secs_t:.1f} s",
+                            "single_thread": {"value": done / secs, "unit": "tok/s", "cores": 1,
+                                              "sample": f"{done} whole token(s), one thread, {secs:.1f} s"}}
         # the threaded oracle (expert FFNs of a token over all the cores), then
         # the plain one-thread loop on the same tokens
-        done_t, secs_t = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s / 4, Wr, bias, sample_x,
-                                       threads)
-        done, secs = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s, Wr, bias, sample_x)
-        cpu_baseline = {"value": done_t / secs_t, "unit": "tok/s", "cores": threads, "kind": "oracle",
-                        "host_cores": cores, "cpu_model": model,
-                        "sample": f"{done_t} whole token(s) of this workload (router + top-{k} on one thread, "
-                                  f"the {k} expert FFNs on {threads} threads, combine), float64 C oracle, "
-                                  f"{secs_t:.1f} s",
-                        "single_thread": {"value": done / secs, "unit": "tok/s", "cores": 1,
-                                          "sample": f"{done} whole token(s), one thread, {secs:.1f} s"}}
+        if not FFN:
+            done_t, secs_t = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s / 4, Wr, bias, sample_x,
+                                           threads)
+            done, secs = oracle_sample(cfg, args.seed, 0, weights_for, args.cpu_budget_s, Wr, bias, sample_x)
+            cpu_baseline = {"value": done_t / secs_t, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                            "host_cores": cores, "cpu_model": model,
+                            "sample": f"{done_t} whole token(s) of this workload (router + top-{k} on one thread, "
+                                      f"the {k} expert FFNs on {threads} threads, combine), float64 C oracle, "
+                                      f"{secs_t:.1f} s",
+                            "single_thread": {"value": done / secs, "unit": "tok/s", "cores": 1,
+                                              "sample": f"{done} whole token(s), one thread, {secs:.1f} s"}}
     del canon
     torch.cuda.empty_cache()
 
     stream = torch.cuda.Stream(dev)
 
-    def step(r, s):
+    def step(r, s, x=None):
+        x = xs[r] if x is None else x
         for li in range(NL):
-            moe.moe_route_forward(layer, xs[r], C, Wr_ds[li], bias_ds[li], packed[li], ids[r][li], wts[r][li],
-                                  ys[r], ws, s)
+            if FFN:
+                moe.moe_ffn_forward(ffn, x, C, Wr_ds[li], bias_ds[li], packed[li], fpacked, ids[r][li], wts[r][li],
+                                    outs[r], ffn_ws, s)
+            else:
+                moe.moe_route_forward(layer, x, C, Wr_ds[li], bias_ds[li], packed[li], ids[r][li], wts[r][li],
+                                      ys[r], ws, s)
 
     # distinct experts each rotating input selects, summed over the layers
     # (the bytes a step streams)
@@ -538,6 +598,10 @@ def main():
     with torch.cuda.stream(stream):
         for i in range(n_prof):
             r = i % ROTATE
+            if FFN:                          # the events bracket the routed kernels inside the layer
+                moe.moe_set_stage_events(layer, evs[i])
+                step(r, stream)
+                continue
             moe.moe_route(layer, xs[r], C, Wr_ds[0], bias_ds[0], ids[r][0], wts[r][0], ws, stream)
             moe.moe_set_stage_events(layer, evs[i])
             moe.moe_forward(layer, xs[r], C, ids[r][0], wts[r][0], packed[0], ys[r], ws, stream)
@@ -572,9 +636,10 @@ def main():
 
     # ---- end to end through the C ABI with host buffers
     n_e2e = min(args.steps, 2000)
+    Hin = FFN["hidden"] if FFN else H
     x_pin = [torch.from_numpy(xh.view(np.int16)).pin_memory() for xh in x_host]
-    y_pin = torch.empty((C, H), dtype=torch.float32).pin_memory()
-    x_stage = torch.empty((C, H), dtype=torch.int16, device=dev)
+    y_pin = torch.empty((C, Hin), dtype=torch.float32).pin_memory()
+    x_stage = torch.empty((C, Hin), dtype=torch.int16, device=dev)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -583,10 +648,8 @@ def main():
         for i in range(n_e2e):
             r = i % ROTATE
             x_stage.copy_(x_pin[r], non_blocking=True)
-            for li in range(NL):
-                moe.moe_route_forward(layer, x_stage, C, Wr_ds[li], bias_ds[li], packed[li], ids[r][li],
-                                      wts[r][li], ys[r], ws, stream)
-            y_pin.copy_(ys[r], non_blocking=True)
+            step(r, stream, x_stage)
+            y_pin.copy_(outs[r] if FFN else ys[r], non_blocking=True)
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
     if world > 1:
@@ -594,8 +657,9 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_s = float(tt.item())
     e2e = {"value": C * n_e2e * NL * world / e2e_s, "unit": "tok/s", "steps": n_e2e,
-           "h2d_bytes_per_step": C * H * 2, "d2h_bytes_per_step": C * H * 4,
-           "path": "pinned host x -> H2D -> moe_route_forward -> D2H y, per step, host-timed"}
+           "h2d_bytes_per_step": C * Hin * 2, "d2h_bytes_per_step": C * Hin * 4,
+           "path": ("pinned host u -> H2D -> moe_ffn_forward -> D2H out" if FFN else
+                    "pinned host x -> H2D -> moe_route_forward -> D2H y") + ", per step, host-timed"}
 
     flags = moe.moe_get_device_status(layer, ws, stream)
     if rank == 0:
@@ -615,6 +679,11 @@ def main():
             "windows_ms_per_step": [w_ / args.steps for w_ in windows],
             "window_spread": (max(windows) - min(windows)) / ms,
             "expert_hbm_gbs": hbm_gbs, "expert_hbm_frac": hbm_gbs / world / hbm_peak,
+            **({"ffn": {"weight_bytes_per_step": avg_distinct * expert_bytes + ffn_bytes,
+                        "ffn_matrix_bytes": ffn_bytes,
+                        "weight_hbm_gbs": (avg_distinct * expert_bytes + ffn_bytes) / (ms_per_step * 1e-3) / 1e9,
+                        "weight_hbm_frac": (avg_distinct * expert_bytes + ffn_bytes) / (ms_per_step * 1e-3) / 1e9
+                                           / hbm_peak}} if FFN else {}),
             "distinct_experts_per_step": avg_distinct,
             **({"routing": zipf_stats} if zipf_stats else {}),
             "roofline": roofline,
@@ -622,7 +691,9 @@ def main():
             # per layer call: C <= 8: fused router, gate/up, down, combine; C > 8: router
             # logits and top-k, then per pass of <= 512 tokens dispatch, x prep, x rows,
             # gate/up, h rows, down, combine
-            "gpu_launches": args.steps * NL * (4 if C <= 8 else 2 + 7 * ((C + 511) // 512)),
+            # FFN: + routed_down (2), routed_norm (1), routed_up (2) and 4 per shared expert
+            "gpu_launches": args.steps * NL * ((4 if C <= 8 else 2 + 7 * ((C + 511) // 512))
+                                               + (5 + 4 * FFN["shared"] if FFN else 0)),
             "clocks": clocks,
             "host_s": t_host,                 # host time of the three windows
             "device_flags": flags,

@@ -209,6 +209,63 @@ moe_status moe_route_noalloc(moe_layer_t layer, const uint16_t *x, int num_token
                              const float *w_router, const float *bias, int32_t *ids,
                              float *weights, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The FFN around the routed sum ("SparkInfer-K3", section "How the TP module
+ * works": FfnPartial = router -> routed_down -> the experts, FfnFinish =
+ * routed_norm -> routed_up -> shared experts; section "The model": hidden
+ * 7168, latent MoE at 3584, 2 shared experts).  For C <= 8 tokens u (bf16,
+ * [C][hidden]):
+ *   x   = routed_down u                      [latent][hidden]; x rounded to bf16
+ *   y_r = the routed layer on x (router, top-k, experts; moe_route_forward)
+ *   n   = routed_norm(y_r) = y_r / sqrt(mean(y_r^2) + eps) * gamma
+ *   out = routed_up n + sum over shared experts s of D_s (silu(G_s u) * (U_s u))
+ * with latent = the routed layer's hidden size.  The partial / finish split
+ * is where an expert-parallel caller sums the ranks' y_r (the reduce sits at
+ * the latent width because the RMS norm is not linear).  Every matrix is in
+ * the routed layer's format (NVFP4, or MXFP4 when the routed layer has
+ * MOE_CONFIG_MXFP4), packed by moe_ffn_pack_weights. */
+typedef struct moe_ffn *moe_ffn_t;
+
+typedef struct {
+  int32_t hidden;               /* the model width (7168 at the K3 shape); multiple of 64, <= 8192 */
+  int32_t shared_experts;       /* S >= 0 (2 at the K3 shape) */
+  int32_t shared_intermediate;  /* FFN width of a shared expert; multiple of 64, <= 4096 */
+  float eps;                    /* routed_norm epsilon (> 0) */
+  uint32_t flags;               /* must be 0 */
+} moe_ffn_config;
+
+typedef struct {
+  moe_fp4_tensor routed_down;   /* one matrix [latent][hidden]: codes [latent][hidden/2], ... scalars [1] */
+  moe_fp4_tensor routed_up;     /* one matrix [hidden][latent] */
+  moe_canonical_weights shared; /* S experts: gate/up [S][shared_intermediate][hidden], down [S][hidden][shared_intermediate] */
+  const float *norm_gamma;      /* device fp32 [latent] */
+} moe_ffn_weights;
+
+/* A host-side handle tied to `routed` (which must outlive it). */
+moe_status moe_ffn_create(const moe_ffn_config *cfg, moe_layer_t routed, moe_ffn_t *out);
+moe_status moe_ffn_destroy(moe_ffn_t ffn);
+/* Bytes of the packed buffer of the FFN's own weights (not the routed ones). */
+moe_status moe_ffn_packed_bytes(moe_ffn_t ffn, size_t *bytes);
+/* Workspace for C tokens (it contains the routed layer's workspace); zero-filled once. */
+moe_status moe_ffn_workspace_bytes(moe_ffn_t ffn, int num_tokens, size_t *bytes);
+/* Pack routed_down, routed_up, the shared experts and gamma (synchronises
+ * `stream`; MOE_ERR_INVALID_VALUE on a NaN scale byte). */
+moe_status moe_ffn_pack_weights(moe_ffn_t ffn, const moe_ffn_weights *w, void *packed, cudaStream_t stream);
+/* FfnPartial: x = routed_down u, then moe_route_forward on x: ids, weights
+ * ([C][k]) and y_routed (device fp32 [C][latent]) are written.  1 <= C <=
+ * min(8, the routed layer's max_tokens). */
+moe_status moe_ffn_partial(moe_ffn_t ffn, const uint16_t *u, int num_tokens, const float *w_router,
+                           const float *bias, const void *routed_packed, const void *ffn_packed, int32_t *ids,
+                           float *weights, float *y_routed, void *ws, size_t ws_bytes, cudaStream_t stream);
+/* FfnFinish: out (device fp32 [C][hidden]) = routed_up(routed_norm(y_routed))
+ * + the shared experts on u. */
+moe_status moe_ffn_finish(moe_ffn_t ffn, const uint16_t *u, int num_tokens, const float *y_routed,
+                          const void *ffn_packed, float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+/* Both phases (y_routed kept in the workspace). */
+moe_status moe_ffn_forward(moe_ffn_t ffn, const uint16_t *u, int num_tokens, const float *w_router,
+                           const float *bias, const void *routed_packed, const void *ffn_packed, int32_t *ids,
+                           float *weights, float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *moe_status_string(moe_status status);
 

@@ -275,6 +275,8 @@ def ffn_layer(ffn, routed, Wr, u_bf16, k, bias=None, threads=1, fmt="nvfp4", ids
       n   = routed_norm(y_r)         (RMS norm with gamma, eps)
       out = routed_up n + sum over the shared experts s of FFN_s(u)
 
+    routed: the experts' canonical dict, or a function mapping a sorted list
+    of expert ids to the dict of those experts.
     ffn: dict with 'routed_down' and 'routed_up' ({'codes','scales','g'}),
     'shared' (gate/up/down dicts over the shared experts, as the routed
     weights), 'gamma' float32 [latent], 'eps'.  Returns (ids, w, gap, x_bf16,
@@ -289,7 +291,13 @@ def ffn_layer(ffn, routed, Wr, u_bf16, k, bias=None, threads=1, fmt="nvfp4", ids
         ids, w, gap = route(router_logits(Wr, x_bf16, bias), k)
     else:
         (ids, w), gap = ids_w, None
-    y_r = moe_forward(routed, x_bf16, ids, w, threads=threads, fmt=fmt)
+    if callable(routed):                       # the experts' weights are fetched for the selected ones
+        sel = sorted(set(int(e) for e in np.asarray(ids).ravel()))
+        remap = {e: i for i, e in enumerate(sel)}
+        y_r = moe_forward(routed(sel), x_bf16, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads,
+                          fmt=fmt)
+    else:
+        y_r = moe_forward(routed, x_bf16, ids, w, threads=threads, fmt=fmt)
     n = rms_norm(y_r, ffn["gamma"], ffn["eps"])
     ru = ffn["routed_up"]
     out = dense_gemv(ru["codes"], ru["scales"], ru["g"], n, fmt)

@@ -108,4 +108,50 @@ cudaError_t launch_group_forward(GroupArgs a, int num_sms, int w_gu, int w_dn, s
                                  size_t dn_tile_bytes, size_t dn_region_off, cudaStream_t stream,
                                  cudaEvent_t after_gate_up);
 
+// ------------------------------------------------ around the routed sum (dense.cu)
+struct PackDenseArgs {
+  const uint8_t *codesA, *scalesA;   // mode 0: the matrix [M][K]; mode 1: the gate matrix [M][K]
+  const uint8_t *codesB, *scalesB;   // mode 1: the up matrix [M][K]
+  uint8_t *dst;                      // packed tiles of the destination matrix
+  int32_t *status;                   // set to 1 on a NaN scale byte
+  int M, K, mode, fmt;               // mode 0: pair rows (2p, 2p+1); mode 1: (gate p, up p)
+  int Wsrc;                          // 512-element K-slices of the source rows
+  int W;                             // slices of a destination tile (its stride)
+  int tile0, wd0;                    // first destination tile and slice
+};
+cudaError_t launch_pack_dense(const PackDenseArgs &a, int num_sms, cudaStream_t stream);
+
+struct DenseArgs {
+  const uint8_t *w;          // packed tiles of the matrix
+  const void *x;             // input vectors [C][K]: bf16 bits (xf32 = 0) or fp32
+  float *part;               // workspace: [tiles * W units][passes][32 lanes] float4
+  int xf32, C, K, W, tiles, fmt;
+  int w0, w1;                // slices of this launch (the B fragments of their K range fit shared memory)
+  size_t tile_bytes;
+};
+// A range of tiles of a dense GEMV and what its finisher writes:
+//   mode 0: plain pair rows (2p, 2p + 1) -> columns col0 + 2p, +1 (fp32
+//           written or added, or bf16); mode 1: SwiGLU of a (gate p, up p)
+//   pair -> column col0 + p (fp32).  p counts from the segment's first tile.
+constexpr int kMaxDenseSegs = 5;
+struct DenseSeg {
+  int tile0, tile1, mode, accumulate, out_ld, col0;
+  const float *ga, *gb;      // device tensor scales (null: 1)
+  float *out_f32;
+  uint16_t *out_bf16;
+};
+struct DenseFinishArgs {
+  const float *part;
+  const float *slice_scale;  // device [W] scale of each K-slice's partial, or null
+  DenseSeg seg[kMaxDenseSegs];
+  int nseg, xf32, C, W, tiles;
+};
+// Workspace bytes of a GEMV's partials and shared memory of its B fragments.
+inline size_t dense_partial_bytes(int tiles, int W, int C, bool xf32) {
+  return (size_t)tiles * W * (xf32 ? (C + 3) / 4 : 1) * 32 * 16;
+}
+cudaError_t launch_dense_gemv(const DenseArgs &a, const DenseFinishArgs &f, int num_sms, cudaStream_t stream);
+cudaError_t launch_rms_norm(const float *y, const float *gamma, float eps, int C, int n, float *out, int out_ld,
+                            cudaStream_t stream);
+
 }  // namespace moe

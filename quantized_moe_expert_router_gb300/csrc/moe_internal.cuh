@@ -28,6 +28,7 @@ constexpr int kGroupSmemBytes = 212992;  // dynamic shared memory of one grouped
 constexpr int kTileSliceBytes = 4608;    // one 512-element K-slice of a tile: 4096 code + 512 scale bytes
 constexpr int kTileSliceBytesMx = 4352;  // the same for MXFP4: 4096 code + 256 scale bytes (one per 32 elements)
 constexpr int kFmtNvfp4 = 0, kFmtMxfp4 = 1;
+constexpr int kDenseSmemBytes = 204800;  // B fragments of a dense GEMV: passes x K/16 k-steps x 256 bytes at most
 
 // Workspace control block (first 256 bytes of the workspace).
 struct WsControl {

@@ -32,7 +32,9 @@ CONFIG_MXFP4 = 0x1                      # MXFP4 weights (e8m0 scale per 32 eleme
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",
     "moe_pack_weights", "moe_route", "moe_forward", "moe_get_device_status",
-    "moe_set_stage_events", "moe_route_noalloc", "moe_route_forward", "moe_status_string",
+    "moe_set_stage_events", "moe_route_noalloc", "moe_route_forward",
+    "moe_ffn_create", "moe_ffn_destroy", "moe_ffn_packed_bytes", "moe_ffn_workspace_bytes",
+    "moe_ffn_pack_weights", "moe_ffn_partial", "moe_ffn_finish", "moe_ffn_forward", "moe_status_string",
 )
 
 
@@ -55,6 +57,16 @@ class moe_fp4_tensor(ctypes.Structure):
 
 class moe_canonical_weights(ctypes.Structure):
     _fields_ = [("gate", moe_fp4_tensor), ("up", moe_fp4_tensor), ("down", moe_fp4_tensor)]
+
+
+class moe_ffn_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("shared_experts", ctypes.c_int32),
+                ("shared_intermediate", ctypes.c_int32), ("eps", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class moe_ffn_weights(ctypes.Structure):
+    _fields_ = [("routed_down", moe_fp4_tensor), ("routed_up", moe_fp4_tensor),
+                ("shared", moe_canonical_weights), ("norm_gamma", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -82,6 +94,14 @@ def load_library(path: str = LIB_PATH):
             lib.moe_set_stage_events.argtypes = [P, P, I32]
             lib.moe_route_noalloc.argtypes = [P, P, I32, P, P, P, P, P]
             lib.moe_route_forward.argtypes = [P, P, I32, P, P, P, P, P, P, P, SZ, P]
+            lib.moe_ffn_create.argtypes = [ctypes.POINTER(moe_ffn_config), P, ctypes.POINTER(P)]
+            lib.moe_ffn_destroy.argtypes = [P]
+            lib.moe_ffn_packed_bytes.argtypes = [P, ctypes.POINTER(SZ)]
+            lib.moe_ffn_workspace_bytes.argtypes = [P, I32, ctypes.POINTER(SZ)]
+            lib.moe_ffn_pack_weights.argtypes = [P, ctypes.POINTER(moe_ffn_weights), P, P]
+            lib.moe_ffn_partial.argtypes = [P, P, I32, P, P, P, P, P, P, P, P, SZ, P]
+            lib.moe_ffn_finish.argtypes = [P, P, I32, P, P, P, P, SZ, P]
+            lib.moe_ffn_forward.argtypes = [P, P, I32, P, P, P, P, P, P, P, P, SZ, P]
             lib.moe_status_string.argtypes = [I32]
             lib.moe_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -220,3 +240,81 @@ def alloc_workspace(layer: Layer, num_tokens: int, device=None) -> torch.Tensor:
 
 def alloc_packed(layer: Layer, device=None) -> torch.Tensor:
     return torch.empty(moe_packed_bytes(layer), dtype=torch.uint8, device=device or f"cuda:{layer.device}")
+
+
+# ------------------------------------------------ the FFN around the routed sum
+
+class Ffn:
+    """Owns one ``moe_ffn_t`` handle tied to a routed ``Layer`` (host memory only)."""
+
+    def __init__(self, routed: Layer, hidden, shared_experts, shared_intermediate, eps=1e-6):
+        lib = load_library()
+        self.routed = routed
+        self.cfg = moe_ffn_config(hidden, shared_experts, shared_intermediate, eps, 0)
+        h = ctypes.c_void_p()
+        _check("moe_ffn_create", lib.moe_ffn_create(ctypes.byref(self.cfg), routed.handle, ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.moe_ffn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+
+def moe_ffn_packed_bytes(ffn: Ffn) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_ffn_packed_bytes", load_library().moe_ffn_packed_bytes(ffn.handle, ctypes.byref(n)))
+    return n.value
+
+
+def moe_ffn_workspace_bytes(ffn: Ffn, num_tokens: int) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_ffn_workspace_bytes", load_library().moe_ffn_workspace_bytes(ffn.handle, num_tokens, ctypes.byref(n)))
+    return n.value
+
+
+def _fp4_1(m):
+    return moe_fp4_tensor(_ptr(m["codes"]), _ptr(m["scales"]), _ptr(m["g"]), _ptr(m["a"]))
+
+
+def moe_ffn_pack_weights(ffn: Ffn, w: dict, packed: torch.Tensor, stream=None) -> None:
+    """w: {'routed_down', 'routed_up': {'codes','scales','g','a'} (g, a: one-element tensors),
+    'shared': {'gate'|'up'|'down': ...}, 'gamma'} device tensors."""
+    sh = w["shared"]
+    cw = moe_ffn_weights(_fp4_1(w["routed_down"]), _fp4_1(w["routed_up"]),
+                         moe_canonical_weights(_fp4(sh["gate"]), _fp4(sh["up"]), _fp4(sh["down"])),
+                         _ptr(w["gamma"]))
+    _check("moe_ffn_pack_weights", load_library().moe_ffn_pack_weights(
+        ffn.handle, ctypes.byref(cw), _ptr(packed), _stream(stream)))
+
+
+def moe_ffn_partial(ffn, u, num_tokens, w_router, bias, routed_packed, ffn_packed, ids, weights, y_routed, ws,
+                    stream=None) -> None:
+    _check("moe_ffn_partial", load_library().moe_ffn_partial(
+        ffn.handle, _ptr(u), num_tokens, _ptr(w_router), _ptr(bias), _ptr(routed_packed), _ptr(ffn_packed),
+        _ptr(ids), _ptr(weights), _ptr(y_routed), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_ffn_finish(ffn, u, num_tokens, y_routed, ffn_packed, out, ws, stream=None) -> None:
+    _check("moe_ffn_finish", load_library().moe_ffn_finish(
+        ffn.handle, _ptr(u), num_tokens, _ptr(y_routed), _ptr(ffn_packed), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_ffn_forward(ffn, u, num_tokens, w_router, bias, routed_packed, ffn_packed, ids, weights, out, ws,
+                    stream=None) -> None:
+    _check("moe_ffn_forward", load_library().moe_ffn_forward(
+        ffn.handle, _ptr(u), num_tokens, _ptr(w_router), _ptr(bias), _ptr(routed_packed), _ptr(ffn_packed),
+        _ptr(ids), _ptr(weights), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def alloc_ffn_workspace(ffn: Ffn, num_tokens: int, device=None) -> torch.Tensor:
+    n = moe_ffn_workspace_bytes(ffn, num_tokens)
+    return torch.zeros(n, dtype=torch.uint8, device=device or f"cuda:{ffn.routed.device}")
+
+
+def alloc_ffn_packed(ffn: Ffn, device=None) -> torch.Tensor:
+    return torch.empty(moe_ffn_packed_bytes(ffn), dtype=torch.uint8, device=device or f"cuda:{ffn.routed.device}")

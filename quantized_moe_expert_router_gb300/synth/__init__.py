@@ -276,7 +276,10 @@ def ffn_weights(seed: int, layer: int, hidden: int, latent: int, shared: int, sh
     for m, name, rows, K in ((0, "gate", shared_inter, hidden), (1, "up", shared_inter, hidden),
                              (2, "down", hidden, shared_inter)):
         ms = [mat(FFN_SHARED, 3 * s + m, rows, K) for s in range(shared)]
-        sh[name] = {f: np.stack([q[f] for q in ms]) for f in ("codes", "scales", "g", "a")}
+        blk = 32 if fmt == "mxfp4" else 16
+        empty = {"codes": np.zeros((0, rows, K // 2), np.uint8), "scales": np.zeros((0, rows, K // blk), np.uint8),
+                 "g": np.zeros(0, np.float32), "a": np.zeros(0, np.float32)}
+        sh[name] = {f: np.stack([q[f] for q in ms]) if ms else empty[f] for f in ("codes", "scales", "g", "a")}
     out["shared"] = sh
     z = normals(key(seed, KIND_FFN, layer, FFN_GAMMA, 0), latent)
     out["gamma"] = (1.0 + 0.1 * z).astype(np.float32)

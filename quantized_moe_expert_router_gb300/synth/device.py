@@ -13,7 +13,8 @@ import threading
 import numpy as np
 import torch
 
-from . import (MAT_DOWN, MAT_GATE, MAT_UP, W_COEF, global_scales, weight_key)
+from . import (FFN_GAMMA, FFN_ROUTED_DOWN, FFN_ROUTED_UP, FFN_SHARED, KIND_FFN, MAT_DOWN, MAT_GATE, MAT_UP, W_ABS_MAX,
+               W_COEF, _E4M3_MAX, global_scales, key, normals, weight_key)
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                          "_lib", "libmoe_synth.so")
@@ -86,3 +87,39 @@ def gather_to_host(canon_dev: dict, experts) -> dict:
 def free(canon_dev: dict) -> None:
     for m in canon_dev.values():
         m.clear()
+
+
+def ffn_weights_device(seed: int, layer: int, hidden: int, latent: int, shared: int, shared_inter: int,
+                       device="cuda:0", stream=None, eps: float = 1e-6) -> dict:
+    """The NVFP4 weights around the routed sum on the device, bit-identical to
+    ``ffn_weights`` of the host generator (same keys, same global scales,
+    same encoder): routed_down / routed_up {'codes','scales','g','a'} (g, a
+    one-element tensors), 'shared' in the routed experts' dict form,
+    'gamma', 'eps'."""
+    lib = _load()
+    stream = stream or torch.cuda.current_stream(device)
+
+    def mat(part, idx, rows, K):
+        k = torch.tensor([np.uint64(key(seed, KIND_FFN, layer, part, idx)).view(np.int64)], device=device)
+        g = np.float32(W_ABS_MAX / (6.0 * _E4M3_MAX) * (1.0 + 0.25 * (idx % 3)))
+        g_d = torch.tensor([g], dtype=torch.float32, device=device)
+        codes = torch.empty((1, rows, K // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty((1, rows, K // 16), dtype=torch.uint8, device=device)
+        rc = lib.synth_generate_matrices(k.data_ptr(), g_d.data_ptr(), 1, rows, K, W_COEF, codes.data_ptr(),
+                                         scales.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"synth_generate_matrices failed with cudaError {rc}")
+        return {"codes": codes[0], "scales": scales[0], "g": g_d,
+                "a": torch.ones(1, dtype=torch.float32, device=device)}
+    out = {"routed_down": mat(FFN_ROUTED_DOWN, 0, latent, hidden), "routed_up": mat(FFN_ROUTED_UP, 0, hidden, latent)}
+    sh = {}
+    for m, name, rows, K in ((0, "gate", shared_inter, hidden), (1, "up", shared_inter, hidden),
+                             (2, "down", hidden, shared_inter)):
+        ms = [mat(FFN_SHARED, 3 * s + m, rows, K) for s in range(shared)]
+        sh[name] = {"codes": torch.stack([q["codes"] for q in ms]), "scales": torch.stack([q["scales"] for q in ms]),
+                    "g": torch.cat([q["g"] for q in ms]), "a": torch.cat([q["a"] for q in ms])}
+    out["shared"] = sh
+    z = normals(key(seed, KIND_FFN, layer, FFN_GAMMA, 0), latent)
+    out["gamma"] = torch.from_numpy((1.0 + 0.1 * z).astype(np.float32)).to(device)
+    out["eps"] = eps
+    return out
