@@ -52,6 +52,12 @@ CONFIGS = {
                     workload="K3-shape MoE layer, decode batch 7, top-16 of 896, NVFP4, uniform routing"),
     "k3c7k8": dict(E=896, k=8, H=3584, I=3072, C=7, layers=1, zipf=False,
                    workload="K3-shape MoE layer, decode batch 7, top-8 of 896, NVFP4, uniform routing"),
+    "k3c16": dict(E=896, k=16, H=3584, I=3072, C=16, layers=1, zipf=False,
+                  workload="K3-shape MoE layer, batch of 16 tokens, top-16 of 896, NVFP4, uniform routing "
+                           "(decode kernels in groups of 8, below the grouped path's crossover)"),
+    "k3c64": dict(E=896, k=16, H=3584, I=3072, C=64, layers=1, zipf=False,
+                  workload="K3-shape MoE layer, batch of 64 tokens, top-16 of 896, NVFP4, uniform routing "
+                           "(grouped tcgen05 path)"),
     "k3x8zipf": dict(E=896, k=16, H=3584, I=3072, C=1, layers=8, zipf=True,
                      workload="8 K3-shape MoE layers (133 GB resident), decode batch 1, top-16 of 896, NVFP4, "
                               "Zipf-biased routing (s = 1.1, per-layer permutation)"),
@@ -615,7 +621,7 @@ def main():
     dn_avg = float(np.mean(dn_ms))
     hbm_peak, peak_src = measured_peaks()
     achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
-    if C > 8:
+    if C >= 28:
         # grouped path: the stage events bracket dispatch, x-row prep and the gate/up GEMM
         traffic_per_expert, traffic_src = ncu_traffic("grouped.cu", f"group_tc_gu_{args.config}")
         kernel_label = ("group_tc_kernel<0> (grouped gate/up + SwiGLU on tcgen05; the timed span also holds "
@@ -688,12 +694,14 @@ def main():
             **({"routing": zipf_stats} if zipf_stats else {}),
             "roofline": roofline,
             "e2e": e2e,
-            # per layer call: C <= 8: fused router, gate/up, down, combine; C > 8: router
-            # logits and top-k, then per pass of <= 512 tokens dispatch, x prep, x rows,
-            # gate/up, h rows, down, combine
             # FFN: + routed_down (2), routed_norm (1), routed_up (2) and 4 per shared expert
-            "gpu_launches": args.steps * NL * ((4 if C <= 8 else 2 + 7 * ((C + 511) // 512))
-                                               + (5 + 4 * FFN["shared"] if FFN else 0)),
+            # routed layer per call: C <= 8: fused router, gate/up, down, combine;
+            # 9 .. 27 tokens: tiled router + top-k, then 3 decode kernels per group
+            # of 8; 28 or more: router, then 7 grouped kernels per pass of 512
+            "gpu_launches": args.steps * NL * ((4 if C <= 8 else 2 + 3 * ((C + 7) // 8) if C < 28
+                                                else 2 + 7 * ((C + 511) // 512))
+                                               # FFN: GEMV A (2), norm (1), GEMV B (2; 3 for C > 4)
+                                               + ((5 if C <= 4 else 6) if FFN else 0)),
             "clocks": clocks,
             "host_s": t_host,                 # host time of the three windows
             "device_flags": flags,

@@ -79,13 +79,21 @@ typedef enum {
  * expert read once per group); the tcgen05 grouped path is NVFP4 only. */
 #define MOE_CONFIG_MXFP4 0x1u
 
+/* moe_config.flags: take the grouped tcgen05 path for every call of more
+ * than 8 tokens.  By default calls of 9 .. 27 tokens run on the decode
+ * kernels in groups of 8, which are faster there (with uniform routing over
+ * 896 experts each expert has one or two tokens, so the grouped GEMM's MMAs
+ * are mostly padding); 28 tokens or more take the grouped path.  NVFP4
+ * layers only. */
+#define MOE_CONFIG_GROUPED_ABOVE_8 0x2u
+
 typedef struct {
   int32_t num_experts;   /* E, 1 .. 1024 */
   int32_t top_k;         /* k, 1 .. min(32, E) */
   int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 4096 */
   int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 4096 */
   int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
-  uint32_t flags;        /* 0, MOE_CONFIG_MXFP4, or the test hook MOE_CONFIG_TEST_ROUTER_STALL */
+  uint32_t flags;        /* MOE_CONFIG_MXFP4, MOE_CONFIG_GROUPED_ABOVE_8, the test hook MOE_CONFIG_TEST_ROUTER_STALL, or 0 */
 } moe_config;
 
 typedef struct {

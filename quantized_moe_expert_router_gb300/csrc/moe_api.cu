@@ -60,7 +60,8 @@ const char *moe_status_string(moe_status s) {
 moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out) {
   if (!cfg || !out) return MOE_ERR_INVALID_ARG;
   const moe_config c = *cfg;
-  if ((c.flags & ~(uint32_t)(MOE_CONFIG_TEST_ROUTER_STALL | MOE_CONFIG_MXFP4)) != 0 || c.max_tokens < 1)
+  if ((c.flags & ~(uint32_t)(MOE_CONFIG_TEST_ROUTER_STALL | MOE_CONFIG_MXFP4 | MOE_CONFIG_GROUPED_ABOVE_8)) != 0 ||
+      c.max_tokens < 1)
     return MOE_ERR_INVALID_ARG;
   if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.top_k < 1 || c.top_k > moe::kMaxTopK || c.top_k > c.num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -92,6 +93,11 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   L->trailer_off = align_up(L->scalars_off + (size_t)c.num_experts * 6 * sizeof(float), 16);
   L->packed_bytes = L->trailer_off + 16;
   L->stage_events_on = 0;
+  // below the crossover the decode kernels (groups of 8 tokens, each expert
+  // read once per group) beat the grouped GEMM, whose MMAs are mostly padding
+  // when an expert has one or two tokens: measured with uniform routing at
+  // 896 experts, top-16, the two paths meet between 24 and 32 tokens
+  L->grouped_min_tokens = (c.flags & MOE_CONFIG_GROUPED_ABOVE_8) ? moe::kGemvTokens + 1 : moe::kGroupedMinTokens;
   if (moe::gemv_setup() != cudaSuccess) {
     delete L;
     return MOE_ERR_CUDA;
@@ -228,7 +234,7 @@ moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
   // C > 8: the grouped tcgen05 path (NVFP4); MXFP4 layers run every C on the
   // decode kernels, in groups of 8 tokens
-  if (C > moe::kGemvTokens && L->fmt == moe::kFmtNvfp4) {
+  if (C >= L->grouped_min_tokens && L->fmt == moe::kFmtNvfp4) {
     // expert-major passes of up to kGroupTokens tokens
     moe::GroupArgs g = {};
     g.packed = pk;

@@ -18,7 +18,8 @@ namespace moe {
 constexpr int kMaxExperts = 1024;        // dispatch bitmap: 32 words of 32 bits
 constexpr int kMaxTopK = 32;             // one top-k slot per lane
 constexpr int kGemvTokens = 8;           // tokens per GEMV group (token mask bits)
-constexpr int kGroupTokens = 512;        // tokens per pass of the grouped (expert-major) path, C > 8
+constexpr int kGroupTokens = 512;        // tokens per pass of the grouped (expert-major) path
+constexpr int kGroupedMinTokens = 28;    // calls of this many tokens or more take the grouped path (measured crossover)
 constexpr int kMaxPairs = kGemvTokens * kMaxTopK;   // (token, slot) pairs per group
 constexpr int kKAlign = 512;             // packed K is padded to this (32 lanes x 16)
 constexpr int kRouteFusedTokens = 8;     // route: fused top-k in the last CTA up to this C
@@ -81,6 +82,7 @@ struct moe_layer {
   size_t packed_bytes;
   cudaEvent_t stage_events[3];
   int stage_events_on;
+  int grouped_min_tokens;     // calls of at least this many tokens take the grouped (tcgen05) path
 };
 
 namespace moe {

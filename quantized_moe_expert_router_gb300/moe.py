@@ -28,6 +28,7 @@ FLAG_DUPLICATE_ID = 0x2
 FLAG_TIMEOUT = 0x4
 CONFIG_TEST_ROUTER_STALL = 0x80000000   # test hook: the router's bounded wait runs out
 CONFIG_MXFP4 = 0x1                      # MXFP4 weights (e8m0 scale per 32 elements)
+CONFIG_GROUPED_ABOVE_8 = 0x2            # the grouped tcgen05 path for every call of more than 8 tokens
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",

@@ -29,10 +29,11 @@ def to_device(canon_h):
 
 class GpuLayer:
     def __init__(self, E, k, H, I, max_tokens, seed=0, layer=0, device_gen=False, router_std=1.0,
-                 zipf=False, fmt="nvfp4"):
+                 zipf=False, fmt="nvfp4", grouped=False):
         self.E, self.k, self.H, self.I = E, k, H, I
         self.seed, self.layer_id, self.fmt = seed, layer, fmt
-        self.h = moe.Layer(E, k, H, I, max_tokens, flags=moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0)
+        flags = (moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0) | (moe.CONFIG_GROUPED_ABOVE_8 if grouped else 0)
+        self.h = moe.Layer(E, k, H, I, max_tokens, flags=flags)
         if device_gen:
             self.canon = synth_dev.canonical_layer_device(seed, layer, E, H, I, DEV, fmt=fmt)
         else:
@@ -204,8 +205,9 @@ def test_odd_shapes_parity(E, k, H, I, C):
 @pytest.mark.parametrize("E,k,H,I,C", [(32, 4, 256, 192, 40), (12, 3, 64, 128, 20), (40, 8, 576, 320, 64),
                                        (7, 7, 192, 1088, 9), (8, 1, 4096, 4096, 9), (16, 2, 64, 4096, 12)])
 def test_grouped_path_parity(E, k, H, I, C):
-    # C > 8 runs expert-major: every expert's weights once for all its tokens
-    L = GpuLayer(E, k, H, I, C, seed=6)
+    # the grouped path for every C > 8 (the layer flag): expert-major, every
+    # expert's weights once for all its tokens
+    L = GpuLayer(E, k, H, I, C, seed=6, grouped=True)
     x = gapped_tokens(6, 0, C, H, L.Wr, k)
     check_layer(L, x, f"grouped E{E} k{k} H{H} I{I} C{C}")
 
@@ -215,16 +217,26 @@ def test_grouped_path_multi_pass_parity(C):
     # more than 512 tokens: passes of 512 (and a ragged last one); ~65 pairs
     # per expert, so the grouped GEMMs split experts into several column
     # chunks (64 pairs for gate/up, 32 for down)
-    L = GpuLayer(32, 4, 256, 192, C, seed=9)
+    L = GpuLayer(32, 4, 256, 192, C, seed=9, grouped=True)
     x = gapped_tokens(9, 0, C, 256, L.Wr, 4)
     check_layer(L, x, f"grouped multi-pass C={C}")
 
 
-@pytest.mark.parametrize("C", [1, 3, 8, 11])
-def test_route_forward_equals_route_then_forward(C):
+@pytest.mark.parametrize("C", [9, 16, 27, 28])
+def test_default_path_switch_parity(C):
+    # without the flag, 9 .. 27 tokens run the decode kernels in groups of 8
+    # and 28 or more the grouped path: both sides of the switch against the
+    # oracle
+    L = GpuLayer(40, 8, 576, 320, C, seed=10)
+    x = gapped_tokens(10, 0, C, 576, L.Wr, 8)
+    check_layer(L, x, f"default path C={C}")
+
+
+@pytest.mark.parametrize("C,grouped", [(1, False), (3, False), (8, False), (11, False), (11, True)])
+def test_route_forward_equals_route_then_forward(C, grouped):
     # the one-call layer gives the separate calls' results bit for bit, call
     # after call
-    L = GpuLayer(32, 4, 256, 192, 16)
+    L = GpuLayer(32, 4, 256, 192, 16, grouped=grouped)
     for rep in range(3):
         x = gapped_tokens(rep, 0, C, 256, L.Wr, 4)
         ids, w, y = L.run(x)
@@ -268,14 +280,15 @@ def test_band_and_slice_partials_sum_to_the_layer(C):
     ids, w, _ = oracle.route(oracle.router_logits(Wr, x), k)
     y_o = oracle.moe_forward(canon, x, ids, w)
     total = np.zeros_like(y_o)
+    gf = moe.CONFIG_GROUPED_ABOVE_8
     for lo, hi in partition.expert_bands(E, 2):
-        total += _forward(moe.Layer(hi - lo, k, H, I, max(C, 8)), x, partition.band_ids(ids, lo, hi), w,
+        total += _forward(moe.Layer(hi - lo, k, H, I, max(C, 8), flags=gf), x, partition.band_ids(ids, lo, hi), w,
                           partition.band_weights(canon, lo, hi), ws_tokens=max(C, 8))
     assert_close(total, y_o, "expert bands")
     total = np.zeros_like(y_o)
     for i0, i1 in partition.intermediate_slices(I, 2):
-        total += _forward(moe.Layer(E, k, H, i1 - i0, max(C, 8)), x, ids, w, partition.slice_weights(canon, i0, i1),
-                          ws_tokens=max(C, 8))
+        total += _forward(moe.Layer(E, k, H, i1 - i0, max(C, 8), flags=gf), x, ids, w,
+                          partition.slice_weights(canon, i0, i1), ws_tokens=max(C, 8))
     assert_close(total, y_o, "intermediate slices")
 
 
@@ -376,7 +389,7 @@ def test_grouped_bad_duplicate_and_absent_ids():
     # and skipped, negative ids are absent slots, a token with no slot left
     # gets a zero output
     C, k = 12, 4
-    L = GpuLayer(32, k, 256, 192, C, seed=4)
+    L = GpuLayer(32, k, 256, 192, C, seed=4, grouped=True)
     x_bits = gapped_tokens(4, 0, C, 256, L.Wr, k)
     ids_h, w_h, _ = oracle.route(oracle.router_logits(L.Wr, x_bits), k)
     ids_h = ids_h.astype(np.int32).copy()
