@@ -90,6 +90,13 @@ def _load():
             lib.oracle_moe_forward.restype = i32
             lib.oracle_moe_forward_mt.argtypes = [i32] * 6 + [P, P, P] * 3 + [P, P, P, P]
             lib.oracle_moe_forward_mt.restype = i32
+            lib.oracle_quantize_nvfp4.argtypes = [i32, P, ctypes.c_float, P, P]
+            lib.oracle_quantize_nvfp4.restype = i32
+            lib.oracle_expert_ffn_w4a4.argtypes = ([i32, i32] + [P, P, ctypes.c_float] * 3 +
+                                                   [ctypes.c_float, ctypes.c_float, P, P, P])
+            lib.oracle_expert_ffn_w4a4.restype = i32
+            lib.oracle_moe_forward_w4a4_mt.argtypes = [i32] * 6 + [P, P, P] * 4 + [P, P, P, P, P]
+            lib.oracle_moe_forward_w4a4_mt.restype = i32
             _lib = lib
     return _lib
 
@@ -217,6 +224,82 @@ def moe_forward(weights, x_bf16, ids, w, threads=1, fmt=None):
     if rc != OK:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return y
+
+
+def quantize_nvfp4_act(v, a):
+    """NVFP4 quantization of activations with the static input scale a, in
+    fp32 as the GPU does it (oracle_quantize_nvfp4): v float32 [..., n] (n a
+    multiple of 16) -> (codes uint8 [..., n/2], scales uint8 [..., n/16])."""
+    v = _c(v, np.float32)
+    n = v.shape[-1]
+    rows = v.reshape(-1, n)
+    codes = np.empty((rows.shape[0], n // 2), np.uint8)
+    scales = np.empty((rows.shape[0], n // 16), np.uint8)
+    for i in range(rows.shape[0]):
+        r = np.ascontiguousarray(rows[i])
+        c, s = codes[i], scales[i]
+        rc = _load().oracle_quantize_nvfp4(n, _ptr(r), float(a), _ptr(c), _ptr(s))
+        if rc != OK:
+            raise ValueError(f"oracle_quantize_nvfp4 failed ({rc})")
+    return codes.reshape(v.shape[:-1] + (n // 2,)), scales.reshape(v.shape[:-1] + (n // 16,))
+
+
+def dequant_nvfp4_act(codes, scales, a):
+    """Values of quantized activations: e2m1(code) * e4m3(scale) * a (float64)."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    n = codes.shape[-1] * 2
+    nib = np.stack([codes & 0x0F, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (n,))
+    e2 = np.array([e2m1_value(i) for i in range(16)])[nib]
+    e4 = np.array([e4m3_value(i) for i in range(256)])[scales]
+    return e2 * np.repeat(e4, 16, axis=-1) * float(np.float32(a))
+
+
+def expert_ffn_w4a4(H, I, gate, up, down, a_in, a_dn, x, return_act=False):
+    """One expert with W4A4 numerics (oracle_expert_ffn_w4a4): gate/up/down =
+    (codes, scales, g); x float64 [H] (bf16 values) -> y float64 [H] (and the
+    float64 activation [I] when return_act)."""
+    x = _c(x, np.float64)
+    y = np.empty((H,), np.float64)
+    act = np.empty((I,), np.float64)
+    keep, args = [], []
+    for m in (gate, up, down):
+        c, s = _c(m[0], np.uint8), _c(m[1], np.uint8)
+        keep.append((c, s))
+        args += [_ptr(c), _ptr(s), float(m[2])]
+    rc = _load().oracle_expert_ffn_w4a4(H, I, *args, float(a_in), float(a_dn), _ptr(x), _ptr(y), _ptr(act))
+    if rc != OK:
+        raise ValueError(f"oracle_expert_ffn_w4a4 failed ({rc})")
+    return (y, act) if return_act else y
+
+
+def moe_forward_w4a4(weights, x_bf16, ids, w, threads=1, return_act=False):
+    """Routed MoE output with W4A4 numerics (oracle_moe_forward_w4a4_mt):
+    weights as for moe_forward (NVFP4) plus each matrix's input scales 'a'
+    [E]; x is quantized per (token, expert) with max(gate a, up a), the
+    activation h with the down matrix's a.  Returns y float64 [C][H] (and the
+    float64 activations [C][k][I] when return_act)."""
+    gate, up, down = weights["gate"], weights["up"], weights["down"]
+    E, I, Hh = gate["codes"].shape
+    H = Hh * 2
+    x = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    C, k = ids.shape
+    keep, args, scl = [], [], []
+    for m in (gate, up, down):
+        c, s, g = _c(m["codes"], np.uint8), _c(m["scales"], np.uint8), _c(m["g"], np.float32)
+        a = _c(m["a"], np.float32)
+        keep.append((c, s, g, a))
+        args += [_ptr(c), _ptr(s), _ptr(g)]
+        scl.append(_ptr(a))
+    y = np.empty((C, H), np.float64)
+    act = np.zeros((C, k, I), np.float64)
+    rc = _load().oracle_moe_forward_w4a4_mt(int(max(1, threads)), C, E, k, H, I, *args, *scl, _ptr(x), _ptr(ids),
+                                            _ptr(w), _ptr(y), _ptr(act))
+    if rc != OK:
+        raise ValueError(f"oracle_moe_forward_w4a4 failed ({rc})")
+    return (y, act) if return_act else y
 
 
 def full_layer(weights, Wr, x_bf16, k, bias=None, fmt="nvfp4"):

@@ -330,7 +330,16 @@ int oracle_expert_ffn(int H, int I,
                                down_codes, down_scales, down_g, x, y);
 }
 
-/* Everything one token needs: the arguments of oracle_moe_forward. */
+int oracle_expert_ffn_w4a4(int H, int I,
+                           const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
+                           const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
+                           const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
+                           float a_in, float a_dn, const double *x, double *y, double *act_out);
+
+/* Everything one token needs: the arguments of oracle_moe_forward.  With
+ * down_a set the experts run with W4A4 numerics (oracle_expert_ffn_w4a4):
+ * x is quantized with max(gate_a[e], up_a[e]) and h with down_a[e]; act, when
+ * set, receives every pair's float64 activation [C * k][I]. */
 typedef struct {
   int fmt;
   int C, E, k, H, I;
@@ -344,23 +353,37 @@ typedef struct {
   const int32_t *ids;
   const double *w;
   double *y;
+  const float *gate_a, *up_a, *down_a;
+  double *act;
 } forward_args;
+
+/* The FFN of expert e on x, in the numerics the arguments select; pair is
+ * the (token, slot) index that names the act row. */
+static int run_expert(const forward_args *a, int e, int64_t pair, const double *x, double *y) {
+  const int H = a->H, I = a->I, B = fmt_block(a->fmt);
+  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / B;
+  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / B;
+  if (a->down_a) {
+    const float ain = a->gate_a[e] > a->up_a[e] ? a->gate_a[e] : a->up_a[e];
+    return oracle_expert_ffn_w4a4(H, I, a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
+                                  a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
+                                  a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
+                                  ain, a->down_a[e], x, y, a->act ? a->act + pair * I : NULL);
+  }
+  return oracle_expert_ffn_fmt(a->fmt, H, I, a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales,
+                               a->gate_g[e], a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
+                               a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e], x, y);
+}
 
 /* y[t] of one token, with the scratch vectors xt[H] and ye[H]. */
 static int forward_token(const forward_args *a, int t, double *xt, double *ye) {
-  const int H = a->H, I = a->I, k = a->k, B = fmt_block(a->fmt);
-  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / B;
-  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / B;
+  const int H = a->H, k = a->k;
   for (int j = 0; j < H; j++) xt[j] = oracle_bf16_value(a->x[(int64_t)t * H + j]);
   for (int j = 0; j < H; j++) a->y[(int64_t)t * H + j] = 0.0;
   for (int i = 0; i < k; i++) {
     int e = a->ids[(int64_t)t * k + i];
     if (e < 0 || e >= a->E) return ORACLE_ERR_BAD_ID;
-    int rc = oracle_expert_ffn_fmt(a->fmt, H, I,
-                               a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
-                               a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
-                               a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
-                               xt, ye);
+    int rc = run_expert(a, e, (int64_t)t * k + i, xt, ye);
     if (rc != ORACLE_OK) return rc;
     double wi = a->w[(int64_t)t * k + i];
     for (int j = 0; j < H; j++) a->y[(int64_t)t * H + j] += wi * ye[j];
@@ -390,7 +413,7 @@ int oracle_moe_forward_fmt(int fmt, int C, int E, int k, int H, int I,
                            const uint16_t *x, const int32_t *ids, const double *w,
                            double *y) {
   forward_args a = {fmt, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
-                    down_codes, down_scales, down_g, x, ids, w, y};
+                    down_codes, down_scales, down_g, x, ids, w, y, NULL, NULL, NULL, NULL};
   if (!forward_args_ok(&a)) return ORACLE_ERR_ARG;
   double *xt = (double *)malloc(sizeof(double) * (size_t)H);
   double *ye = (double *)malloc(sizeof(double) * (size_t)H);
@@ -434,9 +457,7 @@ typedef struct {
 static void *forward_worker(void *p) {
   forward_job *j = (forward_job *)p;
   const forward_args *a = j->a;
-  const int H = a->H, I = a->I, k = a->k, B = fmt_block(a->fmt);
-  const int64_t gu_codes = (int64_t)I * H / 2, gu_scales = (int64_t)I * H / B;
-  const int64_t dn_codes = (int64_t)H * I / 2, dn_scales = (int64_t)H * I / B;
+  const int H = a->H, k = a->k;
   double *xt = (double *)malloc(sizeof(double) * (size_t)H);
   j->rc = xt ? ORACLE_OK : ORACLE_ERR_ARG;
   for (int64_t pr = j->first; pr < (int64_t)a->C * k && j->rc == ORACLE_OK; pr += j->step) {
@@ -447,15 +468,13 @@ static void *forward_worker(void *p) {
       break;
     }
     for (int q = 0; q < H; q++) xt[q] = oracle_bf16_value(a->x[t * H + q]);
-    j->rc = oracle_expert_ffn_fmt(a->fmt, H, I,
-                              a->gate_codes + e * gu_codes, a->gate_scales + e * gu_scales, a->gate_g[e],
-                              a->up_codes + e * gu_codes, a->up_scales + e * gu_scales, a->up_g[e],
-                              a->down_codes + e * dn_codes, a->down_scales + e * dn_scales, a->down_g[e],
-                              xt, j->ye_all + pr * H);
+    j->rc = run_expert(a, e, pr, xt, j->ye_all + pr * H);
   }
   free(xt);
   return NULL;
 }
+
+static int forward_mt(forward_args a, int nthreads);
 
 int oracle_moe_forward_mt_fmt(int fmt, int nthreads, int C, int E, int k, int H, int I,
                               const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
@@ -464,7 +483,31 @@ int oracle_moe_forward_mt_fmt(int fmt, int nthreads, int C, int E, int k, int H,
                               const uint16_t *x, const int32_t *ids, const double *w,
                               double *y) {
   forward_args a = {fmt, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
-                    down_codes, down_scales, down_g, x, ids, w, y};
+                    down_codes, down_scales, down_g, x, ids, w, y, NULL, NULL, NULL, NULL};
+  return forward_mt(a, nthreads);
+}
+
+/* The routed MoE output with W4A4 numerics (NVFP4 weights, activations
+ * quantized to NVFP4 with each expert's static input scales, see
+ * oracle_expert_ffn_w4a4), on `nthreads` threads as oracle_moe_forward_mt.
+ * act, when not NULL, receives the float64 activation of every (token, slot)
+ * pair [C * k][I] (rows of skipped slots are left as they were). */
+int oracle_moe_forward_w4a4_mt(int nthreads, int C, int E, int k, int H, int I,
+                               const uint8_t *gate_codes, const uint8_t *gate_scales, const float *gate_g,
+                               const uint8_t *up_codes, const uint8_t *up_scales, const float *up_g,
+                               const uint8_t *down_codes, const uint8_t *down_scales, const float *down_g,
+                               const float *gate_a, const float *up_a, const float *down_a,
+                               const uint16_t *x, const int32_t *ids, const double *w, double *y, double *act) {
+  if (!gate_a || !up_a || !down_a) return ORACLE_ERR_ARG;
+  forward_args a = {ORACLE_FMT_NVFP4, C, E, k, H, I, gate_codes, gate_scales, gate_g, up_codes, up_scales, up_g,
+                    down_codes, down_scales, down_g, x, ids, w, y, gate_a, up_a, down_a, act};
+  return forward_mt(a, nthreads);
+}
+
+static int forward_mt(forward_args a, int nthreads) {
+  const int C = a.C, k = a.k, H = a.H;
+  const double *w = a.w;
+  double *y = a.y;
   if (!forward_args_ok(&a) || nthreads < 1) return ORACLE_ERR_ARG;
   init_tables();                       /* fill the shared tables before any thread reads them */
   const int64_t npairs = (int64_t)C * k;
@@ -576,4 +619,144 @@ uint16_t oracle_bf16_round(double v) {
   uint32_t u;
   memcpy(&u, &f, sizeof u);
   return (uint16_t)((u >> 16) | (neg ? 0x8000u : 0u));
+}
+
+/* ------------------------------------------------------ W4A4 activations */
+
+/* Round a non-negative float to e4m3 (nearest, ties to even mantissa, values
+ * above the largest finite 448 saturate to 448): the byte. */
+static uint8_t e4m3_rne_sat(float v) {
+  if (!(v > 0.0f)) return 0;
+  if (v >= 448.0f) return 0x7E;
+  const double d = (double)v;                  /* exact */
+  if (d < 0.015625) {                          /* subnormal: multiples of 2^-9 */
+    double q = d * 512.0, r = floor(q), f = q - r;
+    if (f > 0.5 || (f == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    return (uint8_t)(r >= 8.0 ? 0x08 : (int)r);  /* 8 * 2^-9 = 2^-6, the smallest normal */
+  }
+  int ex;
+  const double m = frexp(d, &ex);              /* d = m 2^ex, m in [0.5, 1) */
+  int e = ex - 1;
+  double q = (2.0 * m - 1.0) * 8.0, r = floor(q), f = q - r;
+  if (f > 0.5 || (f == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  if (r >= 8.0) { r = 0.0; e += 1; }
+  if (e > 8 || (e == 8 && r > 6.0)) return 0x7E;
+  return (uint8_t)(((e + 7) << 3) | (int)r);
+}
+
+/* Round a float to e2m1 (nearest, ties to even, |v| > 6 saturates to 6): the
+ * 4-bit code, sign in bit 3 (a negative value that rounds to zero keeps its
+ * sign bit). */
+static uint8_t e2m1_rne_sat(float v) {
+  const float a = fabsf(v);
+  uint8_t mag;
+  /* magnitudes 0 0.5 1 1.5 2 3 4 6; midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5,
+   * a tie goes to the even mantissa (codes 0, 2, 4, 6) */
+  if (a <= 0.25f) mag = 0;
+  else if (a < 0.75f) mag = 1;
+  else if (a <= 1.25f) mag = 2;
+  else if (a < 1.75f) mag = 3;
+  else if (a <= 2.5f) mag = 4;
+  else if (a < 3.5f) mag = 5;
+  else if (a <= 5.0f) mag = 6;
+  else mag = 7;
+  return (uint8_t)(mag | (signbit(v) ? 8 : 0));
+}
+
+/* NVFP4 quantization of an activation vector v[n] (n a multiple of 16) with
+ * the static per-tensor input scale a (the second fp32 of a matrix in the
+ * NVFP4 checkpoint, "Kimi-K3 on the same pod, two engines", section "Same
+ * hardware, same weights": 24 bytes of fp32 scalars per expert), in fp32
+ * arithmetic step for step as the GPU does it:
+ *   per block of 16: amax = max |v|;  s = e4m3(amax / (6 a))  (the byte);
+ *   each element: code = e2m1(v / (e4m3value(s) a));  all-zero block: 0.
+ * The dequantized element is e2m1(code) * e4m3value(s) * a.  Codes are
+ * packed two per byte, low nibble = even element. */
+int oracle_quantize_nvfp4(int n, const float *v, float a, uint8_t *codes, uint8_t *scales) {
+  if (n <= 0 || n % 16 || !v || !codes || !scales || !(a > 0.0f)) return ORACLE_ERR_ARG;
+  init_tables();
+  for (int b = 0; b < n / 16; b++) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(v[16 * b + i]));
+    const float denom = 6.0f * a;
+    const float t = amax / denom;
+    const uint8_t sb = e4m3_rne_sat(t);
+    scales[b] = sb;
+    const float sv = (float)e4m3_table[sb];     /* exact in float */
+    const float m = sv * a;
+    for (int i = 0; i < 16; i += 2) {
+      uint8_t c0 = 0, c1 = 0;
+      if (sv > 0.0f) {
+        c0 = e2m1_rne_sat(v[16 * b + i] / m);
+        c1 = e2m1_rne_sat(v[16 * b + i + 1] / m);
+      }
+      codes[(16 * b + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* The dequantized value of every element of a quantized activation vector:
+ * e2m1(code) * e4m3(scale) * a (float64, exact). */
+static void dequant_act(int n, const uint8_t *codes, const uint8_t *scales, float a, double *out) {
+  for (int k = 0; k < n; k++) {
+    const uint8_t byte = codes[k / 2];
+    const uint8_t nib = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+    out[k] = e2m1_table[nib] * e4m3_table[scales[k / 16]] * (double)a;
+  }
+}
+
+/* One expert's FFN with W4A4 numerics (NVFP4 weights and activations):
+ *   xq  = Q(x, a_in)                  the input quantized with the gate
+ *                                     matrix's input scale (gate and up see
+ *                                     the same x)
+ *   g = G xq, u = U xq;  act = silu(g) * u    (float64)
+ *   aq  = Q((float) act, a_dn)        the down projection's input quantized
+ *                                     with the down matrix's input scale
+ *   y   = D aq
+ * Q is oracle_quantize_nvfp4 followed by the exact dequantization.  The
+ * float64 activation silu(g) * u before its rounding to float goes to
+ * act_out[I] when act_out is not NULL. */
+int oracle_expert_ffn_w4a4(int H, int I,
+                           const uint8_t *gate_codes, const uint8_t *gate_scales, float gate_g,
+                           const uint8_t *up_codes, const uint8_t *up_scales, float up_g,
+                           const uint8_t *down_codes, const uint8_t *down_scales, float down_g,
+                           float a_in, float a_dn, const double *x, double *y, double *act_out) {
+  if (H <= 0 || I <= 0 || H % 16 || I % 16 || !x || !y || !(a_in > 0.0f) || !(a_dn > 0.0f)) return ORACLE_ERR_ARG;
+  init_tables();
+  if (fmt_has_nan(ORACLE_FMT_NVFP4, gate_scales, (int64_t)I * (H / 16)) ||
+      fmt_has_nan(ORACLE_FMT_NVFP4, up_scales, (int64_t)I * (H / 16)) ||
+      fmt_has_nan(ORACLE_FMT_NVFP4, down_scales, (int64_t)H * (I / 16)))
+    return ORACLE_ERR_NAN_SCALE;
+  float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+  double *xq = (double *)malloc(sizeof(double) * (size_t)H);
+  float *af = (float *)malloc(sizeof(float) * (size_t)I);
+  double *aq = (double *)malloc(sizeof(double) * (size_t)I);
+  uint8_t *qc = (uint8_t *)malloc((size_t)(H > I ? H : I) / 2);
+  uint8_t *qs = (uint8_t *)malloc((size_t)(H > I ? H : I) / 16);
+  int rc = (xf && xq && af && aq && qc && qs) ? ORACLE_OK : ORACLE_ERR_ARG;
+  if (rc == ORACLE_OK) {
+    for (int k = 0; k < H; k++) xf[k] = (float)x[k];      /* x is bf16: exact */
+    oracle_quantize_nvfp4(H, xf, a_in, qc, qs);
+    dequant_act(H, qc, qs, a_in, xq);
+    for (int r = 0; r < I; r++) {
+      double g = 0.0, u = 0.0;
+      for (int k = 0; k < H; k++) {
+        g += fp4_weight(ORACLE_FMT_NVFP4, gate_codes, gate_scales, gate_g, H, r, k) * xq[k];
+        u += fp4_weight(ORACLE_FMT_NVFP4, up_codes, up_scales, up_g, H, r, k) * xq[k];
+      }
+      const double h = silu(g) * u;
+      if (act_out) act_out[r] = h;
+      af[r] = (float)h;
+    }
+    oracle_quantize_nvfp4(I, af, a_dn, qc, qs);
+    dequant_act(I, qc, qs, a_dn, aq);
+    for (int r = 0; r < H; r++) {
+      double s = 0.0;
+      for (int k = 0; k < I; k++) s += fp4_weight(ORACLE_FMT_NVFP4, down_codes, down_scales, down_g, I, r, k) * aq[k];
+      y[r] = s;
+    }
+  }
+  free(xf); free(xq); free(af); free(aq); free(qc); free(qs);
+  return rc;
 }

@@ -46,6 +46,7 @@ IH8_INV_SD = 1.0 / math.sqrt(8 * (65536 ** 2 - 1) / 12)
 WEIGHT_STD = 0.02
 W_COEF = WEIGHT_STD * IH8_INV_SD          # multiplies (S - 262140) to give w
 W_ABS_MAX = 262140.0 * W_COEF             # largest |w| the generator can emit
+X_ABS_MAX = 262140.0 * IH8_INV_SD         # largest |z| of a standard deviate (4.899)
 
 # Key kinds (first part after the seed).
 KIND_WEIGHT = 1
@@ -197,15 +198,30 @@ def quantize_mxfp4(w: np.ndarray):
 
 # ------------------------------------------------------------ layer inputs
 
-def global_scales(seed: int, layer: int, E: int):
-    """Per-(expert, matrix) fp32 weight scales g and (unused) input scales a.
+def global_scales(seed: int, layer: int, E: int, H: int):
+    """Per-(expert, matrix) fp32 weight scales g and input scales a.
 
     g = (W_ABS_MAX / (6 * 448)) * (1 + 0.5 u): the block scale never saturates
-    and each matrix gets its own g.  Returns float32 arrays g[3][E], a[3][E]."""
+    and each matrix gets its own g.
+
+    a is the static activation scale a calibration pass would store: the
+    calibrated largest |input| over 6 * 448, so that an input block whose
+    largest element reaches that bound gets the largest e4m3 block scale.
+      gate, up: the input x is N(0, 1) with |x| <= X_ABS_MAX (the Irwin-Hall
+                bound); a = X_ABS_MAX / (6 * 448) * (1 + 0.25 u), the same
+                value for gate and up (they read the same input);
+      down:     the input h = silu(g) u with g, u of standard deviation
+                sigma = WEIGHT_STD sqrt(H) (H products of N(0, 0.02^2)
+                weights with N(0, 1) inputs); a = 16 sigma^2 / (6 * 448) *
+                (1 + 0.25 u), so |h| saturates only far in the tails.
+    Only W4A4 layers use a.  Returns float32 arrays g[3][E], a[3][E]."""
     u = uniforms(key(seed, KIND_GSCALE, layer), 6 * E).reshape(6, E)
     base = W_ABS_MAX / (6.0 * _E4M3_MAX)
     g = (base * (1.0 + 0.5 * u[:3])).astype(np.float32)
-    a = (0.5 + u[3:]).astype(np.float32)
+    sigma2 = WEIGHT_STD * WEIGHT_STD * H
+    a_x = (X_ABS_MAX / (6.0 * _E4M3_MAX)) * (1.0 + 0.25 * u[3])
+    a_h = (16.0 * sigma2 / (6.0 * _E4M3_MAX)) * (1.0 + 0.25 * u[5])
+    a = np.stack([a_x, a_x, a_h]).astype(np.float32)
     return g, a
 
 
@@ -231,7 +247,7 @@ def canonical_layer(seed: int, layer: int, E: int, H: int, I: int, experts=None,
     g/a [n] for the experts listed (all E by default), in that order.  MXFP4
     matrices carry the tensor scale g = 1."""
     experts = list(range(E)) if experts is None else list(experts)
-    g, a = global_scales(seed, layer, E)
+    g, a = global_scales(seed, layer, E, H)
     if fmt == "mxfp4":
         g = np.ones_like(g)
     blk = 32 if fmt == "mxfp4" else 16

@@ -48,7 +48,7 @@ def canonical_layer_device(seed: int, layer: int, E: int, H: int, I: int, device
     [E][rows][K/16] (NVFP4) or [E][rows][K/32] (MXFP4) uint8, [E] float32,
     [E] float32; MXFP4 matrices have g = 1)."""
     lib = _load()
-    g, a = global_scales(seed, layer, E)
+    g, a = global_scales(seed, layer, E, H)
     if fmt == "mxfp4":
         g = np.ones_like(g)
     stream = stream or torch.cuda.current_stream(device)
