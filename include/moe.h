@@ -87,13 +87,28 @@ typedef enum {
  * layers only. */
 #define MOE_CONFIG_GROUPED_ABOVE_8 0x2u
 
+/* moe_config.flags: W4A4 numerics (NVFP4 layers only).  Each matrix's input
+ * is quantized to NVFP4 with that matrix's fp32 input scale a (the second of
+ * its two scalars; "Kimi-K3 on the same pod, two engines", section "Same
+ * hardware, same weights": 24 bytes of fp32 scalars per expert): per block of
+ * 16 elements the e4m3 scale byte s = e4m3(max|v| / (6 a)) and the e2m1
+ * codes e2m1(v / (s a)), both rounded to nearest even and saturating; the
+ * quantized value is e2m1 * s * a.  x is quantized per (token, expert) with
+ * max(a_gate, a_up) (gate and up read one quantized x); h = silu(g) * u per
+ * (token, expert) with a_down; the router weight multiplies the expert's
+ * output after the down projection.  Every C takes the grouped tcgen05 path.
+ * Results agree with the W4A16 ones only to the activation quantization
+ * noise (a few per cent). */
+#define MOE_CONFIG_W4A4 0x4u
+
 typedef struct {
   int32_t num_experts;   /* E, 1 .. 1024 */
   int32_t top_k;         /* k, 1 .. min(32, E) */
   int32_t hidden;        /* H, expert input/output width, multiple of 64, <= 4096 */
   int32_t intermediate;  /* I, expert FFN width, multiple of 64, <= 4096 */
   int32_t max_tokens;    /* largest C passed to route/forward, >= 1 */
-  uint32_t flags;        /* MOE_CONFIG_MXFP4, MOE_CONFIG_GROUPED_ABOVE_8, the test hook MOE_CONFIG_TEST_ROUTER_STALL, or 0 */
+  uint32_t flags;        /* MOE_CONFIG_MXFP4 or MOE_CONFIG_W4A4, MOE_CONFIG_GROUPED_ABOVE_8, the test hook
+                            MOE_CONFIG_TEST_ROUTER_STALL, or 0; MXFP4 with W4A4: MOE_ERR_INVALID_ARG */
 } moe_config;
 
 typedef struct {
@@ -249,7 +264,9 @@ typedef struct {
   const float *norm_gamma;      /* device fp32 [latent] */
 } moe_ffn_weights;
 
-/* A host-side handle tied to `routed` (which must outlive it). */
+/* A host-side handle tied to `routed` (which must outlive it).  The dense
+ * projections run W4A16 numerics; a routed layer created with
+ * MOE_CONFIG_W4A4 is rejected (MOE_ERR_INVALID_ARG). */
 moe_status moe_ffn_create(const moe_ffn_config *cfg, moe_layer_t routed, moe_ffn_t *out);
 moe_status moe_ffn_destroy(moe_ffn_t ffn);
 /* Bytes of the packed buffer of the FFN's own weights (not the routed ones). */
@@ -273,6 +290,29 @@ moe_status moe_ffn_finish(moe_ffn_t ffn, const uint16_t *u, int num_tokens, cons
 moe_status moe_ffn_forward(moe_ffn_t ffn, const uint16_t *u, int num_tokens, const float *w_router,
                            const float *bias, const void *routed_packed, const void *ffn_packed, int32_t *ids,
                            float *weights, float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
+ * The W4A4 activation quantizer (MOE_CONFIG_W4A4) as a call of its own.
+ * Quantizes `rows` rows of n elements (n a multiple of 16) to NVFP4 with the
+ * static input scale a (finite, > 0): per block of 16 elements the e4m3 scale
+ * byte s = e4m3(max|v| / (6 a)) and the e2m1 codes e2m1(v / (e4m3(s) a)),
+ * each step one correctly rounded fp32 operation, both roundings to nearest
+ * even and saturating (an all-zero block, or one whose s underflows to 0,
+ * gets zero codes); the input scale of "Kimi-K3 on the same pod, two
+ * engines", section "Same hardware, same weights".  The kernels of the W4A4
+ * layers quantize with the same device code.
+ *   src     device, [rows][n], bf16 bits (src_dtype MOE_ACT_BF16) or fp32
+ *           (MOE_ACT_F32), 16-byte aligned; read only
+ *   codes   device, [rows][n/2], low nibble = even element, 16-byte aligned
+ *   scales  device, [rows][n/16] e4m3 bytes
+ * The caller owns every buffer.  Queued on `stream`; MOE_ERR_INVALID_ARG on a
+ * null or misaligned pointer, rows < 1, n < 16, n % 16 != 0, an unknown
+ * src_dtype or a not finite or not positive a; MOE_ERR_CUDA if the launch
+ * fails. */
+#define MOE_ACT_BF16 0
+#define MOE_ACT_F32 1
+moe_status moe_quantize_nvfp4(const void *src, int32_t src_dtype, int64_t rows, int32_t n, float a,
+                              uint8_t *codes, uint8_t *scales, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char *moe_status_string(moe_status status);

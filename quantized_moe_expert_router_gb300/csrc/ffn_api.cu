@@ -140,6 +140,7 @@ moe_status moe_ffn_create(const moe_ffn_config *cfg, moe_layer_t routed, moe_ffn
   const moe_ffn_config c = *cfg;
   if (c.flags != 0 || !(c.eps > 0.f) || c.shared_experts < 0 || c.shared_experts > moe::kMaxDenseSegs - 1)
     return MOE_ERR_INVALID_ARG;
+  if (routed->w4a4) return MOE_ERR_INVALID_ARG;     // the projections around the routed sum are W4A16
   if (c.hidden < 64 || c.hidden % 64 || c.hidden > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.shared_experts > 0 && (c.shared_intermediate < 64 || c.shared_intermediate % 64 || c.shared_intermediate > 4096))
     return MOE_ERR_UNSUPPORTED_SHAPE;

@@ -65,6 +65,7 @@
 #include "moe_internal.cuh"
 #include "kernels.h"
 #include "gemv_core.cuh"
+#include "quant_core.cuh"
 
 namespace moe {
 
@@ -309,6 +310,74 @@ __global__ void __launch_bounds__(kHprepThreads) group_hprep_kernel(const GroupA
   }
 }
 
+// ---------------------------------------------------------------- W4A4 rows
+// W4A4: the B rows hold the NVFP4-quantized activations of each dispatched
+// pair, e2m1 * e4m3 in f16 (exact); the input scale a is applied in the
+// epilogue.  One item per (block of 16 elements, pair): 16 inputs, one
+// quantized block, two 16-byte stores (k-groups 2 kb and 2 kb + 1).
+//   x rows: token t_j's x quantized with its expert's gate/up input scale
+//           max(a_gate, a_up) (gate and up read one quantized x);
+//   h rows: pair p's h quantized with its expert's down input scale a_down.
+__device__ __forceinline__ void store_quant_block(uint16_t *buf, int R, int kb, int j, const uint32_t (&vals)[8]) {
+  uint4 *dst = reinterpret_cast<uint4 *>(buf);
+  dst[(size_t)(2 * kb) * R + j] = make_uint4(vals[0], vals[1], vals[2], vals[3]);
+  dst[(size_t)(2 * kb + 1) * R + j] = make_uint4(vals[4], vals[5], vals[6], vals[7]);
+}
+
+__global__ void __launch_bounds__(256) group_xquant_kernel(const GroupArgs a) {
+  const int n = a.gd[0];
+  const int total = gd_off(a.gd, a.E)[n];
+  const int *pairs = gd_pairs(a.gd, a.E);
+  const int P = a.C * a.k, KB = a.Hp / 16;
+  const int items = total * KB;
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+    const int kb = it / total, j = it - kb * total;
+    const int p = __ldg(pairs + j), t = p / a.k, e = __ldg(a.ids + p);
+    uint32_t vals[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (16 * kb < a.H) {
+      const float ain = fmaxf(__ldg(a.scalars + (size_t)e * 6 + 1), __ldg(a.scalars + (size_t)e * 6 + 3));
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + 16 * kb);
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      uint32_t codes[2];
+      nvfp4_quant_block(v, ain, codes, vals);
+    }
+    store_quant_block(a.xg, P, kb, j, vals);
+  }
+}
+
+__global__ void __launch_bounds__(256) group_hquant_kernel(const GroupArgs a) {
+  const int n = a.gd[0];
+  const int total = gd_off(a.gd, a.E)[n];
+  const int *pairs = gd_pairs(a.gd, a.E);
+  const int P = a.C * a.k, KB = a.Ip / 16;
+  const int items = total * KB;
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+    const int kb = it / total, j = it - kb * total;
+    const int p = __ldg(pairs + j), e = __ldg(a.ids + p);
+    uint32_t vals[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (16 * kb < a.I) {
+      const float adn = __ldg(a.scalars + (size_t)e * 6 + 5);
+      const float4 *src = reinterpret_cast<const float4 *>(a.hbuf + (size_t)p * a.I + 16 * kb);
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const float4 f = __ldcg(src + i);
+        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+      }
+      uint32_t codes[2];
+      nvfp4_quant_block(v, adn, codes, vals);
+    }
+    store_quant_block(a.hg, P, kb, j, vals);
+  }
+}
+
 // ---------------------------------------------------------------- tensor-core GEMM
 struct GroupTcArgs {
   CUtensorMap bmap[kTcBoxes];   // B rows: boxes of (8, 16 << i, 32) over [K/8][rows][8] f16
@@ -482,11 +551,17 @@ __device__ __forceinline__ void unit_shape(int np, int rf, int &rows, int &N, in
   bi = N <= 16 ? 0 : (N <= 32 ? 1 : 2);
 }
 
+// MODE 0: gate/up + SwiGLU (x rows f16, per-token 2^-s, router weight folded
+// into h); 1: down (hi and lo rows of h, per-pair 2^-s); 2: gate/up with W4A4
+// rows (x quantized, the input scale applied here, h without the router
+// weight); 3: down with W4A4 rows (one row per pair; input scale and router
+// weight applied here).
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_constant__ GroupTcArgs a) {
   extern __shared__ uint8_t dsm[];
   __shared__ TcSmem s;
-  constexpr int rf = MODE == 0 ? 1 : 2;            // B rows per pair
+  constexpr bool GU = MODE == 0 || MODE == 2;
+  constexpr int rf = MODE == 1 ? 2 : 1;            // B rows per pair
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, cols = a.cols;
   const int MP = (a.tiles + kTcUnitTiles - 1) / kTcUnitTiles;   // m-tile pairs per expert
@@ -742,15 +817,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
     const int g = (lane >> 1) & 7, hi = lane & 1;
     const uint32_t trow = tbase + ((uint32_t)(32 * wq) << 16);
     int ud = 0, cur = -1;
-    float sc0 = 0.f, sc1 = 0.f;
+    float sc0 = 0.f, sc1 = 0.f, xa = 1.f;            // tensor scales; W4A4: the input scale
     for (TcUnit u = beg; unit_before(u, end); unit_next(s, u, MP, cols), ud++) {
       const int off = s.off[u.d], np = min(cols, s.off[u.d + 1] - off - u.nc * cols);
       const int j0 = off + u.nc * cols;
       if (u.d != cur) {
         cur = u.d;
         const float *sc = a.scalars + (size_t)s.expert[u.d] * 6;
-        sc0 = MODE == 0 ? sc[0] : sc[4];
+        sc0 = GU ? sc[0] : sc[4];
         sc1 = sc[2];
+        if constexpr (MODE == 2) xa = fmaxf(sc[1], sc[3]);
+        if constexpr (MODE == 3) xa = sc[5];
       }
       epi_sync();                                    // the previous unit's column data is read
       if (et < np) {
@@ -759,8 +836,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         if constexpr (MODE == 0) {
           s.colw[et] = __ldg(a.weights + p);
           s.cols[et] = __ldg(a.colscale + p / a.k);
-        } else {
+        } else if constexpr (MODE == 1) {
           s.cols[et] = __ldcg(a.colscale + p);
+        } else if constexpr (MODE == 3) {
+          s.colw[et] = __ldg(a.weights + p);
         }
       }
       const int db = ud & 1;
@@ -795,6 +874,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
                 const float gg = v[i] * xs * sc0, uu = up * xs * sc1;
                 __stcs(a.out + (size_t)s.colp[nn] * a.I + 8 * T + g, s.colw[nn] * silu(gg) * uu);
               }
+            }
+          } else if constexpr (MODE == 2) {
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+              const int nn = c0 + i;
+              if (nn >= np) break;
+              const float up = __shfl_xor_sync(kFull, v[i], 1);
+              if (!hi && T < a.tiles) {
+                const float gg = v[i] * xa * sc0, uu = up * xa * sc1;
+                __stcs(a.out + (size_t)s.colp[nn] * a.I + 8 * T + g, silu(gg) * uu);
+              }
+            }
+          } else if constexpr (MODE == 3) {
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+              const int nn = c0 + i;
+              if (nn >= np) break;
+              if (T < a.tiles)
+                __stcs(a.out + (size_t)s.colp[nn] * a.H + 16 * T + (lane & 15), v[i] * xa * sc0 * s.colw[nn]);
             }
           } else {
 #pragma unroll
@@ -915,6 +1013,10 @@ cudaError_t group_setup() {
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(group_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(group_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(group_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+  if (err == cudaSuccess)
     err = cudaFuncSetAttribute(group_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)group_dispatch_smem(kMaxExperts));
   return err;
@@ -932,9 +1034,13 @@ cudaError_t launch_group_forward(GroupArgs a, int num_sms, int w_gu, int w_dn, s
   if (err != cudaSuccess) return err;
   group_dispatch_kernel<<<1, kGDispatchThreads, group_dispatch_smem(a.E), stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  group_xprep_kernel<<<a.C, 128, 0, stream>>>(a);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  group_xgather_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  if (a.w4a4) {
+    group_xquant_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  } else {
+    group_xprep_kernel<<<a.C, 128, 0, stream>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    group_xgather_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  }
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // gate/up + SwiGLU
   t.scalars = a.scalars;
@@ -950,22 +1056,25 @@ cudaError_t launch_group_forward(GroupArgs a, int num_sms, int w_gu, int w_dn, s
   if ((err = encode_a_maps(t.amap, a.packed, 0, w_gu, t.tiles, (int)gu_tile_bytes, a.E, a.expert_bytes)) !=
       cudaSuccess)
     return err;
-  group_tc_kernel<0><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
+  if (a.w4a4) group_tc_kernel<2><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
+  else group_tc_kernel<0><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (after_gate_up && (err = cudaEventRecord(after_gate_up, stream)) != cudaSuccess) return err;
-  group_hprep_kernel<<<num_sms * 8, kHprepThreads, 0, stream>>>(a);
+  if (a.w4a4) group_hquant_kernel<<<num_sms * 4, 256, 0, stream>>>(a);
+  else group_hprep_kernel<<<num_sms * 8, kHprepThreads, 0, stream>>>(a);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // down
-  if ((err = encode_b_maps(t.bmap, a.hg, 2 * P, a.Ip)) != cudaSuccess) return err;
+  if ((err = encode_b_maps(t.bmap, a.hg, a.w4a4 ? P : 2 * P, a.Ip)) != cudaSuccess) return err;
   t.colscale = a.hinv;
   t.out = a.ypair;
   t.Kp = a.Ip;
   t.tiles = a.H / 16;
-  t.cols = kTcColsDN;
+  t.cols = a.w4a4 ? kTcColsGU : kTcColsDN;
   if ((err = encode_a_maps(t.amap, a.packed, dn_region_off, w_dn, t.tiles, (int)dn_tile_bytes, a.E, a.expert_bytes)) !=
       cudaSuccess)
     return err;
-  group_tc_kernel<1><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
+  if (a.w4a4) group_tc_kernel<3><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
+  else group_tc_kernel<1><<<num_sms, kTcThreads, kTcSmemBytes, stream>>>(t);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   group_combine_kernel<<<a.C, 128, 0, stream>>>(a);
   return cudaGetLastError();

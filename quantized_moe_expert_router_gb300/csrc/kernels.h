@@ -98,6 +98,7 @@ struct GroupArgs {
   int32_t *flags;
   int C, k, E, H, I, Hp, Ip;
   size_t expert_bytes;
+  int w4a4;                  // W4A4 numerics: xg and hg hold NVFP4-quantized values, one hg row per pair
 };
 // Opt-in shared memory of the grouped kernels (once per device; idempotent).
 cudaError_t group_setup();

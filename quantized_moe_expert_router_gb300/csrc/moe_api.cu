@@ -60,9 +60,11 @@ const char *moe_status_string(moe_status s) {
 moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out) {
   if (!cfg || !out) return MOE_ERR_INVALID_ARG;
   const moe_config c = *cfg;
-  if ((c.flags & ~(uint32_t)(MOE_CONFIG_TEST_ROUTER_STALL | MOE_CONFIG_MXFP4 | MOE_CONFIG_GROUPED_ABOVE_8)) != 0 ||
+  if ((c.flags & ~(uint32_t)(MOE_CONFIG_TEST_ROUTER_STALL | MOE_CONFIG_MXFP4 | MOE_CONFIG_GROUPED_ABOVE_8 |
+                             MOE_CONFIG_W4A4)) != 0 ||
       c.max_tokens < 1)
     return MOE_ERR_INVALID_ARG;
+  if ((c.flags & MOE_CONFIG_MXFP4) && (c.flags & MOE_CONFIG_W4A4)) return MOE_ERR_INVALID_ARG;
   if (c.num_experts < 1 || c.num_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.top_k < 1 || c.top_k > moe::kMaxTopK || c.top_k > c.num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.hidden < 64 || c.hidden % 64 || c.hidden > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -78,6 +80,7 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   if (!L) return MOE_ERR_OUT_OF_MEMORY;
   L->cfg = c;
   L->fmt = (c.flags & MOE_CONFIG_MXFP4) ? moe::kFmtMxfp4 : moe::kFmtNvfp4;
+  L->w4a4 = (c.flags & MOE_CONFIG_W4A4) ? 1 : 0;
   L->device = device;
   L->num_sms = sms;
   L->Hp = (int)align_up(c.hidden, moe::kKAlign);
@@ -98,6 +101,7 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   // when an expert has one or two tokens: measured with uniform routing at
   // 896 experts, top-16, the two paths meet between 24 and 32 tokens
   L->grouped_min_tokens = (c.flags & MOE_CONFIG_GROUPED_ABOVE_8) ? moe::kGemvTokens + 1 : moe::kGroupedMinTokens;
+  if (L->w4a4) L->grouped_min_tokens = 1;    // the W4A4 rows exist on the grouped path only
   if (moe::gemv_setup() != cudaSuccess) {
     delete L;
     return MOE_ERR_CUDA;
@@ -232,8 +236,8 @@ moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *
 
   cudaError_t err = cudaSuccess;
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
-  // C > 8: the grouped tcgen05 path (NVFP4); MXFP4 layers run every C on the
-  // decode kernels, in groups of 8 tokens
+  // C >= grouped_min_tokens: the grouped tcgen05 path (NVFP4; every C for
+  // W4A4); MXFP4 layers run every C on the decode kernels, in groups of 8
   if (C >= L->grouped_min_tokens && L->fmt == moe::kFmtNvfp4) {
     // expert-major passes of up to kGroupTokens tokens
     moe::GroupArgs g = {};
@@ -249,6 +253,7 @@ moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *
     g.flags = a.flags;
     g.k = k; g.E = L->cfg.num_experts; g.H = H; g.I = I; g.Hp = L->Hp; g.Ip = L->Ip;
     g.expert_bytes = L->expert_bytes;
+    g.w4a4 = L->w4a4;
     for (int t0 = 0; t0 < C && err == cudaSuccess; t0 += moe::kGroupTokens) {
       g.C = (C - t0) < moe::kGroupTokens ? (C - t0) : moe::kGroupTokens;
       g.x = x + (size_t)t0 * H;

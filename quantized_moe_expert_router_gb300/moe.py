@@ -29,13 +29,16 @@ FLAG_TIMEOUT = 0x4
 CONFIG_TEST_ROUTER_STALL = 0x80000000   # test hook: the router's bounded wait runs out
 CONFIG_MXFP4 = 0x1                      # MXFP4 weights (e8m0 scale per 32 elements)
 CONFIG_GROUPED_ABOVE_8 = 0x2            # the grouped tcgen05 path for every call of more than 8 tokens
+CONFIG_W4A4 = 0x4                       # activations quantized to NVFP4 with each matrix's input scale
+ACT_BF16, ACT_F32 = 0, 1                # source types of moe_quantize_nvfp4
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_packed_bytes", "moe_workspace_bytes",
     "moe_pack_weights", "moe_route", "moe_forward", "moe_get_device_status",
     "moe_set_stage_events", "moe_route_noalloc", "moe_route_forward",
     "moe_ffn_create", "moe_ffn_destroy", "moe_ffn_packed_bytes", "moe_ffn_workspace_bytes",
-    "moe_ffn_pack_weights", "moe_ffn_partial", "moe_ffn_finish", "moe_ffn_forward", "moe_status_string",
+    "moe_ffn_pack_weights", "moe_ffn_partial", "moe_ffn_finish", "moe_ffn_forward", "moe_quantize_nvfp4",
+    "moe_status_string",
 )
 
 
@@ -103,6 +106,7 @@ def load_library(path: str = LIB_PATH):
             lib.moe_ffn_partial.argtypes = [P, P, I32, P, P, P, P, P, P, P, P, SZ, P]
             lib.moe_ffn_finish.argtypes = [P, P, I32, P, P, P, P, SZ, P]
             lib.moe_ffn_forward.argtypes = [P, P, I32, P, P, P, P, P, P, P, P, SZ, P]
+            lib.moe_quantize_nvfp4.argtypes = [P, I32, ctypes.c_int64, I32, ctypes.c_float, P, P, P]
             lib.moe_status_string.argtypes = [I32]
             lib.moe_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -225,6 +229,19 @@ def moe_set_stage_events(layer, events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     layer._stage_events = (events, arr)      # keep alive
     _check("moe_set_stage_events", lib.moe_set_stage_events(layer.handle, arr, len(events)))
+
+
+def moe_quantize_nvfp4(src: torch.Tensor, a: float, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """NVFP4 quantization of src [rows][n] (torch.bfloat16, or uint16 bf16
+    bits, or torch.float32) with input scale a into codes uint8 [rows][n/2]
+    and scales uint8 [rows][n/16] (device tensors)."""
+    dtype = ACT_F32 if src.dtype == torch.float32 else ACT_BF16
+    if src.dtype not in (torch.float32, torch.bfloat16, torch.uint16, torch.int16):
+        raise TypeError(f"moe_quantize_nvfp4: unsupported source dtype {src.dtype}")
+    n = src.shape[-1]
+    rows = src.numel() // n if n else 0
+    _check("moe_quantize_nvfp4", load_library().moe_quantize_nvfp4(
+        _ptr(src), dtype, rows, n, float(a), _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def moe_status_string(status: int) -> str:

@@ -277,3 +277,49 @@ def test_forward_is_w4a16_plus_activation_quantization_noise():
     y4 = oracle.moe_forward_w4a4(L, x, ids, w)
     rel = np.linalg.norm(y4 - y16) / np.linalg.norm(y16)
     assert 0.02 < rel < 0.25, rel
+
+
+# ---------------------------------------------------------------- the W4A4 tolerance
+
+def simulated_outputs(L, ids, w, act, noise, rng, fold_weight=False, a_scale=1.0):
+    """y from the oracle's activations perturbed by `noise` * (block max |h|)
+    (what a different summation order can do), quantized by the brute-force
+    quantizer; fold_weight quantizes w * h instead of h (a planted mistake);
+    a_scale multiplies the down input scale (another)."""
+    C, k, I = act.shape
+    H = L["down"]["codes"].shape[1]
+    y = np.zeros((C, H))
+    for t in range(C):
+        for i in range(k):
+            e = int(ids[t, i])
+            h = act[t, i].reshape(-1, 16)
+            h = (h + noise * np.abs(h).max(1, keepdims=True) * rng.uniform(-1, 1, h.shape)).reshape(-1)
+            if fold_weight:
+                y[t] += deq(L["down"], e) @ brute_deq((w[t, i] * h).astype(np.float32), L["down"]["a"][e])
+            else:
+                aq = brute_deq(h.astype(np.float32), np.float32(L["down"]["a"][e] * a_scale))
+                y[t] += w[t, i] * (deq(L["down"], e) @ aq)
+    return y
+
+
+def test_w4a4_tolerance_covers_tie_flips_and_catches_planted_mistakes():
+    from helpers import W4A4_EPS, assert_close_w4a4, w4a4_allowance
+    E, H, I, k, C = 6, 512, 384, 3, 3
+    L = synth.canonical_layer(21, 0, E, H, I)
+    x = synth.tokens(21, 0, C, H)
+    ids = np.array([[0, 1, 2], [3, 4, 5], [5, 0, 2]], np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.4, 0.4, 0.2], [0.6, 0.3, 0.1]])
+    oy, act = oracle.moe_forward_w4a4(L, x, ids, w, return_act=True)
+    allow, n_amb = w4a4_allowance(L["down"], ids, w, act)
+    assert n_amb > 0
+    rng = np.random.default_rng(1)
+    # noise at and below the bound: decisions near ties flip, the allowance covers them
+    for noise in (1e-6, W4A4_EPS / 2, W4A4_EPS):
+        assert_close_w4a4(simulated_outputs(L, ids, w, act, noise, rng), oy, allow, f"noise {noise}")
+    # without the allowance the flips at noise = eps are visible
+    y_flip = simulated_outputs(L, ids, w, act, W4A4_EPS, rng)
+    assert np.abs(y_flip - oy).max() > 0
+    # planted mistakes: router weight folded into h before quantization, wrong down scale
+    for kw in ({"fold_weight": True}, {"a_scale": 1.5}):
+        with pytest.raises(AssertionError):
+            assert_close_w4a4(simulated_outputs(L, ids, w, act, 0.0, rng, **kw), oy, allow, str(kw))
