@@ -81,6 +81,13 @@ CONFIGS = {
                     workload="K3-shape MoE FFN at decode batch 1: routed_down 7168->3584, router + top-16 of 896 "
                              "experts, routed_norm, routed_up 3584->7168, 2 shared experts (7168->3072->7168), "
                              "NVFP4"),
+    "prefill512w4a4": dict(E=896, k=16, H=3584, I=3072, C=512, layers=1, zipf=True, w4a4=True,
+                           workload="K3-shape MoE layer, prefill of 512 tokens, top-16 of 896, NVFP4 weights, "
+                                    "W4A4 (x and h quantized to NVFP4 with each expert's static input scales), "
+                                    "Zipf-biased routing (s = 1.1)"),
+    "k3b1w4a4": dict(E=896, k=16, H=3584, I=3072, C=1, layers=1, zipf=False, w4a4=True,
+                     workload="K3-shape MoE layer, decode batch 1, top-16 of 896, NVFP4 weights, W4A4 "
+                              "(grouped tcgen05 path), uniform routing"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -257,8 +264,11 @@ def oracle_sample(cfg, seed, layer_id, weights_for, budget_s, Wr, bias, x_bits, 
         weights = weights_for(sel)                       # input staging, not timed
         t_prep = time.perf_counter() - t_prep0
         remap = {e: i for i, e in enumerate(sel)}
-        oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads,
-                           fmt=cfg.get("fmt", "nvfp4"))
+        if cfg.get("w4a4"):
+            oracle.moe_forward_w4a4(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads)
+        else:
+            oracle.moe_forward(weights, xb, np.vectorize(remap.get)(ids).astype(np.int32), w, threads=threads,
+                               fmt=cfg.get("fmt", "nvfp4"))
         t_total += time.perf_counter() - t0 - t_prep
         done += 1
         if t_total >= budget_s:
@@ -363,7 +373,10 @@ def main():
     # one handle serves every layer (it holds the shapes only); per layer its
     # packed weights, router and (Zipf) router bias
     fmt = cfg.get("fmt", "nvfp4")
-    layer = moe.Layer(E, k, H, I, C, device=local, flags=moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0)
+    w4a4 = bool(cfg.get("w4a4"))
+    layer = moe.Layer(E, k, H, I, C, device=local,
+                      flags=(moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0) | (moe.CONFIG_W4A4 if w4a4 else 0))
+    grouped = C >= 28 or w4a4                     # the path moe_forward takes
     router_std = synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0
     packed, Wr_ds, bias_ds, biases = [], [], [], []
     canon = None
@@ -621,11 +634,11 @@ def main():
     dn_avg = float(np.mean(dn_ms))
     hbm_peak, peak_src = measured_peaks()
     achieved = gu_units * gu_bytes_per_expert / (gu_avg * 1e-3) / 1e9
-    if C >= 28:
+    if grouped:
         # grouped path: the stage events bracket dispatch, x-row prep and the gate/up GEMM
         traffic_per_expert, traffic_src = ncu_traffic("grouped.cu", f"group_tc_gu_{args.config}")
-        kernel_label = ("group_tc_kernel<0> (grouped gate/up + SwiGLU on tcgen05; the timed span also holds "
-                        "the dispatch and x-row kernels)")
+        kernel_label = (f"group_tc_kernel<{2 if w4a4 else 0}> (grouped gate/up + SwiGLU on tcgen05; the timed span "
+                        f"also holds the dispatch and x-row {'quantization ' if w4a4 else ''}kernels)")
     else:
         traffic_per_expert, traffic_src = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
         kernel_label = (f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
@@ -672,7 +685,9 @@ def main():
         line = {
             "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, f16 mma, f32 accumulate",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("nvfp4 weights and activations (W4A4), f16 mma of the exact e2m1 x e4m3 values, "
+                      "f32 accumulate" if w4a4 else "nvfp4 weights, f16 mma, f32 accumulate"),
             "data": "synthetic",
             "config": {"workload": cfg["workload"], "experts": E, "top_k": k, "hidden": H,
                        "intermediate": I, "tokens_per_step": C, "layers": NL,
@@ -697,9 +712,11 @@ def main():
             # FFN: + routed_down (2), routed_norm (1), routed_up (2) and 4 per shared expert
             # routed layer per call: C <= 8: fused router, gate/up, down, combine;
             # 9 .. 27 tokens: tiled router + top-k, then 3 decode kernels per group
-            # of 8; 28 or more: router, then 7 grouped kernels per pass of 512
-            "gpu_launches": args.steps * NL * ((4 if C <= 8 else 2 + 3 * ((C + 7) // 8) if C < 28
-                                                else 2 + 7 * ((C + 511) // 512))
+            # of 8; 28 or more: router, then 7 grouped kernels per pass of 512;
+            # W4A4: router (1 kernel for C <= 8, else 2), then 6 grouped kernels per pass
+            "gpu_launches": args.steps * NL * ((((1 if C <= 8 else 2) + 6 * ((C + 511) // 512)) if w4a4 else
+                                                (4 if C <= 8 else 2 + 3 * ((C + 7) // 8) if C < 28
+                                                 else 2 + 7 * ((C + 511) // 512)))
                                                # FFN: GEMV A (2), norm (1), GEMV B (2; 3 for C > 4)
                                                + ((5 if C <= 4 else 6) if FFN else 0)),
             "clocks": clocks,
