@@ -629,7 +629,11 @@ def main():
     gu_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof)]
     dn_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_prof)]
     gu_bytes_per_expert = 2 * (I * H // 2 + I * H // (32 if fmt == "mxfp4" else 16))
-    gu_units = sum(len(set(ids[i % ROTATE][0].cpu().numpy().ravel().tolist())) for i in range(n_prof)) / n_prof
+    # the stage events bracket the first gate/up launch of the call: on the
+    # decode path that is the first group of at most 8 tokens
+    first = C if grouped else min(C, 8)
+    gu_units = sum(len(set(ids[i % ROTATE][0][:first].cpu().numpy().ravel().tolist()))
+                   for i in range(n_prof)) / n_prof
     gu_avg = float(np.mean(gu_ms))
     dn_avg = float(np.mean(dn_ms))
     hbm_peak, peak_src = measured_peaks()
@@ -642,7 +646,8 @@ def main():
     else:
         traffic_per_expert, traffic_src = ncu_traffic("expert_gemv.cu", f"expert_gemv_gu_{args.config}")
         kernel_label = (f"expert_gemv_kernel<{2 if C <= 2 else 0}> (gate/up + SwiGLU, "
-                        f"{'two tiles' if C <= 2 else 'one tile'} per stage)")
+                        f"{'two tiles' if C <= 2 else 'one tile'} per stage"
+                        f"{'; the first group of 8 tokens' if C > 8 else ''})")
     roofline = {"kernel": kernel_label, "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": peak_src,

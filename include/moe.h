@@ -115,7 +115,8 @@ typedef struct {
   const uint8_t *codes;        /* device, [E][rows][K/2] */
   const uint8_t *scales;       /* device, [E][rows][K/16] e4m3 (NVFP4) or [E][rows][K/32] e8m0 (MXFP4) */
   const float *global_scale;   /* device, [E] */
-  const float *input_scale;    /* device, [E] (copied into the packed buffer, unused) */
+  const float *input_scale;    /* device, [E] (copied into the packed buffer; read only by
+                                  MOE_CONFIG_W4A4 layers, which quantise the matrix's input with it) */
 } moe_fp4_tensor;
 
 typedef struct {
@@ -146,7 +147,12 @@ moe_status moe_packed_bytes(moe_layer_t layer, size_t *bytes);
 moe_status moe_workspace_bytes(moe_layer_t layer, int num_tokens, size_t *bytes);
 
 /* Reorder canonical NVFP4 (or MXFP4) weights (all E experts) into the packed layout the
- * kernels stream: per expert, I "gate/up pair rows" (gate row r and up row r
+ * kernels stream.  The canonical form is the checkpoint's per matrix ("Kimi-K3
+ * on the same pod, two engines", section "Same hardware, same weights": 4-bit
+ * codes, an e4m3 scale per 16 elements, and two fp32 scalars -- the 24 bytes
+ * per expert beside the codes and scales); MXFP4 is the ggml microbench format
+ * of "Kimi-K3 on 2x A40 - measured findings" ("Why the placement experiments
+ * all looked the same").  Per expert, I "gate/up pair rows" (gate row r and up row r
  * interleaved per 16-element block) then H/2 "down pair rows" (down rows 2p
  * and 2p+1 interleaved), each pair row holding its codes and then its scale
  * bytes; the 6 fp32 scalars of all experts follow.  Offline, once per layer:
@@ -174,8 +180,15 @@ moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
                      const float *w_router, const float *bias, int32_t *ids,
                      float *weights, void *ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Routed expert FFN and combine for C tokens:
+/* Routed expert FFN and combine for C tokens: the MUL_MAT_ID step of "Kimi-K3
+ * on 2x A40 - measured findings" ("Why the placement experiments all looked
+ * the same": each token's selected experts' 3584->3072->3584 FFNs) with the
+ * routed sum of "SparkInfer-K3" ("How the TP module works"):
  *   y[t] = sum_i weights[t][i] * D_e (silu(G_e x[t]) * (U_e x[t])),  e = ids[t][i]
+ * (MOE_CONFIG_W4A4: G_e and U_e see x quantised to NVFP4, D_e sees h
+ * quantised, as that flag describes).  Below 28 tokens (MXFP4: every C) the
+ * decode kernels run groups of 8 tokens; from 28 tokens (W4A4: every C) the
+ * grouped tcgen05 kernels run passes of up to 512 tokens expert-major.
  * x: device bf16 bits [C][H]; ids: device int32 [C][k] (any order; each
  * token's ids must be distinct and < E -- offending slots are skipped and
  * flagged; a negative id marks an absent slot, skipped without a flag, which
@@ -200,7 +213,8 @@ moe_status moe_route_forward(moe_layer_t layer, const uint16_t *x, int num_token
 
 /* Synchronise `stream`, return the device flag bits accumulated in `ws` since
  * the last call (MOE_FLAG_*), and clear them together with the router's
- * completion counters.  No other call may be in flight on `ws`. */
+ * completion counters (after a MOE_FLAG_TIMEOUT the workspace is then as good
+ * as new).  No other call may be in flight on `ws`. */
 moe_status moe_get_device_status(moe_layer_t layer, void *ws, cudaStream_t stream,
                                  int32_t *flags);
 
