@@ -87,7 +87,7 @@ CONFIGS = {
                                     "Zipf-biased routing (s = 1.1)"),
     "k3b1w4a4": dict(E=896, k=16, H=3584, I=3072, C=1, layers=1, zipf=False, w4a4=True,
                      workload="K3-shape MoE layer, decode batch 1, top-16 of 896, NVFP4 weights, W4A4 "
-                              "(grouped tcgen05 path), uniform routing"),
+                              "(x and h quantized to NVFP4 in the decode kernels' fragments), uniform routing"),
     "tiny": dict(E=32, k=4, H=256, I=192, C=1, layers=1, zipf=False,
                  workload="tiny MoE layer, 32 experts, top-4, hidden 256, FFN 192, batch 1 (L2-resident)"),
 }
@@ -376,7 +376,7 @@ def main():
     w4a4 = bool(cfg.get("w4a4"))
     layer = moe.Layer(E, k, H, I, C, device=local,
                       flags=(moe.CONFIG_MXFP4 if fmt == "mxfp4" else 0) | (moe.CONFIG_W4A4 if w4a4 else 0))
-    grouped = C >= 28 or w4a4                     # the path moe_forward takes
+    grouped = C >= 28                             # the path moe_forward takes
     router_std = synth.ZIPF_ROUTER_STD if cfg["zipf"] else 1.0
     packed, Wr_ds, bias_ds, biases = [], [], [], []
     canon = None
@@ -718,10 +718,9 @@ def main():
             # routed layer per call: C <= 8: fused router, gate/up, down, combine;
             # 9 .. 27 tokens: tiled router + top-k, then 3 decode kernels per group
             # of 8; 28 or more: router, then 7 grouped kernels per pass of 512;
-            # W4A4: router (1 kernel for C <= 8, else 2), then 6 grouped kernels per pass
-            "gpu_launches": args.steps * NL * ((((1 if C <= 8 else 2) + 6 * ((C + 511) // 512)) if w4a4 else
-                                                (4 if C <= 8 else 2 + 3 * ((C + 7) // 8) if C < 28
-                                                 else 2 + 7 * ((C + 511) // 512)))
+            # (W4A4 from 28 tokens: 6 grouped kernels per pass)
+            "gpu_launches": args.steps * NL * ((4 if C <= 8 else 2 + 3 * ((C + 7) // 8) if C < 28
+                                                else 2 + (6 if w4a4 else 7) * ((C + 511) // 512))
                                                # FFN: GEMV A (2), norm (1), GEMV B (2; 3 for C > 4)
                                                + ((5 if C <= 4 else 6) if FFN else 0)),
             "clocks": clocks,

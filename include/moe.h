@@ -96,9 +96,10 @@ typedef enum {
  * quantized value is e2m1 * s * a.  x is quantized per (token, expert) with
  * max(a_gate, a_up) (gate and up read one quantized x); h = silu(g) * u per
  * (token, expert) with a_down; the router weight multiplies the expert's
- * output after the down projection.  Every C takes the grouped tcgen05 path.
- * Results agree with the W4A16 ones only to the activation quantization
- * noise (a few per cent). */
+ * output after the down projection.  Below 28 tokens the decode kernels
+ * quantize x and h in their MMA fragments; from 28 tokens the grouped tcgen05
+ * kernels quantize the gathered rows.  Results agree with the W4A16 ones only
+ * to the activation quantization noise (a few per cent). */
 #define MOE_CONFIG_W4A4 0x4u
 
 typedef struct {
@@ -187,8 +188,8 @@ moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
  *   y[t] = sum_i weights[t][i] * D_e (silu(G_e x[t]) * (U_e x[t])),  e = ids[t][i]
  * (MOE_CONFIG_W4A4: G_e and U_e see x quantised to NVFP4, D_e sees h
  * quantised, as that flag describes).  Below 28 tokens (MXFP4: every C) the
- * decode kernels run groups of 8 tokens; from 28 tokens (W4A4: every C) the
- * grouped tcgen05 kernels run passes of up to 512 tokens expert-major.
+ * decode kernels run groups of 8 tokens; from 28 tokens the grouped tcgen05
+ * kernels run passes of up to 512 tokens expert-major.
  * x: device bf16 bits [C][H]; ids: device int32 [C][k] (any order; each
  * token's ids must be distinct and < E -- offending slots are skipped and
  * flagged; a negative id marks an absent slot, skipped without a flag, which

@@ -67,7 +67,7 @@ constexpr int kDnTilesPerStage = 2;             // down projection: two tiles of
 // (decode groups of at most 2 tokens: their partials are 1/4 of a warp's
 // accumulators, so a stage's reduction slots stay small); MODE 1: down, two
 // tiles per stage.
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool A4>
 __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const GemvArgs a) {
   constexpr bool GU = MODE != 1;
   constexpr bool MX = FMT == kFmtMxfp4;
@@ -106,7 +106,10 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   uint32_t bf[kWarpSteps][2];
   float colinv0 = 1.f, colinv1 = 1.f;           // 2^-s of accumulator columns 2q, 2q+1
   if constexpr (GU) {
-    if (is_consumer) build_x_fragments(a.x, a.C, a.H, ks0, bf, colinv0, colinv1);
+    if (is_consumer) {
+      if constexpr (A4) load_x_raw(a.x, a.C, a.H, ks0, bf);   // quantized once the stage's expert is known
+      else build_x_fragments(a.x, a.C, a.H, ks0, bf, colinv0, colinv1);
+    }
   }
 
   if constexpr (GU) pdl_wait();                  // ids/weights come from the router
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
           cur_d = d;
         }
       }
-      const int npass = GU ? 1 : (ds.nslot[d] + 3) / 4;
+      const int npass = (GU || A4) ? 1 : (ds.nslot[d] + 3) / 4;
       const int eslot = i % S;
       if (!mbar_wait_bounded(&red_full[eslot], (uint32_t)(i / S) & 1u)) {
         atomicOr(a.flags, MOE_FLAG_TIMEOUT);
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
               const int p = ds.pair[d][t];
               const float gg = (c2 ? sum.y : sum.x) * ds.scal[d][0];
               const float uu = (c2 ? sum.w : sum.z) * ds.scal[d][1];
-              const float h = ds.wt[p] * silu(gg) * uu;
+              const float h = (A4 ? 1.f : ds.wt[p]) * silu(gg) * uu;   // W4A4: router weight after down
               hrow[(size_t)p * a.I] = h;
               if (c2) hm1 = fmaxf(hm1, fabsf(h)); else hm0 = fmaxf(hm0, fabsf(h));
             }
@@ -230,10 +233,35 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
                 const int p = ds.pair[d][t];
                 const float gg = (t ? sum.y : sum.x) * ds.scal[d][0];
                 const float uu = (t ? sum.w : sum.z) * ds.scal[d][1];
-                const float h = ds.wt[p] * silu(gg) * uu;
+                const float h = (A4 ? 1.f : ds.wt[p]) * silu(gg) * uu;
                 hrow[(size_t)p * a.I] = h;
                 if (t) hm1 = fmaxf(hm1, fabsf(h)); else hm0 = fmaxf(hm0, fabsf(h));
               }
+            }
+          }
+        } else if constexpr (A4) {
+          // one MMA column per slot: lane q holds slots 2q and 2q+1, rows A
+          // and B; the router weight multiplies the expert's output here
+          const float4 *pr4 = red + (size_t)eslot * a.red_stage_f4 + lane;
+          const float gd = ds.scal[d][2];
+          const int ns = ds.nslot[d];
+#pragma unroll
+          for (int tt = 0; tt < kDnTilesPerStage; tt++) {
+            float4 sum = pr4[(size_t)tt * W * 32];
+            for (int ww = 1; ww < W; ww++) {
+              const float4 v = pr4[(size_t)(tt * W + ww) * 32];
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            const size_t col = 2 * ((tile * kDnTilesPerStage + tt) * 8 + g);
+            if (2 * q < ns) {
+              const int p0 = ds.slot_pair[d][2 * q];
+              *reinterpret_cast<float2 *>(a.ypair + (size_t)p0 * a.H + col) =
+                  make_float2(sum.x * gd * ds.wt[p0], sum.z * gd * ds.wt[p0]);
+            }
+            if (2 * q + 1 < ns) {
+              const int p1 = ds.slot_pair[d][2 * q + 1];
+              *reinterpret_cast<float2 *>(a.ypair + (size_t)p1 * a.H + col) =
+                  make_float2(sum.y * gd * ds.wt[p1], sum.w * gd * ds.wt[p1]);
             }
           }
         } else {
@@ -270,12 +298,28 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
   int d = t0 / a.tiles, tile = t0 - d * a.tiles;
   int item = 0;
   bool ok = true;
+  int xq_d = -1;                                 // W4A4 gate/up: expert rank bf is quantized for
+  float ascale = 1.f;                            // W4A4: that rank's input scale (gate/up) or down scale
   for (int i = 0; i < nstage && ok; i++) {
     const int slot = i % S;
-    const int npass = GU ? 1 : (ds.nslot[d] + 3) / 4;
+    const int npass = (GU || A4) ? 1 : (ds.nslot[d] + 3) / 4;
+    if (A4 && d != xq_d) {   // (A4 is a template constant)
+      // the rank's input scale, loaded before the data wait: gate/up reads x
+      // quantized with max(a_gate, a_up), down h with a_down
+      const float *sc = a.scalars + (size_t)ds.expert[d] * 6;
+      ascale = GU ? fmaxf(__ldg(sc + 1), __ldg(sc + 3)) : __ldg(sc + 5);
+    }
     if (!mbar_wait_bounded(&full_bar[slot], (uint32_t)(i / S) & 1u)) {
       atomicOr(a.flags, MOE_FLAG_TIMEOUT);
       break;
+    }
+    if constexpr (GU) {
+      if (A4 && d != xq_d) {
+        if (xq_d >= 0) load_x_raw(a.x, a.C, a.H, ks0, bf);   // bf holds the previous rank's values
+        quant_x_fragments(bf, ascale);
+        colinv0 = colinv1 = ascale;
+        xq_d = d;
+      }
     }
     // scale units: NVFP4 256 B per half slice (8 rows x 8 k-steps x 2 rows x 2
     // groups), MXFP4 128 B (8 rows x 8 k-step pairs x 2 rows)
@@ -290,8 +334,15 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         const int key = d * 2 + pass;
         if (key != cur_key) {
           cur_key = key;
-          const int sl = 4 * pass + (g >> 1);
-          colinv0 = colinv1 = build_h_fragments(a.hbuf, a.hamax, a.I, ks0, sl < ds.nslot[d] ? ds.slot_pair[d][sl] : -1, bf);
+          if constexpr (A4) {
+            build_h_fragments_a4(a.hbuf, a.I, ks0, g < ds.nslot[d] ? ds.slot_pair[d][g] : -1, ascale, bf);
+            colinv0 = colinv1 = ascale;
+            xq_d = d;
+          } else {
+            const int sl = 4 * pass + (g >> 1);
+            colinv0 = colinv1 =
+                build_h_fragments(a.hbuf, a.hamax, a.I, ks0, sl < ds.nslot[d] ? ds.slot_pair[d][sl] : -1, bf);
+          }
         }
       }
 
@@ -320,9 +371,17 @@ __global__ void __launch_bounds__(kMaxCtaThreads, 1) expert_gemv_kernel(const Ge
         float accA[4], accB[4];
         if constexpr (MX) mma_half_slice_x2_mx(codes, scales, codes + tb, scales + tb, bf, accA, accB);
         else mma_half_slice_x2(codes, scales, codes + tb, scales + tb, bf, accA, accB);
-        float2 *r2 = reinterpret_cast<float2 *>(red + (size_t)rs * red_slot_f4);
-        r2[(size_t)warp * 32 + lane] = make_float2((accA[0] + accA[1]) * colinv0, (accA[2] + accA[3]) * colinv0);
-        r2[(size_t)(W + warp) * 32 + lane] = make_float2((accB[0] + accB[1]) * colinv0, (accB[2] + accB[3]) * colinv0);
+        if constexpr (A4) {
+          // columns 2q, 2q+1 are slots 2q, 2q+1: a partial is one float4 per tile
+          float4 *r4 = red + (size_t)slot * a.red_stage_f4;
+          r4[(size_t)warp * 32 + lane] = make_float4(accA[0] * colinv0, accA[1] * colinv0, accA[2] * colinv0, accA[3] * colinv0);
+          r4[(size_t)(W + warp) * 32 + lane] =
+              make_float4(accB[0] * colinv0, accB[1] * colinv0, accB[2] * colinv0, accB[3] * colinv0);
+        } else {
+          float2 *r2 = reinterpret_cast<float2 *>(red + (size_t)rs * red_slot_f4);
+          r2[(size_t)warp * 32 + lane] = make_float2((accA[0] + accA[1]) * colinv0, (accA[2] + accA[3]) * colinv0);
+          r2[(size_t)(W + warp) * 32 + lane] = make_float2((accB[0] + accB[1]) * colinv0, (accB[2] + accB[3]) * colinv0);
+        }
       }
     }
     __syncwarp();
@@ -341,7 +400,7 @@ void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_
   *smem_bytes = s * (stage_bytes + red_stage_bytes);
 }
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool A4>
 static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -353,35 +412,40 @@ static cudaError_t launch_one(const GemvArgs &a, int grid, bool pdl, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE, FMT>, a);
+  return cudaLaunchKernelEx(&cfg, expert_gemv_kernel<MODE, FMT, A4>, a);
 }
 
-template <int FMT>
+template <int FMT, bool A4>
 static cudaError_t launch_fmt(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
-  return mode == 0 ? launch_one<0, FMT>(a, grid, pdl, stream)
-                   : mode == 2 ? launch_one<2, FMT>(a, grid, pdl, stream) : launch_one<1, FMT>(a, grid, pdl, stream);
+  return mode == 0   ? launch_one<0, FMT, A4>(a, grid, pdl, stream)
+         : mode == 2 ? launch_one<2, FMT, A4>(a, grid, pdl, stream)
+                     : launch_one<1, FMT, A4>(a, grid, pdl, stream);
 }
 
 cudaError_t launch_expert_gemv(int mode, const GemvArgs &a, int grid, bool pdl, cudaStream_t stream) {
-  return a.fmt == kFmtMxfp4 ? launch_fmt<kFmtMxfp4>(mode, a, grid, pdl, stream)
-                            : launch_fmt<kFmtNvfp4>(mode, a, grid, pdl, stream);
+  if (a.fmt == kFmtMxfp4) return launch_fmt<kFmtMxfp4, false>(mode, a, grid, pdl, stream);   // W4A4 is NVFP4 only
+  return a.w4a4 ? launch_fmt<kFmtNvfp4, true>(mode, a, grid, pdl, stream)
+                : launch_fmt<kFmtNvfp4, false>(mode, a, grid, pdl, stream);
 }
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool A4>
 static cudaError_t allow_smem(int smem) {
-  return cudaFuncSetAttribute(expert_gemv_kernel<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return cudaFuncSetAttribute(expert_gemv_kernel<MODE, FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 cudaError_t gemv_setup() {
   // the largest dynamic shared memory any geometry requests (the attribute is
   // per kernel and device, so it must not depend on the layer that sets it)
   const int smem = kGemvSmemBytes;
-  cudaError_t err = allow_smem<0, kFmtNvfp4>(smem);
-  if (err == cudaSuccess) err = allow_smem<1, kFmtNvfp4>(smem);
-  if (err == cudaSuccess) err = allow_smem<2, kFmtNvfp4>(smem);
-  if (err == cudaSuccess) err = allow_smem<0, kFmtMxfp4>(smem);
-  if (err == cudaSuccess) err = allow_smem<1, kFmtMxfp4>(smem);
-  if (err == cudaSuccess) err = allow_smem<2, kFmtMxfp4>(smem);
+  cudaError_t err = allow_smem<0, kFmtNvfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<1, kFmtNvfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<2, kFmtNvfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<0, kFmtMxfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<1, kFmtMxfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<2, kFmtMxfp4, false>(smem);
+  if (err == cudaSuccess) err = allow_smem<0, kFmtNvfp4, true>(smem);
+  if (err == cudaSuccess) err = allow_smem<1, kFmtNvfp4, true>(smem);
+  if (err == cudaSuccess) err = allow_smem<2, kFmtNvfp4, true>(smem);
   return err;
 }
 

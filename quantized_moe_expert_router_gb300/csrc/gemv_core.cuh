@@ -6,6 +6,7 @@
 #pragma once
 
 #include "moe_internal.cuh"
+#include "quant_core.cuh"
 
 namespace moe {
 
@@ -244,6 +245,52 @@ __device__ __forceinline__ void build_x_fragments(const uint16_t *x, int C, int 
     }
   colinv0 = __shfl_sync(kFull, inv, (2 * q) * 4);
   colinv1 = __shfl_sync(kFull, inv, (2 * q + 1) * 4);
+}
+
+// W4A4: the raw bf16 pairs of x for the same fragment positions (quantized
+// per expert by quant_x_fragments once the stage's expert is known).
+__device__ __forceinline__ void load_x_raw(const uint16_t *x, int C, int H, int ks0, uint32_t (&bf)[kWarpSteps][2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const bool tok = g < C;
+  const uint16_t *xr = x + (size_t)(tok ? g : 0) * H;
+#pragma unroll
+  for (int s = 0; s < kWarpSteps; s++) {
+    const int k0 = 16 * (ks0 + s) + 2 * q;
+    uint32_t v0 = 0, v1 = 0;
+    if (tok && k0 < H) {
+      v0 = *reinterpret_cast<const uint32_t *>(xr + k0);
+      v1 = *reinterpret_cast<const uint32_t *>(xr + k0 + 8);
+    }
+    bf[s][0] = v0;
+    bf[s][1] = v1;
+  }
+}
+// W4A4: the raw bf16 fragments of x quantized in place to NVFP4 values
+// e2m1 * e4m3 (f16, exact) with the input scale a; each k-step is one
+// 16-element block, held by the lane quad of the token.
+__device__ __forceinline__ void quant_x_fragments(uint32_t (&bf)[kWarpSteps][2], float a) {
+#pragma unroll
+  for (int s = 0; s < kWarpSteps; s++) {
+    const uint32_t w0 = bf[s][0], w1 = bf[s][1];
+    nvfp4_quant_quad(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 << 16),
+                     __uint_as_float(w1 & 0xFFFF0000u), a, bf[s][0], bf[s][1]);
+  }
+}
+// W4A4 B fragments of h (down): column g = slot g of the expert (pair = that
+// slot's (token, slot) index or -1), h quantized to NVFP4 values with the
+// down input scale a; one MMA column per slot, so 8 slots in one pass.
+__device__ __forceinline__ void build_h_fragments_a4(const float *hbuf, int I, int ks0, int pair, float a,
+                                                     uint32_t (&bf)[kWarpSteps][2]) {
+  const int lane = threadIdx.x & 31, q = lane & 3;
+  const bool have = pair >= 0;
+  const float4 *hr4 = reinterpret_cast<const float4 *>(hbuf + (size_t)(have ? pair : 0) * I) + q;
+#pragma unroll
+  for (int s = 0; s < kWarpSteps; s++) {
+    const int ks = ks0 + s;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (have && 16 * ks < I) v = __ldcg(hr4 + 4 * ks);
+    nvfp4_quant_quad(v.x, v.y, v.z, v.w, a, bf[s][0], bf[s][1]);
+  }
 }
 
 // B fragments of h for a consumer warp's 16 k-steps starting at ks0 (down):

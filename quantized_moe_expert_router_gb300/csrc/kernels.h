@@ -62,6 +62,7 @@ struct GemvArgs {
   int red_stage_f4;          // reduction slots of one stage, in float4
   int smem_bytes;            // dynamic shared memory: ring + reduction slots
   int fmt;                   // kFmtNvfp4 or kFmtMxfp4 (scale unit layout and decode)
+  int w4a4;                  // W4A4: x and h quantized to NVFP4 in the fragments, router weight after down
 };
 // Ring geometry and dynamic shared memory of one kernel.
 void gemv_geometry(int stage_bytes, int red_stage_bytes, int *stages, int *smem_bytes);

@@ -101,7 +101,6 @@ moe_status moe_layer_create(const moe_config *cfg, int device, moe_layer_t *out)
   // when an expert has one or two tokens: measured with uniform routing at
   // 896 experts, top-16, the two paths meet between 24 and 32 tokens
   L->grouped_min_tokens = (c.flags & MOE_CONFIG_GROUPED_ABOVE_8) ? moe::kGemvTokens + 1 : moe::kGroupedMinTokens;
-  if (L->w4a4) L->grouped_min_tokens = 1;    // the W4A4 rows exist on the grouped path only
   if (moe::gemv_setup() != cudaSuccess) {
     delete L;
     return MOE_ERR_CUDA;
@@ -233,11 +232,12 @@ moe_status forward_impl(moe_layer_t L, const uint16_t *x, int C, const int32_t *
   a.k = k; a.E = L->cfg.num_experts; a.H = H; a.I = I;
   a.expert_bytes = L->expert_bytes;
   a.fmt = L->fmt;
+  a.w4a4 = L->w4a4;
 
   cudaError_t err = cudaSuccess;
   if (L->stage_events_on) err = cudaEventRecord(L->stage_events[0], stream);
-  // C >= grouped_min_tokens: the grouped tcgen05 path (NVFP4; every C for
-  // W4A4); MXFP4 layers run every C on the decode kernels, in groups of 8
+  // C >= grouped_min_tokens: the grouped tcgen05 path (NVFP4); MXFP4 layers
+  // run every C on the decode kernels, in groups of 8
   if (C >= L->grouped_min_tokens && L->fmt == moe::kFmtNvfp4) {
     // expert-major passes of up to kGroupTokens tokens
     moe::GroupArgs g = {};

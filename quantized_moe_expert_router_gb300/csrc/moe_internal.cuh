@@ -69,7 +69,7 @@ struct WsLayout {
 struct moe_layer {
   moe_config cfg;
   int fmt;                    // kFmtNvfp4 or kFmtMxfp4 (MOE_CONFIG_MXFP4)
-  int w4a4;                   // MOE_CONFIG_W4A4: activations quantized to NVFP4, grouped path for every C
+  int w4a4;                   // MOE_CONFIG_W4A4: activations quantized to NVFP4 (decode and grouped paths)
   int device;
   int num_sms;
   int Hp, Ip;                 // K of gate/up and of down, padded to kKAlign
@@ -104,7 +104,7 @@ inline WsLayout ws_layout(const moe_layer &L, int C) {
   w.hbuf = take(sizeof(float) * pairs * I);
   w.hamax = take(sizeof(uint32_t) * pairs);
   w.ypair = take(sizeof(float) * pairs * H);
-  if (C > kGemvTokens || L.w4a4) {
+  if (C > kGemvTokens) {
     const size_t Cg = C < kGroupTokens ? C : kGroupTokens, Pg = Cg * k;
     w.glogits = take(sizeof(float) * kRouteSplits * (size_t)C * E);
     w.gd = take(sizeof(int) * (16 + E + (E + 1) + Pg));

@@ -26,6 +26,30 @@
 
 namespace moe {
 
+// The block scale from the block's largest magnitude: returns the e4m3 byte,
+// writes its value (f16, exact) and m = value * a (fp32), the divisor of the
+// elements.
+__device__ __forceinline__ uint8_t nvfp4_block_scale(float amax, float a, __half &sh, float &m) {
+  const float denom = 6.0f * a;
+  const float t = __fdiv_rn(amax, denom);
+  const uint8_t sb = (uint8_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+  sh = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3));
+  m = __fmul_rn(__half2float(sh), a);
+  return sb;
+}
+
+// One element: its e2m1 code and the value e2m1 * e4m3 (f16, exact); a zero
+// block scale gives code 0.
+__device__ __forceinline__ uint32_t nvfp4_element(float v, float m, __half sh, __half &val) {
+  uint32_t c = 0u;
+  val = __float2half_rn(0.f);
+  if (__half2float(sh) > 0.f) {
+    c = (uint32_t)__nv_cvt_float_to_fp4(__fdiv_rn(v, m), __NV_E2M1, cudaRoundNearest) & 0xFu;
+    val = __hmul(__half(__nv_cvt_fp4_to_halfraw((__nv_fp4_storage_t)c, __NV_E2M1)), sh);
+  }
+  return c;
+}
+
 // Quantizes v[16] with input scale a: returns the e4m3 scale byte, writes the
 // 16 codes (low nibble = even element, elements 0..7 in codes[0]) and the 16
 // values e2m1 * e4m3 as f16 pairs (vals[j] = elements 2j, 2j+1; low half =
@@ -35,30 +59,43 @@ __device__ __forceinline__ uint8_t nvfp4_quant_block(const float (&v)[16], float
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(v[i]));
-  const float denom = 6.0f * a;
-  const float t = __fdiv_rn(amax, denom);
-  const uint8_t sb = (uint8_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
-  const __half sh = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3));
-  const float sv = __half2float(sh);
-  const float m = __fmul_rn(sv, a);
+  __half sh;
+  float m;
+  const uint8_t sb = nvfp4_block_scale(amax, a, sh, m);
   codes[0] = codes[1] = 0u;
 #pragma unroll
   for (int j = 0; j < 8; j++) {
-    uint32_t c2[2] = {0u, 0u};
-    __half h2[2] = {__float2half_rn(0.f), __float2half_rn(0.f)};
-#pragma unroll
-    for (int b = 0; b < 2; b++) {
-      if (sv > 0.f) {
-        const uint32_t c = (uint32_t)__nv_cvt_float_to_fp4(__fdiv_rn(v[2 * j + b], m), __NV_E2M1, cudaRoundNearest) & 0xFu;
-        c2[b] = c;
-        h2[b] = __hmul(__half(__nv_cvt_fp4_to_halfraw((__nv_fp4_storage_t)c, __NV_E2M1)), sh);
-      }
-    }
-    codes[j >> 2] |= (c2[0] | (c2[1] << 4)) << (8 * (j & 3));
-    const __half2 hv = __halves2half2(h2[0], h2[1]);
+    __half h0, h1;
+    const uint32_t c0 = nvfp4_element(v[2 * j], m, sh, h0);
+    const uint32_t c1 = nvfp4_element(v[2 * j + 1], m, sh, h1);
+    codes[j >> 2] |= (c0 | (c1 << 4)) << (8 * (j & 3));
+    const __half2 hv = __halves2half2(h0, h1);
     vals[j] = *reinterpret_cast<const uint32_t *>(&hv);
   }
   return sb;
+}
+
+// The same quantization spread over the four lanes q = 0..3 of an MMA
+// fragment quad: this lane holds elements 2q, 2q+1 (v0, v1) and 2q+8, 2q+9
+// (v2, v3) of a 16-element block, the quad together the whole block.  Writes
+// this lane's four values as two f16 pairs (the B fragment registers).  All
+// 32 lanes of the warp must call it.
+__device__ __forceinline__ void nvfp4_quant_quad(float v0, float v1, float v2, float v3, float a, uint32_t &b0,
+                                                 uint32_t &b1) {
+  float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  __half sh;
+  float m;
+  nvfp4_block_scale(amax, a, sh, m);
+  __half h0, h1, h2, h3;
+  nvfp4_element(v0, m, sh, h0);
+  nvfp4_element(v1, m, sh, h1);
+  nvfp4_element(v2, m, sh, h2);
+  nvfp4_element(v3, m, sh, h3);
+  const __half2 p0 = __halves2half2(h0, h1), p1 = __halves2half2(h2, h3);
+  b0 = *reinterpret_cast<const uint32_t *>(&p0);
+  b1 = *reinterpret_cast<const uint32_t *>(&p1);
 }
 
 }  // namespace moe

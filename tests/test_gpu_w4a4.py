@@ -1,8 +1,9 @@
 """GPU parity of the W4A4 numerics (MOE_CONFIG_W4A4): the activation
-quantizer bit for bit against the oracle's, and the routed layer on the
-grouped tcgen05 path against the oracle's W4A4 mode within the acceptance
-tolerance plus the W4A4 allowance of ``helpers`` (rounding-tie decisions on
-h that fp32 accumulation noise can move)."""
+quantizer bit for bit against the oracle's, and the routed layer (the decode
+kernels below 28 tokens, the grouped tcgen05 path from 28) against the
+oracle's W4A4 mode within the acceptance tolerance plus the W4A4 allowance of
+``helpers`` (rounding-tie decisions on h that fp32 accumulation noise can
+move)."""
 import numpy as np
 import pytest
 import torch
@@ -148,8 +149,9 @@ class W4A4Layer:
         return err, n_amb
 
 
-@pytest.mark.parametrize("C", [1, 7, 40])
+@pytest.mark.parametrize("C", [1, 7, 12, 40])
 def test_w4a4_parity_small(C):
+    # C < 28: the decode kernels (12: two groups of at most 8); 40: the grouped path
     L = W4A4Layer(64, 8, 1024, 768, 64, seed=3)
     x = gapped_tokens(3, 0, C, 1024, L.Wr, 8)
     L.check(x, f"w4a4 E64 C={C}")
