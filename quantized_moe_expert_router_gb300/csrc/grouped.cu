@@ -416,8 +416,13 @@ struct TcSmem {
 struct TcUnit {
   int d, mt, nc;
 };
+// Units are ordered m-tile pair first, then expert, then column chunk: the
+// CTAs' contiguous ranges then cover every m-tile pair of an expert at about
+// the same time (an expert's B rows, which all its m-tile pairs read, are
+// fetched from DRAM once and then hit L2), while consecutive chunks of one
+// m-tile pair stay together in a CTA (its weights are re-read from L2).
 __device__ __forceinline__ bool unit_before(const TcUnit &u, const TcUnit &e) {
-  return u.d != e.d ? u.d < e.d : (u.mt != e.mt ? u.mt < e.mt : u.nc < e.nc);
+  return u.mt != e.mt ? u.mt < e.mt : (u.d != e.d ? u.d < e.d : u.nc < e.nc);
 }
 __device__ __forceinline__ int unit_nch(const TcSmem &s, int d, int cols) {
   return (s.off[d + 1] - s.off[d] + cols - 1) / cols;
@@ -425,9 +430,9 @@ __device__ __forceinline__ int unit_nch(const TcSmem &s, int d, int cols) {
 __device__ __forceinline__ void unit_next(const TcSmem &s, TcUnit &u, int MT, int cols) {
   if (++u.nc == unit_nch(s, u.d, cols)) {
     u.nc = 0;
-    if (++u.mt == MT) {
-      u.mt = 0;
-      u.d++;
+    if (++u.d == s.n) {
+      u.d = 0;
+      u.mt++;
     }
   }
 }
@@ -439,29 +444,31 @@ __device__ __forceinline__ int mtile_cost(int cnt, int cols, int rf, int &cfull)
   cfull = unit_cost(cols * rf);
   return (nch - 1) * cfull + unit_cost((cnt - (nch - 1) * cols) * rf);
 }
-// First unit whose work start is >= c.
+// First unit whose work start is >= c; pre[d] is the work of the m-tile
+// pairs of experts 0..d-1 in one m-tile row, pre[n] that of a whole row.
 __device__ __forceinline__ TcUnit unit_at(const TcSmem &s, int MT, int cols, int rf, long long c) {
-  int lo = 0, hi = s.n;                            // largest d with pre[d] <= c
+  const long long row = s.pre[s.n];
+  TcUnit u = {0, MT, 0};
+  if (row <= 0) return u;                          // no units
+  u.mt = (int)(c / row);
+  if (u.mt >= MT) return u;
+  const int r = (int)(c - (long long)u.mt * row);
+  int lo = 0, hi = s.n - 1;                        // largest d with pre[d] <= r
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s.pre[mid] <= c) lo = mid; else hi = mid - 1;
+    if (s.pre[mid] <= r) lo = mid; else hi = mid - 1;
   }
-  TcUnit u = {lo, 0, 0};
-  if (lo >= s.n) return u;
+  u.d = lo;
   const int cnt = s.off[lo + 1] - s.off[lo], nch = (cnt + cols - 1) / cols;
   int cf;
-  const int cmt = mtile_cost(cnt, cols, rf, cf);
-  const int r = (int)(c - s.pre[lo]);
-  u.mt = r / cmt;
-  const int rr = r - u.mt * cmt;
-  u.nc = (rr + cf - 1) / cf;
+  mtile_cost(cnt, cols, rf, cf);
+  u.nc = (r - s.pre[lo] + cf - 1) / cf;
   if (u.nc >= nch) {
     u.nc = 0;
-    u.mt++;
-  }
-  if (u.mt >= MT) {
-    u.mt = 0;
-    u.d++;
+    if (++u.d == s.n) {
+      u.d = 0;
+      u.mt++;
+    }
   }
   return u;
 }
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         const int o = a.gd[16 + E + d], o1 = a.gd[17 + E + d];
         s.off[d] = o;
         int cf;
-        cost = MP * mtile_cost(o1 - o, cols, rf, cf);
+        cost = mtile_cost(o1 - o, cols, rf, cf);    // one m-tile pair of the expert
       }
       int t1;
       const int pre = cta_scan_excl(cost, s.wsum, t1) + run;
@@ -625,7 +632,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
     }
     __syncthreads();
     if (tid == 0) {
-      const long long total = s.pre[n];
+      const long long total = (long long)MP * s.pre[n];
       const TcUnit u0 = unit_at(s, MP, cols, rf, total * blockIdx.x / gridDim.x);
       const TcUnit u1 = unit_at(s, MP, cols, rf, total * (blockIdx.x + 1) / gridDim.x);
       s.range[0] = u0.d; s.range[1] = u0.mt; s.range[2] = u0.nc;
