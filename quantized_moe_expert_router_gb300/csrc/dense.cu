@@ -13,7 +13,10 @@
 // pair rows (2p, 2p+1) for a plain matrix, (gate row p, up row p) for a
 // shared expert's gate/up.  A GEMV runs in two kernels:
 //   dense_partial_kernel  one warp per unit (tile of 16 rows, 512-element
-//                         K-slice): the unit's code and scale bytes come
+//                         K-slice; units slice-major, an equal contiguous
+//                         range per CTA, so a CTA builds the B fragments of
+//                         only the one or two slices it covers): the unit's
+//                         code and scale bytes come
 //                         straight from global memory into registers (all
 //                         twelve 16-byte loads of a lane in flight at once),
 //                         the B operand (the C <= 8 input vectors as f16,
@@ -71,13 +74,20 @@ __global__ void pack_dense_kernel(const PackDenseArgs a) {
 // four tokens; bf16: one)
 template <int FMT, bool XF32, int NP>
 __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(const DenseArgs a) {
-  extern __shared__ uint2 frag[];                // [npass][KS][32 lanes]: B fragments of every k-step
+  extern __shared__ uint2 frag[];                // [npass][KSL][32 lanes]: B fragments of this CTA's k-steps
   __shared__ float s_inv[kGemvTokens];           // 2^-s of each token's f16 scale
   __shared__ float s_max[kDenseWarps][kGemvTokens];
   constexpr bool MX = FMT == kFmtMxfp4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-  const int NWL = a.w1 - a.w0, KS = 32 * NWL;    // this launch's slices and k-steps
-  const int kbase = 512 * a.w0;                  // first element of its K range
+  const int NWL = a.w1 - a.w0;                   // this launch's slices
+  // units slice-major (u = slice * tiles + tile): this CTA's contiguous range
+  // spans one or two slices
+  const int units = a.tiles * NWL;
+  const int u0 = split_point(units, blockIdx.x, gridDim.x), u1 = split_point(units, blockIdx.x + 1, gridDim.x);
+  if (u0 >= u1) return;
+  const int wf = u0 / a.tiles, nsl = (u1 - 1) / a.tiles - wf + 1;
+  const int KSL = 32 * nsl;                      // k-steps of the CTA's slices
+  const int kbase = 512 * (a.w0 + wf);           // first element of their K range
   constexpr int npass = NP;
   const uint16_t *xb = static_cast<const uint16_t *>(a.x);
   const float *xf = static_cast<const float *>(a.x);
@@ -85,11 +95,26 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
     if (k >= a.K) return 0.f;
     return XF32 ? __ldg(xf + (size_t)t * a.K + k) : __uint_as_float((uint32_t)__ldg(xb + (size_t)t * a.K + k) << 16);
   };
-  // per-token max |x| over the whole K (fixed reduction tree): every launch of
-  // one GEMV scales a token alike
+  // per-token max |x| over the whole K (fixed reduction tree): every CTA and
+  // every launch of one GEMV scale a token alike; 16-byte loads (K % 64 == 0)
   for (int t = 0; t < a.C; t++) {
     float m = 0.f;
-    for (int k = tid; k < a.K; k += blockDim.x) m = fmaxf(m, fabsf(xval(t, k)));
+    if constexpr (XF32) {
+      const float4 *r = reinterpret_cast<const float4 *>(xf + (size_t)t * a.K);
+      for (int j = tid; j < a.K / 4; j += blockDim.x) {
+        const float4 v = __ldg(r + j);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+    } else {
+      const uint4 *r = reinterpret_cast<const uint4 *>(xb + (size_t)t * a.K);
+      for (int j = tid; j < a.K / 8; j += blockDim.x) {
+        const uint4 v = __ldg(r + j);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[e] << 16)), fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
     if (lane == 0) s_max[warp][t] = m;
@@ -106,8 +131,8 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
   // B fragments: lane (g, q) of k-step ks holds elements 16 ks + 2q, +1 and
   // 16 ks + 2q + 8, +9 of column g: token g (bf16 input), or the hi (g even)
   // / lo (g odd) part of token 4 pass + g / 2 (fp32 input)
-  for (int i = tid; i < npass * KS * 32; i += blockDim.x) {
-    const int l = i & 31, ks = (i >> 5) % KS, pass = (i >> 5) / KS;
+  for (int i = tid; i < npass * KSL * 32; i += blockDim.x) {
+    const int l = i & 31, ks = (i >> 5) % KSL, pass = (i >> 5) / KSL;
     const int gg = l >> 2, qq = l & 3;
     const int t = XF32 ? 4 * pass + (gg >> 1) : gg;
     uint2 v = make_uint2(0u, 0u);
@@ -134,11 +159,9 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
     cinv[pass][0] = t0 < a.C ? s_inv[t0] : 0.f;
     cinv[pass][1] = t1 < a.C ? s_inv[t1] : 0.f;
   }
-  const int units = a.tiles * NWL;
-  const int nw = gridDim.x * kDenseWarps;
   const uint64_t pol = l2_evict_first_policy();
-  for (int u = blockIdx.x * kDenseWarps + warp; u < units; u += nw) {
-    const int tile = u / NWL, wl = u - tile * NWL, w = a.w0 + wl;
+  for (int u = u0 + warp; u < u1; u += kDenseWarps) {
+    const int wl = u / a.tiles, tile = u - wl * a.tiles, w = a.w0 + wl;
     const uint8_t *base = a.w + (size_t)tile * a.tile_bytes;
     uint4 cw[8], sc[4];
 #pragma unroll
@@ -153,7 +176,7 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
         sc[q8] = ld_stream_v4(base + (size_t)a.W * 4096 + (size_t)w * 512 + ((size_t)q8 * 8 + g) * 16, pol);
     }
     float acc[NP][2][4] = {};                    // [pass][chain][fragment]
-    const uint2 *fr = frag + (size_t)(32 * wl) * 32 + lane;
+    const uint2 *fr = frag + (size_t)(32 * (wl - wf)) * 32 + lane;
     if constexpr (MX) {
 #pragma unroll
       for (int P = 0; P < 16; P++) {             // k-step pairs 2P, 2P + 1
@@ -164,7 +187,7 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
         const uint32_t sab = (wi == 0 ? s4.x : wi == 1 ? s4.y : wi == 2 ? s4.z : s4.w) >> (16 * (P & 1));
 #pragma unroll
         for (int pass = 0; pass < npass; pass++) {
-          const uint2 b0 = fr[(size_t)(pass * KS + 2 * P) * 32], b1 = fr[(size_t)(pass * KS + 2 * P + 1) * 32];
+          const uint2 b0 = fr[(size_t)(pass * KSL + 2 * P) * 32], b1 = fr[(size_t)(pass * KSL + 2 * P + 1) * 32];
           const uint32_t bb0[2] = {b0.x, b0.y}, bb1[2] = {b1.x, b1.y};
           mx_pair_step(w0, w1, bb0, bb1, sab, acc[pass][P & 1]);
         }
@@ -187,7 +210,7 @@ __global__ void __launch_bounds__(32 * kDenseWarps, 1) dense_partial_kernel(cons
         A[3] = hmul2_hi(A[3], s2);
 #pragma unroll
         for (int pass = 0; pass < npass; pass++) {
-          const uint2 b = fr[(size_t)(pass * KS + s) * 32];
+          const uint2 b = fr[(size_t)(pass * KSL + s) * 32];
           mma16816(acc[pass][s & 1], A, b.x, b.y);
         }
       }
@@ -217,23 +240,34 @@ __global__ void dense_finish_kernel(const DenseFinishArgs a) {
   const int pass = a.xf32 ? t >> 2 : 0, q = a.xf32 ? (t & 3) : (t >> 1), c = a.xf32 ? 0 : (t & 1);
   const int lane = 4 * g + q;
   float sa = 0.f, sb = 0.f;
-  for (int w = 0; w < a.W; w++) {
-    const float4 v = reinterpret_cast<const float4 *>(a.part)[((size_t)(tile * a.W + w) * npass + pass) * 32 + lane];
-    float va, vb;
-    if (a.xf32) {                                // hi + lo columns of the token
-      va = v.x + v.y;
-      vb = v.z + v.w;
-    } else {
-      va = c ? v.y : v.x;
-      vb = c ? v.w : v.z;
+  // the slices' partials in batches whose loads are all in flight together,
+  // then added in slice order
+  constexpr int kBatch = 8;
+  const float4 *pp = reinterpret_cast<const float4 *>(a.part) + ((size_t)tile * a.W * npass + pass) * 32 + lane;
+  for (int w0 = 0; w0 < a.W; w0 += kBatch) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; j++)
+      v[j] = w0 + j < a.W ? __ldcg(pp + (size_t)(w0 + j) * npass * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kBatch; j++) {
+      if (w0 + j >= a.W) break;
+      float va, vb;
+      if (a.xf32) {                              // hi + lo columns of the token
+        va = v[j].x + v[j].y;
+        vb = v[j].z + v[j].w;
+      } else {
+        va = c ? v[j].y : v[j].x;
+        vb = c ? v[j].w : v[j].z;
+      }
+      if (a.slice_scale) {
+        const float ss = a.slice_scale[w0 + j];
+        va *= ss;
+        vb *= ss;
+      }
+      sa += va;
+      sb += vb;
     }
-    if (a.slice_scale) {
-      const float ss = a.slice_scale[w];
-      va *= ss;
-      vb *= ss;
-    }
-    sa += va;
-    sb += vb;
   }
   int si = 0;
   while (si + 1 < a.nseg && tile >= a.seg[si].tile1) si++;
@@ -310,20 +344,36 @@ static cudaError_t launch_partial_fmt(const DenseArgs &a, int grid, size_t smem,
   return a.C <= 4 ? launch_partial<FMT, true, 1>(a, grid, smem, stream) : launch_partial<FMT, true, 2>(a, grid, smem, stream);
 }
 
+// Grid of a launch over `slices` slices and the most slices one CTA's
+// contiguous unit range spans (ceil(range / tiles) + 1).
+static void partial_grid(int tiles, int slices, int num_sms, int *grid, int *span) {
+  const int units = tiles * slices;
+  int g = (units + kDenseWarps - 1) / kDenseWarps;
+  if (g > num_sms) g = num_sms;
+  const int per_cta = (units + g - 1) / g;
+  int sp = (per_cta + tiles - 1) / tiles + 1;
+  if (sp > slices) sp = slices;
+  *grid = g;
+  *span = sp;
+}
+
 cudaError_t launch_dense_gemv(const DenseArgs &a0, const DenseFinishArgs &f, int num_sms, cudaStream_t stream) {
   if (a0.C < 1 || a0.C > kGemvTokens || f.nseg < 1 || f.nseg > kMaxDenseSegs) return cudaErrorInvalidValue;
-  // slices per launch: as many as the B fragments of shared memory hold
-  int per = a0.W;
-  while (per > 1 && frag_bytes(per, a0.C, a0.xf32 != 0) > (size_t)kDenseSmemBytes) per = (per + 1) / 2;
+  // slices per launch: as many as keep the B fragments of the slices one CTA
+  // spans within shared memory (normally all of them in one launch)
+  int per = a0.W, grid = 1, span = 1;
+  for (;;) {
+    partial_grid(a0.tiles, per, num_sms, &grid, &span);
+    if (per == 1 || frag_bytes(span, a0.C, a0.xf32 != 0) <= (size_t)kDenseSmemBytes) break;
+    per = (per + 1) / 2;
+  }
   cudaError_t err = cudaSuccess;
   for (int w0 = 0; w0 < a0.W && err == cudaSuccess; w0 += per) {
     DenseArgs a = a0;
     a.w0 = w0;
     a.w1 = w0 + per < a0.W ? w0 + per : a0.W;
-    const size_t smem = frag_bytes(a.w1 - a.w0, a.C, a.xf32 != 0);
-    const int units = a.tiles * (a.w1 - a.w0);
-    int grid = (units + kDenseWarps - 1) / kDenseWarps;
-    if (grid > num_sms) grid = num_sms;
+    partial_grid(a.tiles, a.w1 - a.w0, num_sms, &grid, &span);
+    const size_t smem = frag_bytes(span, a.C, a.xf32 != 0);
     err = a.fmt == kFmtMxfp4 ? launch_partial_fmt<kFmtMxfp4>(a, grid, smem, stream)
                              : launch_partial_fmt<kFmtNvfp4>(a, grid, smem, stream);
   }
