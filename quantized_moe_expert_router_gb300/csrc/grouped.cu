@@ -403,7 +403,7 @@ struct TcSmem {
   uint64_t drain[kTcIssuers];
   uint32_t tmem_base;
   int n;
-  int verdict;                  // epilogue: the D wait succeeded
+  int d_ok;                     // epilogue: the D wait succeeded
   int range[6];                 // first unit (d, mt, nc) of this CTA and the end
   int wsum[33];
   int colp[kTcBRows];           // epilogue: pair of each column of the unit
@@ -850,9 +850,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) group_tc_kernel(const __grid_co
         }
       }
       const int db = ud & 1;
-      if (et == 0) s.verdict = mbar_wait_bounded(&s.d_full[db], (uint32_t)(ud >> 1) & 1u) ? 1 : 0;
+      if (et == 0) s.d_ok = mbar_wait_bounded(&s.d_full[db], (uint32_t)(ud >> 1) & 1u) ? 1 : 0;
       epi_sync();
-      if (!s.verdict) {
+      if (!s.d_ok) {
         if (et == 0) atomicOr(a.flags, MOE_FLAG_TIMEOUT);
         break;
       }

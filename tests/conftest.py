@@ -10,7 +10,7 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size case, minutes on the GPU box")
+    config.addinivalue_line("markers", "slow: full-size case, minutes on a GB300")
 
 
 def pytest_collection_modifyitems(config, items):
