@@ -176,7 +176,8 @@ moe_status moe_pack_weights(moe_layer_t layer, const moe_canonical_weights *cano
  * Failure: if a router block's bounded wait for its weight rows runs out
  * (C <= 8), MOE_FLAG_TIMEOUT is raised and every id of the call is written as
  * -1 (weight 0), which moe_forward treats as an absent slot; the workspace
- * stays usable for the next call. */
+ * stays usable for the next call.  A token whose logits include a NaN (from a
+ * NaN in x, w_router or bias) selects nothing in the same way. */
 moe_status moe_route(moe_layer_t layer, const uint16_t *x, int num_tokens,
                      const float *w_router, const float *bias, int32_t *ids,
                      float *weights, void *ws, size_t ws_bytes, cudaStream_t stream);

@@ -141,6 +141,42 @@ __device__ __forceinline__ int operand_order(int k) {
 __device__ __forceinline__ void build_dispatch(DispatchSmem &s, const int32_t *ids, const float *weights, int C, int k,
                                                int E, int32_t *flags) {
   const int tid = threadIdx.x, nt = blockDim.x, P = C * k;
+  if (C == 1) {
+    // one token: warp 0 alone, slot i in lane i (k <= 32); the same tables
+    // as below with one CTA barrier instead of five
+    if (tid < 32) {
+      int e = -1;
+      if (tid < k) {
+        e = ids[tid];
+        s.ids[tid] = e;
+        s.wt[tid] = weights[tid];
+      }
+      const bool inr = tid < k && (unsigned)e < (unsigned)E;
+      if (tid < k && e >= E) atomicOr(flags, MOE_FLAG_BAD_EXPERT_ID);
+      bool first = inr;                          // the lowest slot holding this id
+      for (int j = 0; j < k; j++) {
+        const int ej = __shfl_sync(kFull, e, j);
+        if (j < tid && ej == e) first = false;
+      }
+      if (inr && !first) atomicOr(flags, MOE_FLAG_DUPLICATE_ID);
+      const uint32_t fm = __ballot_sync(kFull, first);
+      int r = 0;                                 // rank by ascending expert id
+      for (int j = 0; j < k; j++) {
+        const int ej = __shfl_sync(kFull, e, j);
+        r += ((fm >> j) & 1u) && ej < e;
+      }
+      if (first) {
+        s.expert[r] = (int16_t)e;
+        s.tokmask[r] = 1u;
+        s.pair[r][0] = tid;
+        s.slot_pair[r][0] = (int16_t)tid;
+        s.nslot[r] = 1;
+      }
+      if (tid == 0) s.n = __popc(fm);
+    }
+    __syncthreads();
+    return;
+  }
   for (int p = tid; p < P; p += nt) {
     s.ids[p] = ids[p];
     s.wt[p] = weights[p];

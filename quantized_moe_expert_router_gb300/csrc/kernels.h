@@ -25,7 +25,6 @@ struct RouteArgs {
   float *weights;        // [C][k]
   float *logits;         // workspace [C][E]
   uint32_t *ticket;      // workspace counter (0 between calls)
-  uint32_t *timeouts;    // workspace counter of router CTAs whose wait ran out (0 between calls)
   int32_t *flags;        // workspace flag word (MOE_FLAG_TIMEOUT)
   int C, E, H, k;
   uint32_t stall_tx;     // test hook: extra bytes every CTA waits for and no copy delivers (0 = off)

@@ -183,7 +183,6 @@ moe_status moe_route(moe_layer_t L, const uint16_t *x, int C, const float *w_rou
   a.x = x; a.w_router = w_router; a.bias = bias; a.ids = ids; a.weights = weights;
   a.logits = reinterpret_cast<float *>(w + (C <= moe::kGemvTokens ? wl.logits : wl.glogits));
   a.ticket = &reinterpret_cast<moe::WsControl *>(w)->route_ticket;
-  a.timeouts = &reinterpret_cast<moe::WsControl *>(w)->route_timeouts;
   a.flags = &reinterpret_cast<moe::WsControl *>(w)->flags;
   a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
   moe::route_wait_policy(L->cfg.flags, &a);
@@ -340,9 +339,9 @@ moe_status moe_get_device_status(moe_layer_t L, void *ws, cudaStream_t stream, i
   moe::WsControl *ctl = static_cast<moe::WsControl *>(ws);
   cudaError_t err = cudaStreamSynchronize(stream);
   if (err == cudaSuccess) err = cudaMemcpy(flags, &ctl->flags, sizeof(int32_t), cudaMemcpyDeviceToHost);
-  // flags, router ticket and router failure count back to zero: a router grid
-  // that stopped early leaves the workspace as good as new
-  static_assert(offsetof(moe::WsControl, route_timeouts) == 8, "control words 0..11");
+  // flags and router ticket (and the reserved word) back to zero: a router
+  // grid that stopped early leaves the workspace as good as new
+  static_assert(offsetof(moe::WsControl, reserved) == 8, "control words 0..11");
   if (err == cudaSuccess) err = cudaMemsetAsync(ctl, 0, 12, stream);
   if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
   return cuda_status(err);

@@ -35,7 +35,7 @@ constexpr int kDenseSmemBytes = 204800;  // B fragments of a dense GEMV: passes 
 struct WsControl {
   int32_t flags;          // MOE_FLAG_* bits, cleared by moe_get_device_status
   uint32_t route_ticket;  // CTAs of the router that finished their logits
-  uint32_t route_timeouts;  // router CTAs of the current call whose wait ran out
+  uint32_t reserved;       // zero
   uint32_t pad[61];
 };
 static_assert(sizeof(WsControl) == 256, "control block is 256 bytes");

@@ -8,12 +8,14 @@
 // (a softmax over all experts renormalised over the kept ones; the full
 // softmax denominator cancels).  ids are written in ascending expert order.
 //
-// Small C (decode): one kernel.  Each warp owns whole router rows and streams
-// them once with 16-byte loads (a whole row in flight per warp) against x held
-// in shared memory; every CTA then takes a ticket, and the last CTA to finish
-// runs the top-k of each token with all its warps (the ticket is reset for
-// the next call).  No CTA ever waits for another.  Large C: a tiled fp32
-// logits kernel and a top-k kernel with one CTA per token.
+// Small C (decode): one kernel.  Each CTA streams a contiguous range of
+// router rows into shared memory with bulk copies, and each warp multiplies
+// its rows by x (fp32, in shared memory) as soon as they are in.  Every CTA
+// then takes a ticket, and the last CTA to finish runs the top-k of each
+// token with all its warps (the ticket is reset for the next call).  No CTA
+// ever waits for another.  A CTA whose rows do not arrive marks its logits
+// NaN, which makes every token select nothing.  Large C: a tiled fp32 logits
+// kernel and a top-k kernel with one CTA per token.
 #include "moe_internal.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   extern __shared__ __align__(128) float4 xs4[];   // [CT][H/4] then [rows][H/4]
   __shared__ int s_last;
   __shared__ SelectSmem tk;
-  __shared__ __align__(8) uint64_t rows_bar;
+  __shared__ __align__(8) uint64_t rows_bar[kRouteWarps];   // round row r arrives on rows_bar[r % 8]
   pdl_wait();
   pdl_launch_dependents();                 // the expert kernel may start its prologue
   const int H4 = a.H / 4;
@@ -61,11 +63,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   float4 *rows4 = xs4 + (size_t)CT * H4;
   const int max_rows = (kRouteSmemBytes - CT * a.H * (int)sizeof(float)) / (a.H * (int)sizeof(float));
   // this CTA's router rows: a contiguous range, streamed into shared memory
-  // with bulk copies in rounds of at most max_rows rows
+  // with bulk copies in rounds of at most max_rows rows; warp w takes rows
+  // w, w + 8, ... of a round as soon as they are in (its own barrier)
   const int r0 = split_point(a.E, blockIdx.x, gridDim.x), r1 = split_point(a.E, blockIdx.x + 1, gridDim.x);
   const uint64_t pol = l2_evict_first_policy();
   if (threadIdx.x == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rows_bar)) : "memory");
+    for (int w = 0; w < kRouteWarps; w++)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rows_bar[w])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -74,14 +78,19 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
   for (int rb = r0; rb < r1; rb += max_rows, round++) {
     const int nr = (r1 - rb) < max_rows ? (r1 - rb) : max_rows;
     if (threadIdx.x == 0) {
-      // (a.stall_tx: test hook, bytes that no copy delivers, so the wait below runs out)
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rows_bar)),
-                   "r"((uint32_t)(nr * row_bytes) + (round == 0 ? a.stall_tx : 0u)) : "memory");
+      // every barrier completes one phase per round (a warp without rows
+      // expects 0 bytes); (a.stall_tx: test hook, bytes that no copy
+      // delivers, so the waits below run out)
+      for (int w = 0; w < kRouteWarps; w++) {
+        const uint32_t nw = nr > w ? (uint32_t)((nr - 1 - w) / kRouteWarps + 1) : 0u;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rows_bar[w])),
+                     "r"(nw * (uint32_t)row_bytes + (round == 0 && w == 0 ? a.stall_tx : 0u)) : "memory");
+      }
       for (int r = 0; r < nr; r++)
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
             ::"r"(smem_addr(rows4 + (size_t)r * H4)), "l"(a.w_router + (size_t)(rb + r) * a.H),
-            "r"((uint32_t)row_bytes), "r"(smem_addr(&rows_bar)), "l"(pol) : "memory");
+            "r"((uint32_t)row_bytes), "r"(smem_addr(&rows_bar[r % kRouteWarps])), "l"(pol) : "memory");
     }
     if (round == 0) {
       // x -> fp32 in shared memory, 8 bf16 per 16-byte load, all loads of a
@@ -99,77 +108,71 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(const Rou
       }
       __syncthreads();
     }
-    // bounded wait for the round's rows (a.wait_ns of %globaltimer, about two seconds)
-    ok = __syncthreads_and(rows_wait(&rows_bar, (uint32_t)(round & 1), a.wait_ns)) != 0;   // one decision for the CTA
-    if (!ok) break;
-    // dot products: warp w takes rows w, w + 8, ... of the round
-    for (int r = warp; r < nr; r += kRouteWarps) {
-      const float4 *wrow = rows4 + (size_t)r * H4;
-      float acc[CT];
+    // bounded wait for this warp's rows of the round (a.wait_ns of
+    // %globaltimer, about two seconds), then its dot products
+    const bool mine = __all_sync(kFull, rows_wait(&rows_bar[warp], (uint32_t)(round & 1), a.wait_ns)) != 0;
+    if (mine) {
+      for (int r = warp; r < nr; r += kRouteWarps) {
+        const float4 *wrow = rows4 + (size_t)r * H4;
+        float acc[CT];
 #pragma unroll
-      for (int t = 0; t < CT; t++) acc[t] = 0.f;
-      for (int j = lane; j < H4; j += 32) {
-        const float4 w = wrow[j];
+        for (int t = 0; t < CT; t++) acc[t] = 0.f;
+        for (int j = lane; j < H4; j += 32) {
+          const float4 w = wrow[j];
 #pragma unroll
-        for (int t = 0; t < CT; t++) {
-          const float4 xv = xs4[t * H4 + j];
-          acc[t] = fmaf(w.x, xv.x, acc[t]);
-          acc[t] = fmaf(w.y, xv.y, acc[t]);
-          acc[t] = fmaf(w.z, xv.z, acc[t]);
-          acc[t] = fmaf(w.w, xv.w, acc[t]);
+          for (int t = 0; t < CT; t++) {
+            const float4 xv = xs4[t * H4 + j];
+            acc[t] = fmaf(w.x, xv.x, acc[t]);
+            acc[t] = fmaf(w.y, xv.y, acc[t]);
+            acc[t] = fmaf(w.z, xv.z, acc[t]);
+            acc[t] = fmaf(w.w, xv.w, acc[t]);
+          }
         }
-      }
-#pragma unroll
-      for (int t = 0; t < CT; t++)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(kFull, acc[t], o);
-      if (lane == 0) {
-        const int e = rb + r;
-        const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
         for (int t = 0; t < CT; t++)
-          if (t < a.C) a.logits[(size_t)t * a.E + e] = acc[t] + b;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(kFull, acc[t], o);
+        if (lane == 0) {
+          const int e = rb + r;
+          const float b = a.bias ? a.bias[e] : 0.f;
+#pragma unroll
+          for (int t = 0; t < CT; t++)
+            if (t < a.C) a.logits[(size_t)t * a.E + e] = acc[t] + b;
+        }
       }
     }
-    __syncthreads();                       // the rows buffer is refilled by the next round
+    // one decision for the CTA; the rows buffer is refilled by the next round
+    ok = __syncthreads_and(mine) != 0;
+    if (!ok) break;
   }
-  if (!ok && threadIdx.x == 0) {
-    // The round's rows did not arrive in time: flag it, count this CTA as
-    // failed for the current call, and give the copies one more bounded wait
-    // so that none is left in flight when the CTA exits.
-    atomicOr(a.flags, MOE_FLAG_TIMEOUT);
-    atomicAdd(a.timeouts, 1u);
-    rows_wait(&rows_bar, (uint32_t)(round & 1), a.wait_ns);
+  if (!ok) {
+    // Some rows of the round did not arrive in time: flag it, give each
+    // warp's copies one more bounded wait so that none is left in flight when
+    // the CTA exits, and write NaN over all this CTA's logits, so that the
+    // selection finds no expert for any token (ids -1, weights 0).
+    if (threadIdx.x == 0) atomicOr(a.flags, MOE_FLAG_TIMEOUT);
+    if (lane == 0) rows_wait(&rows_bar[warp], (uint32_t)(round & 1), a.wait_ns);
+    for (int i = threadIdx.x; i < a.C * (r1 - r0); i += blockDim.x) {
+      const int t = i / (r1 - r0), e = r0 + (i - t * (r1 - r0));
+      a.logits[(size_t)t * a.E + e] = __int_as_float(0x7FC00000);
+    }
   }
   // Every CTA takes a ticket, failed or not, so the last one always resets
-  // the counters for the next call.  The last CTA runs the top-k; if any CTA
-  // failed, the logits are incomplete and it writes ids -1 (an absent slot
-  // for moe_forward) and weights 0 instead.
-  __threadfence();
+  // the counter for the next call.  Thread 0's acquire-release add publishes
+  // this CTA's logits (ordered before it by the barrier) and, in the last
+  // CTA, makes every other CTA's visible to the selection after the barrier.
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t done = atomicAdd(a.ticket, 1u);
+    uint32_t done;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(done) : "l"(a.ticket) : "memory");
     s_last = (done == gridDim.x - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
-  const bool failed = *reinterpret_cast<volatile uint32_t *>(a.timeouts) != 0u;
-  if (failed) {
-    for (int i = threadIdx.x; i < a.C * a.k; i += blockDim.x) {
-      a.ids[i] = -1;
-      a.weights[i] = 0.f;
-    }
-  } else {
-    for (int t = 0; t < a.C; t++)
-      cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k,
-                                        a.weights + (size_t)t * a.k, tk);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    *a.ticket = 0u;
-    *a.timeouts = 0u;
-  }
+  for (int t = 0; t < a.C; t++)
+    cta_select_topk<kRouteWarps * 32>(a.logits + (size_t)t * a.E, a.E, a.k, a.ids + (size_t)t * a.k,
+                                      a.weights + (size_t)t * a.k, tk);
+  if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
 // ------------------------------------------------------------ large C

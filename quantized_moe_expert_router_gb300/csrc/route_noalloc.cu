@@ -38,7 +38,7 @@ constexpr int kNoAllocTokens = 8;
 constexpr int kNoAllocLogits = 8192;                 // floats: C * E limit
 constexpr size_t kNoAllocBytes = 256 + sizeof(float) * kNoAllocLogits;
 
-// [0, 256): uint32 completion counter, flag word, failure counter (+ padding);
+// [0, 256): uint32 completion counter, flag word, reserved word (+ padding);
 // [256, ...): logits.
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
@@ -84,7 +84,6 @@ extern "C" moe_status moe_route_noalloc(moe_layer_t L, const uint16_t *x, int C,
     a.logits = reinterpret_cast<float *>(scratch + 256);
     a.ticket = reinterpret_cast<uint32_t *>(scratch);
     a.flags = reinterpret_cast<int32_t *>(scratch + sizeof(uint32_t));
-    a.timeouts = reinterpret_cast<uint32_t *>(scratch + 2 * sizeof(uint32_t));
     a.C = C; a.E = L->cfg.num_experts; a.H = L->cfg.hidden; a.k = L->cfg.top_k;
     moe::route_wait_policy(L->cfg.flags, &a);
     const int grid = a.E < L->num_sms ? a.E : L->num_sms;

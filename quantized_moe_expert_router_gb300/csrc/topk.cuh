@@ -23,6 +23,10 @@
 // ties only make the candidate list (and the rank loop) longer.  The
 // selection is latency-bound: every step is a few warp-wide operations
 // between CTA barriers.
+//
+// A token with a NaN among its logits selects nothing: ids -1 (absent
+// slots) and weights 0.  The fused router marks the rows of a block whose
+// copies did not arrive that way.
 #pragma once
 
 #include "moe_internal.cuh"
@@ -74,9 +78,12 @@ __device__ __forceinline__ void cta_select_topk(const float *lg, int E, int k, i
   const bool part = tid < NT;
   uint32_t key[V];
   uint32_t m = 0;
+  bool nan_seen = false;
 #pragma unroll
   for (int v = 0; v < V; v++) {
-    key[v] = (part && e0 + v < E) ? order_key(__ldcg(lg + e0 + v)) : 0u;
+    const float l = (part && e0 + v < E) ? __ldcg(lg + e0 + v) : 0.f;
+    nan_seen |= l != l;
+    key[v] = (part && e0 + v < E) ? order_key(l) : 0u;
     m = max(m, key[v]);
   }
   for (int i = tid; i < kMaxExperts / 32; i += blockDim.x) s.kept[i] = 0u;
@@ -95,7 +102,14 @@ __device__ __forceinline__ void cta_select_topk(const float *lg, int E, int k, i
   if (warp < nfull && (lane & ((1 << lg_g) - 1)) == 0) s.gmax[(warp << lg_gpw) + (lane >> lg_g)] = gm;
   const uint32_t wm = __reduce_max_sync(kAll, m);
   if (lane == 0) s.wmax[warp] = wm;
-  __syncthreads();
+  if (__syncthreads_or(nan_seen)) {
+    if (tid < k) {
+      ids_out[tid] = -1;
+      w_out[tid] = 0.f;
+    }
+    __syncthreads();                             // s is reused by the next call
+    return;
+  }
   // T = k-th largest group maximum (with multiplicity): the value v with
   // #(> v) < k <= #(>= v), found by warp 0 (lane l holds groups l and l + 32
   // and counts against all groups by shuffles).  T = 0 when there are fewer

@@ -321,13 +321,15 @@ def test_forward_reads_x_written_by_the_previous_kernel(C):
     assert moe.moe_get_device_status(L.h, L.ws) == 0
 
 
-def test_router_wait_timeout_is_reported_and_recovered():
+@pytest.mark.parametrize("C", [1, 3])
+def test_router_wait_timeout_is_reported_and_recovered(C):
     # the test hook makes every router block wait for bytes that never come:
     # the bounded wait runs out (20 ms), MOE_FLAG_TIMEOUT is raised, ids come
     # back as -1 with weights 0, moe_forward then treats every slot as absent
     # (y = 0), and the same workspace and the no-alloc router work normally on
-    # the next call
-    E, k, H, I, C = 32, 4, 256, 192, 3
+    # the next call.  C = 1 takes the logits-only router, whose failed blocks
+    # mark their logits NaN for the expert kernels' own selection.
+    E, k, H, I = 32, 4, 256, 192
     good = GpuLayer(E, k, H, I, 8)
     stall = moe.Layer(E, k, H, I, 8, flags=moe.CONFIG_TEST_ROUTER_STALL)
     x_bits = gapped_tokens(0, 0, C, H, good.Wr, k)
@@ -343,7 +345,7 @@ def test_router_wait_timeout_is_reported_and_recovered():
     assert flags == moe.FLAG_TIMEOUT, f"{flags:#x}"
     oids, ow, _, oy = good.oracle(x_bits)
     for rep in range(2):                      # the workspace is as good as new
-        ids2, w2, y2 = good.run(x_bits)
+        ids2, w2, y2 = good.run(x_bits) if rep == 0 else good.run_fused(x_bits)
         assert (ids2 == oids).all()
         assert_close(y2, oy, f"after a router timeout, call {rep}")
         assert moe.moe_get_device_status(good.h, good.ws) == 0
@@ -382,6 +384,27 @@ def test_bad_and_duplicate_ids_are_flagged_and_skipped():
                             np.array([[0.25, 0.25, 0.25]]))
     assert_close(y.cpu().numpy()[1:], y1, "duplicate id")
     assert moe.moe_get_device_status(L.h, L.ws) == 0    # cleared
+
+
+def test_one_token_unsorted_bad_duplicate_and_absent_ids():
+    # a single token takes its own dispatch path: slots in any order, an id
+    # >= E and a repeated id are flagged and skipped (the repeat keeps its
+    # lowest slot), negative ids are absent without a flag
+    L = GpuLayer(32, 4, 256, 192, 2)
+    x_bits = gapped_tokens(3, 0, 1, 256, L.Wr, 4)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV)
+    y = torch.empty((1, 256), dtype=torch.float32, device=DEV)
+    cases = [([7, 40, 2, 7], [0.3, 0.1, 0.2, 0.4], [7, 2], [0.3, 0.2],
+              moe.FLAG_BAD_EXPERT_ID | moe.FLAG_DUPLICATE_ID),
+             ([-1, 5, -1, 1], [0.5, 0.25, 0.5, 0.75], [5, 1], [0.25, 0.75], 0),
+             ([31, 0, 16, 8], [0.25, 0.125, 0.5, 0.125], [31, 0, 16, 8], [0.25, 0.125, 0.5, 0.125], 0)]
+    for ids_l, w_l, oids, ow, want in cases:
+        ids = torch.tensor([ids_l], dtype=torch.int32, device=DEV)
+        w = torch.tensor([w_l], dtype=torch.float32, device=DEV)
+        moe.moe_forward(L.h, x, 1, ids, w, L.packed, y, L.ws)
+        assert moe.moe_get_device_status(L.h, L.ws) == want, ids_l
+        yo = oracle.moe_forward(L.host_weights(range(32)), x_bits, np.array([oids], np.int32), np.array([ow]))
+        assert_close(y.cpu().numpy(), yo, f"one token, ids {ids_l}")
 
 
 def test_grouped_bad_duplicate_and_absent_ids():
