@@ -21,6 +21,7 @@ constexpr int kCombineThreads = 64;
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
   __shared__ int order[kGemvTokens][kMaxTopK];
   __shared__ int cnt[kGemvTokens];
+  __shared__ int s_live;                        // 0: instruction warm-up pass, 1: the sums
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int t = warp; t < a.C; t += kCombineThreads / 32) {
     const int e = lane < a.k ? a.ids[(size_t)t * a.k + lane] : -1;
@@ -41,30 +42,46 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
     if (valid) order[t][rank] = t * a.k + lane;
     if (lane == 0) cnt[t] = __popc(vm);
   }
+  // The sums run twice through the same instructions: first before the wait
+  // with every memory access predicated off (the down grid is still running;
+  // this only brings the code into the SM's instruction cache), then for
+  // real.  The pass flag is read from shared memory in the loop, so the
+  // compiler cannot split the loop into two copies.
+  if (tid == 0) s_live = 0;
   __syncthreads();
-  pdl_wait();                                   // ypair comes from the down kernel
-  if (blockIdx.x == 0)                          // the down kernel has read every |h| maximum
-    for (int i = tid; i < a.C * a.k; i += blockDim.x) a.hamax[i] = 0u;
   const int H4 = a.H / 4;
-  for (int it = blockIdx.x * blockDim.x + tid; it < a.C * H4; it += gridDim.x * blockDim.x) {
-    const int t = it / H4, c4 = it - t * H4;
-    const int n = cnt[t];
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    // all loads of a batch in flight together, then summed in slot order
-    for (int j0 = 0; j0 < n; j0 += kCombineBatch) {
-      float4 v[kCombineBatch];
+#pragma unroll 1
+  for (int pass = 0; pass < 2; pass++) {
+    if (pass == 1) {
+      __syncthreads();                          // every thread is done with the warm-up pass
+      pdl_wait();                               // ypair comes from the down kernel
+      if (blockIdx.x == 0)                      // the down kernel has read every |h| maximum
+        for (int i = tid; i < a.C * a.k; i += blockDim.x) a.hamax[i] = 0u;
+      if (tid == 0) s_live = 1;
+      __syncthreads();
+    }
+    for (int it = blockIdx.x * blockDim.x + tid; it < a.C * H4; it += gridDim.x * blockDim.x) {
+      const bool live = *reinterpret_cast<volatile int *>(&s_live) != 0;
+      const int t = it / H4, c4 = it - t * H4;
+      const int n = cnt[t];
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      // all loads of a batch in flight together, then summed in slot order
+      for (int j0 = 0; j0 < n; j0 += kCombineBatch) {
+        float4 v[kCombineBatch];
 #pragma unroll
-      for (int j = 0; j < kCombineBatch; j++)
-        v[j] = j0 + j < n ? __ldcg(reinterpret_cast<const float4 *>(a.ypair + (size_t)order[t][j0 + j] * a.H) + c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < kCombineBatch; j++)
+          v[j] = live && j0 + j < n
+                     ? __ldcg(reinterpret_cast<const float4 *>(a.ypair + (size_t)order[t][j0 + j] * a.H) + c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < kCombineBatch; j++) {
-        if (j0 + j < n) {
-          s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
+        for (int j = 0; j < kCombineBatch; j++) {
+          if (j0 + j < n) {
+            s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
+          }
         }
       }
+      if (live) reinterpret_cast<float4 *>(a.y + (size_t)t * a.H)[c4] = s;
     }
-    reinterpret_cast<float4 *>(a.y + (size_t)t * a.H)[c4] = s;
   }
 }
 
