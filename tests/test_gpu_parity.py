@@ -358,6 +358,26 @@ def test_router_wait_timeout_is_reported_and_recovered(C):
     assert (ids.cpu().numpy() == oids).all()
 
 
+@pytest.mark.parametrize("C,nan_token", [(3, 1), (12, 9)])
+def test_nan_token_selects_nothing(C, nan_token):
+    # a token whose router logits include a NaN (here from one NaN element of
+    # its x) selects no expert: ids -1, weights 0, output 0, with no flag; the
+    # other tokens of the call are unaffected (the fused router for C <= 8,
+    # the tiled router and the per-token top-k above)
+    L = GpuLayer(32, 4, 256, 192, 16)
+    x_bits = gapped_tokens(7, 0, C, 256, L.Wr, 4)
+    bad = x_bits.copy()
+    bad[nan_token, 17] = 0x7FC0                  # a bf16 quiet NaN
+    ids, w, y = L.run_fused(bad)
+    assert moe.moe_get_device_status(L.h, L.ws) == 0
+    assert (ids[nan_token] == -1).all() and (w[nan_token] == 0).all() and (y[nan_token] == 0).all()
+    keep = [t for t in range(C) if t != nan_token]
+    oids, ow, _, oy = L.oracle(x_bits[keep])
+    assert (ids[keep] == oids).all()
+    np.testing.assert_allclose(w[keep], ow, rtol=2e-5, atol=1e-7)
+    assert_close(y[keep], oy, f"tokens beside a NaN token, C={C}")
+
+
 def test_forward_is_deterministic():
     L = GpuLayer(32, 4, 256, 192, 8)
     x = gapped_tokens(0, 0, 8, 256, L.Wr, 4)
